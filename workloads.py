@@ -1,0 +1,269 @@
+"""Seeded synthetic inputs for the paged KV-cache decode path.
+
+Both the GPU library (through the tests and the benchmark) and the CPU oracle
+consume what this module makes; it holds none of the method's arithmetic.  It
+draws random numbers and lays out the caller-side bookkeeping a block manager
+would hold: context lengths, a random placement of each sequence's logical blocks
+in the physical pool, block tables, the slot of each new token, and the
+copy-on-write pairs.
+
+Workloads (shapes and distributions of the benchmark configurations):
+  tiny    4 sequences, context lengths {1, 17, 40, 100}, 2 query / 2 kv heads,
+          head_dim 64, block size 16, pool of 32 blocks, scale 1/8.
+  mha13b  Llama-2-13B-shaped layer: 64 sequences, 40 / 40 heads, head_dim 128,
+          block size 16, context lengths uniform in [200, 2048].
+  gqa70b  Llama-3-70B-shaped layer: 20 sequences of 8000 tokens, 64 / 8 heads,
+          head_dim 128, block size 16.
+  prefix  50 sequences sharing one 2000-token prefix (the same 125 physical blocks)
+          plus 64..512 own tokens each, 32 / 8 heads, head_dim 128, block size 16,
+          one copy-on-write block pair per sequence.
+  int8    Llama-3-8B-shaped layer with an int8 cache: 256 sequences, 32 / 8 heads,
+          head_dim 128, block size 32, context lengths log-uniform in [128, 32768].
+All values (queries, cached keys and values, the new token's key and value) are
+N(0, 1) rounded to bf16.  context_lens count the token appended in this step: the
+new token sits at position context_len - 1.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+BF16_NAN_BITS = 0x7FC0
+
+
+@dataclass
+class PagedCase:
+    name: str
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    N: int
+    M: int
+    kv_dtype: str  # "bf16" or "int8"
+    scale: float
+    q: torch.Tensor  # [S][Hq][D] bf16
+    k_pool: torch.Tensor  # [N][Hkv][bs][D] bf16 (int8 workloads: the bf16 source to quantise)
+    v_pool: torch.Tensor
+    block_tables: torch.Tensor  # [S][M] int32 (table used by this step's decode)
+    context_lens: torch.Tensor  # [S] int32, including the new token
+    new_key: torch.Tensor  # [S][Hkv][D] bf16, the token at position context_len - 1
+    new_value: torch.Tensor
+    slot_mapping: torch.Tensor  # [S] int64, slot of the new token
+    cow_pairs: torch.Tensor  # [n][2] int64 (src, dst) physical blocks; n may be 0
+    shared_prefix_blocks: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    def to(self, device) -> "PagedCase":
+        moved = {}
+        for k, v in self.__dict__.items():
+            moved[k] = v.to(device) if isinstance(v, torch.Tensor) else v
+        return PagedCase(**moved)
+
+
+def _gen(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _randn_bf16(shape, gen, device) -> torch.Tensor:
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def blocks_needed(ctx: int, bs: int) -> int:
+    return (ctx + bs - 1) // bs
+
+
+def build_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, context_lens,
+               seed: int, kv_dtype: str = "bf16", pool_blocks: int | None = None,
+               prefix_tokens: int = 0, cow: bool = False, poison: bool = True,
+               device="cpu", scale: float | None = None) -> PagedCase:
+    """Make one seeded paged-decode case.
+
+    Physical blocks are drawn from a random permutation of the pool; with
+    ``prefix_tokens`` > 0 the first prefix_tokens // bs logical blocks of every
+    sequence point at the same physical blocks.  With ``cow`` each sequence's
+    last logical block gets a (src, dst) copy-on-write pair: the cache content is
+    written into src, the decode table already points at dst.  With ``poison``
+    every slot that holds no valid token is filled with bf16 NaN, so a kernel that
+    reads past a context shows up in the results.
+    """
+    meta_gen = _gen(seed)  # small metadata always on the CPU generator
+    ctx = torch.as_tensor(context_lens, dtype=torch.int64).clone()
+    assert ctx.numel() == S and int(ctx.min()) >= 0
+    if prefix_tokens:
+        assert prefix_tokens % bs == 0 and int(ctx.min()) > prefix_tokens
+    n_shared = prefix_tokens // bs
+    nblk = [blocks_needed(int(c), bs) for c in ctx]
+    M = max(1, max(nblk))
+    private = [nb - n_shared for nb in nblk]
+    n_cow = S if cow else 0
+    used = n_shared + sum(private) + n_cow
+    N = pool_blocks if pool_blocks is not None else used
+    assert N >= used, f"pool of {N} blocks cannot hold {used}"
+    perm = torch.randperm(N, generator=meta_gen).tolist()
+    nxt = 0
+    shared_ids = perm[nxt:nxt + n_shared]
+    nxt += n_shared
+    tables = torch.zeros((S, M), dtype=torch.int32)  # padding entries: block 0
+    content_tables = torch.zeros((S, M), dtype=torch.int32)
+    cow_pairs = []
+    for s in range(S):
+        own = perm[nxt:nxt + private[s]]
+        nxt += private[s]
+        row = shared_ids + own
+        if row:
+            tables[s, : len(row)] = torch.tensor(row, dtype=torch.int32)
+            content_tables[s, : len(row)] = torch.tensor(row, dtype=torch.int32)
+        if cow and nblk[s] > 0:
+            dst = perm[nxt]
+            nxt += 1
+            src = row[-1]
+            cow_pairs.append((src, dst))
+            tables[s, nblk[s] - 1] = dst
+    cow_t = torch.tensor(cow_pairs, dtype=torch.int64).reshape(-1, 2)
+
+    big = _gen(seed + 1, device)
+    q = _randn_bf16((S, Hq, D), big, device)
+    k_pool = _randn_bf16((N, Hkv, bs, D), big, device)
+    v_pool = _randn_bf16((N, Hkv, bs, D), big, device)
+    new_key = _randn_bf16((S, Hkv, D), big, device)
+    new_value = _randn_bf16((S, Hkv, D), big, device)
+
+    # slot of the new token (position ctx - 1) through the decode-time table
+    slots = torch.full((S,), -1, dtype=torch.int64)
+    for s in range(S):
+        c = int(ctx[s])
+        if c > 0:
+            pos = c - 1
+            slots[s] = int(tables[s, pos // bs]) * bs + pos % bs
+
+    if poison:
+        valid = valid_slot_mask(content_tables, ctx - 1, bs, N)  # tokens present before the append
+        bad = ~valid.to(device)
+        nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
+        for pool in (k_pool, v_pool):
+            view = pool.permute(0, 2, 1, 3)  # [N][bs][Hkv][D]
+            view[bad] = nan
+    return PagedCase(name=name, S=S, Hq=Hq, Hkv=Hkv, D=D, bs=bs, N=N, M=M, kv_dtype=kv_dtype,
+                     scale=scale if scale is not None else 1.0 / math.sqrt(D),
+                     q=q, k_pool=k_pool, v_pool=v_pool, block_tables=tables,
+                     context_lens=ctx.to(torch.int32), new_key=new_key, new_value=new_value,
+                     slot_mapping=slots, cow_pairs=cow_t, shared_prefix_blocks=n_shared,
+                     meta={"seed": seed, "content_tables": content_tables,
+                           "prefix_tokens": prefix_tokens})
+
+
+def valid_slot_mask(tables: torch.Tensor, lengths: torch.Tensor, bs: int, N: int) -> torch.Tensor:
+    """Boolean [N][bs]: True where a slot holds one of the first lengths[s] tokens of some
+    sequence s, reached through tables[s]."""
+    mask = torch.zeros((N, bs), dtype=torch.bool)
+    for s in range(tables.shape[0]):
+        n = int(lengths[s])
+        if n <= 0:
+            continue
+        pos = torch.arange(n)
+        blocks = tables[s, pos // bs].long()
+        mask[blocks, pos % bs] = True
+    return mask
+
+
+# --------------------------------------------------------------------------- configs
+def tiny(seed: int = 0, device="cpu", poison=True) -> PagedCase:
+    return build_case("tiny", S=4, Hq=2, Hkv=2, D=64, bs=16, context_lens=[1, 17, 40, 100],
+                      seed=seed, pool_blocks=32, poison=poison, device=device, scale=1.0 / 8.0)
+
+
+def mha13b(seed: int = 1, device="cpu", poison=False) -> PagedCase:
+    lens = torch.randint(200, 2049, (64,), generator=_gen(seed + 100)).tolist()
+    return build_case("mha13b", S=64, Hq=40, Hkv=40, D=128, bs=16, context_lens=lens,
+                      seed=seed, poison=poison, device=device)
+
+
+def gqa70b(seed: int = 2, device="cpu", poison=False) -> PagedCase:
+    return build_case("gqa70b", S=20, Hq=64, Hkv=8, D=128, bs=16, context_lens=[8000] * 20,
+                      seed=seed, pool_blocks=10000, poison=poison, device=device)
+
+
+def prefix(seed: int = 3, device="cpu", poison=False) -> PagedCase:
+    own = torch.randint(64, 513, (50,), generator=_gen(seed + 100))
+    lens = (2000 + own).tolist()
+    return build_case("prefix", S=50, Hq=32, Hkv=8, D=128, bs=16, context_lens=lens, seed=seed,
+                      prefix_tokens=2000, cow=True, poison=poison, device=device)
+
+
+def int8_lengths(S: int, seed: int, lo: int = 128, hi: int = 32768) -> list[int]:
+    u = torch.rand((S,), generator=_gen(seed + 100), dtype=torch.float64)
+    lens = torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo))).round().long()
+    return lens.clamp(lo, hi).tolist()
+
+
+def int8(seed: int = 4, device="cpu", poison=False) -> PagedCase:
+    return build_case("int8", S=256, Hq=32, Hkv=8, D=128, bs=32, context_lens=int8_lengths(256, seed),
+                      seed=seed, kv_dtype="int8", poison=poison, device=device)
+
+
+CONFIGS = {"tiny": tiny, "mha13b": mha13b, "gqa70b": gqa70b, "prefix": prefix, "int8": int8}
+
+
+# ------------------------------------------------------------------ byte accounting
+def kv_cache_bytes(layers: int, heads: int, head_dim: int, tokens: int, batch: int,
+                   bytes_per_value: float) -> float:
+    """KV-cache size: 2 (K and V) x layers x heads x head_dim x tokens x batch x bytes
+    (ia-vox-magazine KV-cache article, "Pourquoi le KV cache domine la consommation
+    memoire" and its FAQ)."""
+    return 2.0 * layers * heads * head_dim * tokens * batch * bytes_per_value
+
+
+def decode_algorithmic_bytes(case: PagedCase, unique_blocks: bool = False) -> int:
+    """Bytes one decode call must move at minimum: every cached K and V element of every
+    sequence's context once (int8: plus one fp32 scale per token, kv head and K/V), the
+    queries, the outputs, the block-table entries and the context lengths.  With
+    ``unique_blocks`` a physical block shared by several tables counts once."""
+    e = 1 if case.kv_dtype == "int8" else 2
+    ctx = case.context_lens.long().cpu()
+    per_token = case.Hkv * case.D * e * 2 + (case.Hkv * 2 * 4 if case.kv_dtype == "int8" else 0)
+    if unique_blocks:
+        seen = {}
+        tabs = case.block_tables.cpu()
+        for s in range(case.S):
+            n = int(ctx[s])
+            nb = blocks_needed(n, case.bs)
+            for j in range(nb):
+                b = int(tabs[s, j])
+                fill = min(case.bs, n - j * case.bs)
+                seen[b] = max(seen.get(b, 0), fill)
+        kv = sum(seen.values()) * per_token
+    else:
+        kv = int(ctx.sum()) * per_token
+    qo = 2 * case.S * case.Hq * case.D * 2
+    tables = sum(blocks_needed(int(c), case.bs) for c in ctx) * 4 + case.S * 4
+    return int(kv + qo + tables)
+
+
+def append_algorithmic_bytes(case: PagedCase) -> int:
+    """Bytes of one append of case.S new tokens: read K and V rows, write them (int8: codes
+    and one fp32 scale per row), plus the slot numbers."""
+    rows = case.S * case.Hkv
+    if case.kv_dtype == "int8":
+        return rows * 2 * (case.D * 2 + case.D + 4) + case.S * 8
+    return rows * 2 * case.D * 2 * 2 + case.S * 8
+
+
+def fragmentation(case: PagedCase, max_len: int) -> dict:
+    """Wasted KV capacity under contiguous max-length reservation versus paging (the pages'
+    internal-fragmentation comparison): the fraction of reserved token slots that hold no
+    token."""
+    ctx = case.context_lens.long().cpu()
+    used = int(ctx.sum())
+    contiguous = case.S * max_len
+    paged = sum(blocks_needed(int(c), case.bs) for c in ctx) * case.bs
+    return {"contiguous_waste": 1.0 - used / contiguous, "paged_waste": 1.0 - used / paged}
