@@ -1,0 +1,484 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = the whole hot path of one decode step of one layer over one batch:
+copy-on-write block copies (prefix workload), append (bf16) or quantise-append
+(int8) of each sequence's new token, then paged decode attention (+ the partition
+merge).  Inputs are seeded and synthetic (workloads.py) and live in HBM before the
+timed region; K/V pools of every workload but `tiny` and `prefix` exceed the 126 MB
+L2, and those two get an L2 flush before every timed step.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job effective bandwidth: the
+algorithmic bytes of all steps on all ranks / the slowest rank's time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mha13b] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64 C, all host cores) on a bounded sample
+of the same workload: the comparison baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "pa_decode effective KV HBM GB/s (% of GB300 peak) and decode tokens/s per layer"
+UNIT = "GB/s"
+DESCRIPTIONS = {
+    "tiny": "tiny paged decode: 4 seqs, ctx {1,17,40,100}, 2/2 heads, head_dim 64, block 16",
+    "mha13b": "Llama-2-13B-shaped MHA layer decode: 64 seqs, 40/40 heads, head_dim 128, block 16, "
+              "ctx U[200,2048], 1-token append per seq",
+    "gqa70b": "Llama-3-70B-shaped GQA layer decode: 20 seqs x 8000 tokens, 64/8 heads, head_dim 128, block 16",
+    "prefix": "prefix-shared decode: 50 seqs sharing a 2000-token prefix + U[64,512] own tokens, "
+              "32/8 heads, head_dim 128, block 16, COW copy of each seq's last block",
+    "int8": "int8 KV decode: Llama-3-8B shape 32/8 heads, head_dim 128, block 32, 256 seqs, "
+            "ctx log-uniform [128,32768], 1-token quantise+append per seq",
+}
+FLUSH_L2 = {"tiny", "prefix"}
+L2_BYTES = 126 * 1024 * 1024
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode launch, from an ncu capture
+# of the kernel source with this sha256 (null once the source changes).
+NCU_TRAFFIC = {}
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def decode_source_hash() -> str:
+    src = ROOT / "paged_kv_cache_197_gb300" / "csrc" / "pa_decode.cu"
+    return hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ clock sampler
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self, t0: float, t1: float) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r for ts, r in self.rows if t0 <= ts <= t1] or [r for _, r in self.rows]
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(num(r[2]) for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------- steps
+class Step:
+    """The device buffers and the calls of one decode step of one workload."""
+
+    def __init__(self, case: workloads.PagedCase, device, stream):
+        import paged_kv_cache_197_gb300 as pa
+
+        self.pa = pa
+        self.case = case
+        self.dev = device
+        self.stream = stream
+        c = case
+        self.int8 = c.kv_dtype == "int8"
+        if self.int8:
+            N, Hkv, bs, D = c.k_pool.shape
+            self.k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.int8, device=device)
+            self.v_cache = torch.empty_like(self.k_cache)
+            self.k_scale = torch.empty((N, Hkv, bs), dtype=torch.float32, device=device)
+            self.v_scale = torch.empty_like(self.k_scale)
+            slots = torch.arange(N * bs, dtype=torch.int64, device=device)
+            rows = lambda p: p.permute(0, 2, 1, 3).reshape(N * bs, Hkv, D).contiguous()  # noqa: E731
+            pa.pa_quantize_kv(rows(c.k_pool), rows(c.v_pool), self.k_cache, self.v_cache,
+                              self.k_scale, self.v_scale, slots, stream=stream)
+            torch.cuda.synchronize(device)
+        else:
+            self.k_cache, self.v_cache = c.k_pool, c.v_pool
+            self.k_scale = self.v_scale = None
+        self.max_ctx = int(c.context_lens.max())
+        self.out = torch.empty_like(c.q)
+        self.ws = pa.decode_workspace(c.q, self.k_cache, self.max_ctx)
+        self.flag = torch.zeros(1, dtype=torch.int32, device=device)
+        self.cow = c.cow_pairs.cpu()
+        plan_parts = math.ceil(self.max_ctx / 512)
+        self.launches = (1 + 1 + (1 if plan_parts > 1 else 0)
+                         + (math.ceil(self.cow.shape[0] / 256) if self.cow.shape[0] else 0))
+
+    def write_cache(self, new_key, new_value, slots):
+        if self.cow.shape[0]:
+            self.pa.pa_copy_blocks(self.k_cache, self.v_cache, self.cow, k_scale=self.k_scale,
+                                   v_scale=self.v_scale, stream=self.stream)
+        if self.int8:
+            self.pa.pa_quantize_kv(new_key, new_value, self.k_cache, self.v_cache, self.k_scale,
+                                   self.v_scale, slots, err_flag=self.flag, stream=self.stream)
+        else:
+            self.pa.pa_reshape_and_cache(new_key, new_value, self.k_cache, self.v_cache, slots,
+                                         err_flag=self.flag, stream=self.stream)
+
+    def decode(self, q, tables, lens, out):
+        self.pa.pa_decode(out, q, self.k_cache, self.v_cache, tables, lens, self.case.scale,
+                          self.max_ctx, workspace=self.ws, k_scale=self.k_scale,
+                          v_scale=self.v_scale, err_flag=self.flag, stream=self.stream)
+
+    def run(self, dec_events=None):
+        c = self.case
+        self.write_cache(c.new_key, c.new_value, c.slot_mapping)
+        if dec_events is not None:
+            dec_events[0].record(self.stream)
+        self.decode(c.q, c.block_tables, c.context_lens, self.out)
+        if dec_events is not None:
+            dec_events[1].record(self.stream)
+
+
+def step_bytes(case) -> dict:
+    dec = workloads.decode_algorithmic_bytes(case)
+    app = workloads.append_algorithmic_bytes(case)
+    cow = 0
+    if case.cow_pairs.shape[0]:
+        per_block = case.Hkv * case.bs * case.D * (1 if case.kv_dtype == "int8" else 2) * 2
+        cow = case.cow_pairs.shape[0] * per_block * 2
+    return {"decode": dec, "append": app, "cow": cow, "total": dec + app + cow,
+            "decode_unique": workloads.decode_algorithmic_bytes(case, unique_blocks=True)}
+
+
+# ------------------------------------------------------------------- our timing
+def run_ours(args, rank, world, device) -> dict | None:
+    stream = torch.cuda.Stream(device)
+    maker = workloads.CONFIGS[args.config]
+    with torch.cuda.stream(stream):
+        case = maker(seed=args.seed + 1000 * rank, device=device, poison=False)
+        torch.cuda.synchronize(device)
+        step = Step(case, device, stream)
+    nbytes = step_bytes(case)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) \
+        if args.config in FLUSH_L2 else None
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    # warm-up: at least W steps and at least half a second, so the clocks settle
+    t_w = time.time()
+    n = 0
+    while n < args.warmup or time.time() - t_w < 0.5:
+        with torch.cuda.stream(stream):
+            step.run()
+        n += 1
+        if n % 50 == 0:
+            torch.cuda.synchronize(device)
+    barrier()
+    t0 = time.time()
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    if flush is None:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            step.run(dec_ev[i])
+        end.record(stream)
+        barrier()
+        total_ms = start.elapsed_time(end)
+    else:  # flush L2 before each step, outside the timed spans
+        spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(args.steps)]
+        for i in range(args.steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(float(i))
+            spans[i][0].record(stream)
+            step.run(dec_ev[i])
+            spans[i][1].record(stream)
+        barrier()
+        total_ms = sum(a.elapsed_time(b) for a, b in spans)
+    t1 = time.time()
+    clocks = sampler.stop(t_w, t1)
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    assert int(step.flag.item()) == 0, f"kernel error flag {int(step.flag.item())}"
+
+    # slowest rank sets the job time
+    t = torch.tensor([total_ms, statistics.mean(dec_ms)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms, dec_mean_ms = float(t[0]), float(t[1])
+    ms_per_step = total_ms / args.steps
+
+    e2e = run_e2e(args, step, case, device, stream, world)
+    if rank != 0:
+        return None
+
+    peaks = measured_peaks()
+    achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
+    src_hash = decode_source_hash()
+    traffic = NCU_TRAFFIC.get((args.config, src_hash))
+    value = nbytes["total"] * world / (ms_per_step * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8" if case.kv_dtype == "int8" else "bf16", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": DESCRIPTIONS[args.config], "name": args.config, "S": case.S,
+                   "Hq": case.Hq, "Hkv": case.Hkv, "head_dim": case.D, "block_size": case.bs,
+                   "pool_blocks": case.N, "total_context_tokens": int(case.context_lens.sum()),
+                   "parallelism": f"replicas x{world} (independent sequence shards)",
+                   "l2": "flushed before each step" if flush is not None else
+                         "K/V pools far larger than L2 (no flush needed)",
+                   "bytes_per_step": nbytes},
+        "tokens_per_s_per_layer": round(case.S * world / (ms_per_step * 1e-3), 1),
+        "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "kernel": "pa_decode call (decode + partition merge)",
+                     "peak_source": peaks["source"], "mean_decode_us": round(dec_mean_ms * 1e3, 2)},
+        "e2e": e2e,
+        "gpu_launches": step.launches * args.steps,
+        "clocks": clocks,
+        "kernel_source": src_hash,
+    }
+    if args.config == "prefix":
+        res["roofline"]["achieved_unique_bytes"] = round(
+            nbytes["decode_unique"] / (dec_mean_ms * 1e-3) / 1e9, 1)
+    if not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(args, case, step, budget_s=args.cpu_seconds)
+    return res
+
+
+def run_e2e(args, step, case, device, stream, world) -> dict:
+    """Same step through the public API with the step's inputs in pinned host memory:
+    host->device copies of queries, new K/V, slots, tables and lengths, and the
+    device->host copy of the output, all inside the timed region."""
+    host = {k: getattr(case, k).cpu().pin_memory() for k in
+            ("q", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens")}
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out_host = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    steps = max(3, min(args.steps, 200))
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        step.write_cache(dev["new_key"], dev["new_value"], dev["slot_mapping"])
+        step.decode(dev["q"], dev["block_tables"], dev["context_lens"], step.out)
+        out_host.copy_(step.out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / steps
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t[0])
+    total = step_bytes(case)["total"]
+    return {"value": round(total * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
+            "steps": steps}
+
+
+# ----------------------------------------------------------------- CPU baseline
+def oracle_sample_inputs(case, step=None):
+    """Host copies of the caches (bf16 bits, or int8 codes and scales) for the oracle."""
+    import numpy as np
+
+    def bits(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    if case.kv_dtype == "int8":
+        import oracle
+
+        orc = oracle.load()
+        kc, ks = orc.quantize_pool(bits(case.k_pool))
+        vc, vs = orc.quantize_pool(bits(case.v_pool))
+        return bits(case.q), kc, vc, ks, vs
+    return bits(case.q), bits(case.k_pool), bits(case.v_pool), None, None
+
+
+def time_oracle(case, inputs, budget_s: float) -> dict:
+    """Oracle decode over the first n sequences, n grown until the run takes ~budget_s."""
+    import numpy as np
+
+    import oracle
+
+    orc = oracle.load()
+    q, kc, vc, ks, vs = inputs
+    tables = case.block_tables.cpu().numpy()
+    lens = case.context_lens.cpu().numpy()
+    n, elapsed = 1, 0.0
+    while True:
+        t0 = time.perf_counter()
+        orc.paged_attention(np.ascontiguousarray(q[:n]), kc, vc, np.ascontiguousarray(tables[:n]),
+                            np.ascontiguousarray(lens[:n]), case.scale, k_scale=ks, v_scale=vs)
+        elapsed = time.perf_counter() - t0
+        if elapsed >= budget_s / 4 or n >= case.S:
+            break
+        n = min(case.S, max(n + 1, int(n * min(8.0, (budget_s / 4) / max(elapsed, 1e-3)))))
+    sub = workloads.PagedCase(**{**case.__dict__})
+    sub.S = n
+    sub.context_lens = case.context_lens[:n].cpu()
+    sub.q = case.q[:n]
+    sub.block_tables = case.block_tables[:n].cpu()
+    nbytes = workloads.decode_algorithmic_bytes(sub)
+    return {"value": round(nbytes / elapsed / 1e9, 4), "unit": UNIT, "cores": orc.num_threads,
+            "kind": "oracle", "seconds": round(elapsed, 3),
+            "sample": f"decode of the first {n} of {case.S} sequences "
+                      f"({int(sub.context_lens.sum())} context tokens), fp64 C oracle, "
+                      f"caches resident in host memory"}
+
+
+def cpu_baseline(args, case, step, budget_s=20.0) -> dict:
+    inputs = oracle_sample_inputs(case, step)
+    return time_oracle(case, inputs, budget_s)
+
+
+def run_reference(args, rank, world) -> dict | None:
+    """The oracle as it stands, on the host cores, over a fixed sample of the workload.
+
+    The sample (the first n sequences) is sized once so that W + K steps take about
+    two minutes in all, at most 3 s a step."""
+    import numpy as np
+
+    import oracle
+
+    if rank != 0:
+        return None
+    case = workloads.CONFIGS[args.config](seed=args.seed, device="cpu", poison=False)
+    inputs = oracle_sample_inputs(case)
+    per_step = min(3.0, 120.0 / (args.warmup + args.steps))
+    info = time_oracle(case, inputs, budget_s=4 * per_step)  # calibrates n
+    n = int(info["sample"].split()[4])
+    orc = oracle.load()
+    q, kc, vc, ks, vs = inputs
+    qn = np.ascontiguousarray(q[:n])
+    tables = np.ascontiguousarray(case.block_tables[:n].numpy())
+    lens = np.ascontiguousarray(case.context_lens[:n].numpy())
+    sub = workloads.PagedCase(**{**case.__dict__})
+    sub.S, sub.q, sub.block_tables, sub.context_lens = n, case.q[:n], case.block_tables[:n], case.context_lens[:n]
+    nbytes = workloads.decode_algorithmic_bytes(sub)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        orc.paged_attention(qn, kc, vc, tables, lens, case.scale, k_scale=ks, v_scale=vs)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms_per_step = 1e3 * sum(times) / len(times)
+    value = round(nbytes / (ms_per_step * 1e-3) / 1e9, 4)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1))",
+            "config": {"workload": DESCRIPTIONS[args.config], "name": args.config},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="mha13b", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    try:
+        res = run_ours(args, rank, world, device)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

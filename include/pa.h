@@ -1,0 +1,178 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache decode library (GB300, sm_103a).
+ *
+ * The library implements the decode hot path of paged attention over a
+ * block-paged KV cache:
+ *   - the KV cache is cut into fixed-size physical blocks of 16 or 32 tokens and a
+ *     per-sequence block table maps logical blocks to physical ones
+ *     (gotburnout.io "PagedAttention & Gestion du KV-Cache", section 2 block-table
+ *     figure; ia-vox-magazine KV-cache article, "PagedAttention : la revolution de
+ *     l'allocation memoire"; deeplearn.tn KV-cache article, "Le Paged Attention");
+ *   - each decode step appends the new token's key and value to its sequence's
+ *     cache (blog.fabienvernieres.com "Cache KV en production", "Un cache par
+ *     requete, une memoire commune") and attends from the new token's query over
+ *     the cached keys and values (same page, opening section; deeplearn.tn, "Le
+ *     compromis fondamental de l'inference": only the new query is needed);
+ *   - sequences sharing a prefix point at the same physical blocks and a block is
+ *     copied only when a sequence starts writing its own tokens (gotburnout.io,
+ *     section 3.01 "Partage de prefixes (Prefix Caching / Copy-on-Write)");
+ *   - an optional int8 cache with a scale recomputed for every token
+ *     (ia-vox-magazine, "Quantization du KV cache").
+ *
+ * Conventions for every call:
+ *   - Tensors are dense, row-major, and 16-byte aligned.  Device pointers are
+ *     owned by the caller; the library allocates nothing and keeps no pointer
+ *     after a call returns.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  A call returns after its kernels are queued.
+ *   - pa_bf16 is a raw bfloat16 bit pattern.
+ *   - Cache layout, K and V alike: [N blocks][Hkv][bs][D]; int8 scales:
+ *     [N][Hkv][bs] fp32, one per (token slot, kv head).
+ *   - Query head h reads kv head h / (Hq / Hkv) (grouped-query attention).
+ *   - Arguments are checked on the host before anything is queued; a failed
+ *     check returns a status other than PA_OK and queues nothing.  Values that
+ *     live in device memory (slots, block ids, context lengths) are checked by
+ *     the kernels: an offending entry is skipped (its rows are neither read nor
+ *     written) and a PA_FLAG_* bit is OR-ed into *err_flag when err_flag is not
+ *     NULL.  The caller reads err_flag after synchronising.
+ *   - pa_last_error_string() describes the last failure of the calling thread.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pa_bf16;
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad alignment, shape mismatch */
+    PA_ERR_UNSUPPORTED = 2, /* head_dim, block size or kv dtype not compiled in */
+    PA_ERR_OUT_OF_RANGE = 3, /* a host-visible index (block id, length) out of range */
+    PA_ERR_CUDA = 4          /* a CUDA launch failed; see pa_last_error_string() */
+} pa_status;
+
+enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1 };
+
+/* Bits OR-ed into *err_flag by the kernels. */
+enum {
+    PA_FLAG_SLOT_OUT_OF_RANGE = 1,    /* slot_mapping[t] >= N * bs: token not written   */
+    PA_FLAG_BLOCK_OUT_OF_RANGE = 2,   /* block_tables entry outside [0, N): block skipped */
+    PA_FLAG_CONTEXT_OUT_OF_RANGE = 4  /* context_lens[s] < 0, > M * bs or > max_context_len:
+                                         clamped to the valid range                        */
+};
+
+/* Version of this ABI (bumped on any signature change). */
+int pa_version(void);
+
+/* Static text for a status code. */
+const char *pa_status_string(pa_status status);
+
+/* Message of the last failed call on this thread ("" when none). */
+const char *pa_last_error_string(void);
+
+/*
+ * Append (reshape_and_cache): write the key and value rows of T new tokens into
+ * their slots of a bf16 cache.
+ *   key, value      [T][Hkv][D] bf16, device.
+ *   k_cache,v_cache [N][Hkv][bs][D] bf16, device; row (slot / bs, h, slot % bs)
+ *                   receives key[t][h] (resp. value[t][h]).
+ *   slot_mapping    [T] int64, device: slot = physical block * bs + offset, i.e.
+ *                   block_table[p / bs] * bs + p % bs for logical position p
+ *                   (gotburnout.io block-table figure).  A negative slot marks a
+ *                   padding token and is skipped.  slot >= N * bs: skipped and
+ *                   PA_FLAG_SLOT_OUT_OF_RANGE raised.
+ *   D in {64, 128}, bs in {16, 32}.  T == 0 is a no-op.
+ * Two tokens with the same slot in one call race; the caller must not do that.
+ */
+pa_status pa_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value, pa_bf16 *k_cache,
+                               pa_bf16 *v_cache, const int64_t *slot_mapping, int T, int Hkv,
+                               int D, int bs, int N, int *err_flag, void *stream);
+
+/*
+ * Quantise-and-append into an int8 cache with a dynamic per-(token, kv head)
+ * scale (ia-vox-magazine, "Quantization du KV cache": the scale is recomputed for
+ * every token; 8 bits halve the cache).  For each new token t and kv head h,
+ * separately for the key row and the value row x[0..D):
+ *   absmax = max_d |x_d|;  scale = absmax / 127 (IEEE fp32 division), or 1 if
+ *   absmax == 0;  code_d = clamp(rint(x_d / scale), -127, 127) (IEEE division,
+ *   round half to even).  Dequantised value: code * scale.
+ *   key, value        [T][Hkv][D] bf16, device.
+ *   k_cache, v_cache  [N][Hkv][bs][D] int8, device.
+ *   k_scale, v_scale  [N][Hkv][bs] fp32, device.
+ *   slot_mapping etc. as in pa_reshape_and_cache.
+ * Results are bit-identical to the CPU statement of the same rule for finite
+ * inputs; non-finite inputs give unspecified codes.
+ */
+pa_status pa_quantize_kv(const pa_bf16 *key, const pa_bf16 *value, int8_t *k_cache,
+                         int8_t *v_cache, float *k_scale, float *v_scale,
+                         const int64_t *slot_mapping, int T, int Hkv, int D, int bs, int N,
+                         int *err_flag, void *stream);
+
+/*
+ * Copy-on-write block copy (gotburnout.io section 3.01): for each pair
+ * (src, dst) copy the whole physical block src onto block dst, in the K cache and
+ * in the V cache, and, when k_scale / v_scale are given, the block's scales.
+ *   k_cache, v_cache   device, N blocks of block_bytes bytes each.
+ *   k_scale, v_scale   device, N blocks of scale_elems_per_block fp32 each, or both
+ *                      NULL (then scale_elems_per_block must be 0).
+ *   block_mapping      HOST array [n][2] int64 of (src, dst) physical block ids.
+ *                      It is read during the call and may be freed right after.
+ *   block_bytes        multiple of 16.
+ * Pairs are validated on the host: every id in [0, N) (else PA_ERR_OUT_OF_RANGE),
+ * destinations pairwise distinct and no destination also a source (else
+ * PA_ERR_INVALID_ARG), because the result would otherwise depend on copy order.
+ */
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                         const int64_t *block_mapping, int n, int N, size_t block_bytes,
+                         int scale_elems_per_block, void *stream);
+
+/*
+ * Bytes of device workspace pa_decode needs for these arguments (0 when the
+ * contexts are short enough to need no split).  Pass the same values to
+ * pa_decode.  Returns 0 for invalid arguments as well; pa_decode reports those.
+ */
+size_t pa_decode_workspace_size(int S, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                int max_context_len);
+
+/*
+ * Paged decode attention (deeplearn.tn, "Le compromis fondamental de
+ * l'inference"; blog.fabienvernieres.com, opening section): for every sequence s
+ * and query head h
+ *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_s[t]) V_s[t],  t < context_lens[s],
+ * where K_s[t], V_s[t] are read from physical block block_tables[s][t / bs] at
+ * offset t % bs, kv head h / (Hq / Hkv); int8 entries are code * scale.  A
+ * sequence with context length 0 gets an all-zero output.
+ *   out             [S][Hq][D] bf16, device (written).
+ *   query           [S][Hq][D] bf16, device.
+ *   k_cache,v_cache [N][Hkv][bs][D], bf16 (kv_dtype PA_KV_BF16) or int8 (PA_KV_INT8).
+ *   k_scale,v_scale [N][Hkv][bs] fp32 for int8; ignored (may be NULL) for bf16.
+ *   block_tables    [S][M] int32, device; entries past a sequence's last block are
+ *                   never read.
+ *   context_lens    [S] int32, device.
+ *   max_context_len host upper bound of context_lens (0 <= it <= M * bs); longer
+ *                   contexts are clamped to it and flagged.
+ *   workspace       device scratch of at least pa_decode_workspace_size(...) bytes
+ *                   (may be NULL when that size is 0); its contents are not
+ *                   preserved.  Calls sharing a workspace must be stream-ordered.
+ *   err_flag        nullable device int (see PA_FLAG_*).
+ * Accumulation is fp32 (softmax statistics, dot products, weighted sums); the
+ * result is rounded once to bf16.  D in {64, 128}, bs in {16, 32}.
+ */
+pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
+                    const void *v_cache, const float *k_scale, const float *v_scale,
+                    int kv_dtype, const int32_t *block_tables, int M,
+                    const int32_t *context_lens, int S, int Hq, int Hkv, int D, int bs, int N,
+                    float scale, int max_context_len, void *workspace, size_t workspace_bytes,
+                    int *err_flag, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,232 @@
+"""Paged KV-cache decode on GB300: Python binding of the C ABI in include/pa.h.
+
+Every function here only marshals arguments (torch tensors -> pointers and sizes)
+and calls the function of the same name in libpa.so; all of the work runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing or
+its call fails, an exception is raised.
+
+Layouts (see include/pa.h):
+  query, out        [S][Hq][D] bf16
+  k_cache, v_cache  [N][Hkv][bs][D] bf16 or int8
+  k_scale, v_scale  [N][Hkv][bs] fp32 (int8 caches)
+  block_tables      [S][M] int32, context_lens [S] int32, slot_mapping [T] int64
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+PKG = Path(__file__).resolve().parent
+LIBRARY = PKG / "libpa.so"
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_CUDA = range(5)
+PA_KV_BF16, PA_KV_INT8 = 0, 1
+PA_FLAG_SLOT_OUT_OF_RANGE = 1
+PA_FLAG_BLOCK_OUT_OF_RANGE = 2
+PA_FLAG_CONTEXT_OUT_OF_RANGE = 4
+
+EXPORTED = ["pa_version", "pa_status_string", "pa_last_error_string", "pa_reshape_and_cache",
+            "pa_quantize_kv", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode"]
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[status {status}] {message}")
+        self.status = status
+
+
+_LIB: ctypes.CDLL | None = None
+
+
+def load_library(path: Path | str | None = None) -> ctypes.CDLL:
+    """Load libpa.so (built by __graft_entry__.build()); raise if it is absent."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = Path(path) if path is not None else LIBRARY
+    if not p.exists():
+        raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(str(p))
+    vp, i32, i64, sz, f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                             ctypes.c_float)
+    lib.pa_version.restype = i32
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_last_error_string.restype = ctypes.c_char_p
+    lib.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    lib.pa_reshape_and_cache.restype = i32
+    lib.pa_quantize_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    lib.pa_quantize_kv.restype = i32
+    lib.pa_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, sz, i32, vp]
+    lib.pa_copy_blocks.restype = i32
+    lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.pa_decode_workspace_size.restype = sz
+    lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
+                              i32, f32, i32, vp, sz, vp, vp]
+    lib.pa_decode.restype = i32
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != PA_OK:
+        lib = load_library()
+        raise PagedAttentionError(status, lib.pa_last_error_string().decode())
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _cuda(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int | None = None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dimensions, got {t.dim()}")
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _flag(err_flag):
+    if err_flag is not None:
+        _cuda(err_flag, "err_flag", torch.int32)
+    return _ptr(err_flag)
+
+
+def pa_version() -> int:
+    return int(load_library().pa_version())
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, err_flag=None,
+                         stream=None) -> None:
+    """Append the bf16 rows key/value [T][Hkv][D] into slots of a bf16 paged cache."""
+    for t, n in ((key, "key"), (value, "value")):
+        _cuda(t, n, torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _cuda(t, n, torch.bfloat16, 4)
+    _cuda(slot_mapping, "slot_mapping", torch.int64, 1)
+    T, Hkv, D = key.shape
+    N, Hkv2, bs, D2 = k_cache.shape
+    if value.shape != key.shape or v_cache.shape != k_cache.shape or (Hkv2, D2) != (Hkv, D) \
+            or slot_mapping.shape[0] != T:
+        raise ValueError("pa_reshape_and_cache: shape mismatch")
+    lib = load_library()
+    _check(lib.pa_reshape_and_cache(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(slot_mapping), T, Hkv, D, bs, N, _flag(err_flag),
+                                    _stream(stream, key.device)))
+
+
+def pa_quantize_kv(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, err_flag=None,
+                   stream=None) -> None:
+    """Quantise bf16 rows [T][Hkv][D] to int8 with a per-(token, kv head) scale and append."""
+    for t, n in ((key, "key"), (value, "value")):
+        _cuda(t, n, torch.bfloat16, 3)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _cuda(t, n, torch.int8, 4)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _cuda(t, n, torch.float32, 3)
+    _cuda(slot_mapping, "slot_mapping", torch.int64, 1)
+    T, Hkv, D = key.shape
+    N, Hkv2, bs, D2 = k_cache.shape
+    if value.shape != key.shape or v_cache.shape != k_cache.shape or (Hkv2, D2) != (Hkv, D) \
+            or tuple(k_scale.shape) != (N, Hkv, bs) or v_scale.shape != k_scale.shape \
+            or slot_mapping.shape[0] != T:
+        raise ValueError("pa_quantize_kv: shape mismatch")
+    lib = load_library()
+    _check(lib.pa_quantize_kv(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                              _ptr(v_scale), _ptr(slot_mapping), T, Hkv, D, bs, N, _flag(err_flag),
+                              _stream(stream, key.device)))
+
+
+def pa_copy_blocks(k_cache, v_cache, block_mapping, k_scale=None, v_scale=None,
+                   stream=None) -> None:
+    """Copy whole physical blocks (src, dst) of both caches (and scales, if given).
+
+    block_mapping is a HOST sequence of (src, dst) pairs (tensor, ndarray or list)."""
+    if k_cache.dtype not in (torch.bfloat16, torch.int8):
+        raise TypeError("k_cache must be bf16 or int8")
+    _cuda(k_cache, "k_cache", k_cache.dtype)
+    _cuda(v_cache, "v_cache", k_cache.dtype)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("pa_copy_blocks: cache shapes differ")
+    pairs = torch.as_tensor(block_mapping, dtype=torch.int64, device="cpu").reshape(-1, 2).contiguous()
+    N = k_cache.shape[0]
+    block_bytes = k_cache.numel() * k_cache.element_size() // N
+    scale_elems = 0
+    if k_scale is not None or v_scale is not None:
+        if k_scale is None or v_scale is None:
+            raise ValueError("give both scale arrays or neither")
+        _cuda(k_scale, "k_scale", torch.float32)
+        _cuda(v_scale, "v_scale", torch.float32)
+        if k_scale.shape[0] != N or v_scale.shape != k_scale.shape:
+            raise ValueError("pa_copy_blocks: scale shapes")
+        scale_elems = k_scale.numel() // N
+    lib = load_library()
+    _check(lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                              pairs.data_ptr(), pairs.shape[0], N, block_bytes, scale_elems,
+                              _stream(stream, k_cache.device)))
+
+
+def pa_decode_workspace_size(S: int, Hq: int, Hkv: int, D: int, bs: int, kv_dtype: int,
+                             max_context_len: int) -> int:
+    return int(load_library().pa_decode_workspace_size(S, Hq, Hkv, D, bs, kv_dtype,
+                                                       max_context_len))
+
+
+def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: float,
+              max_context_len: int, workspace=None, k_scale=None, v_scale=None, err_flag=None,
+              stream=None) -> None:
+    """Paged decode attention; writes out [S][Hq][D] bf16."""
+    _cuda(out, "out", torch.bfloat16, 3)
+    _cuda(query, "query", torch.bfloat16, 3)
+    kv_dtype = PA_KV_INT8 if k_cache.dtype == torch.int8 else PA_KV_BF16
+    cache_dtype = torch.int8 if kv_dtype == PA_KV_INT8 else torch.bfloat16
+    _cuda(k_cache, "k_cache", cache_dtype, 4)
+    _cuda(v_cache, "v_cache", cache_dtype, 4)
+    _cuda(block_tables, "block_tables", torch.int32, 2)
+    _cuda(context_lens, "context_lens", torch.int32, 1)
+    if kv_dtype == PA_KV_INT8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an int8 cache needs k_scale and v_scale")
+        _cuda(k_scale, "k_scale", torch.float32, 3)
+        _cuda(v_scale, "v_scale", torch.float32, 3)
+    S, Hq, D = query.shape
+    N, Hkv, bs, D2 = k_cache.shape
+    M = block_tables.shape[1]
+    if out.shape != query.shape or v_cache.shape != k_cache.shape or D2 != D \
+            or block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("pa_decode: shape mismatch")
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda(workspace, "workspace", workspace.dtype)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    lib = load_library()
+    _check(lib.pa_decode(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                         _ptr(v_scale), kv_dtype, _ptr(block_tables), M, _ptr(context_lens), S, Hq,
+                         Hkv, D, bs, N, float(scale), int(max_context_len), _ptr(workspace),
+                         ws_bytes, _flag(err_flag), _stream(stream, query.device)))
+
+
+def decode_workspace(query, k_cache, max_context_len: int) -> torch.Tensor | None:
+    """Allocate (with torch) the scratch pa_decode needs for these shapes, or None."""
+    S, Hq, D = query.shape
+    N, Hkv, bs, _ = k_cache.shape
+    kv_dtype = PA_KV_INT8 if k_cache.dtype == torch.int8 else PA_KV_BF16
+    n = pa_decode_workspace_size(S, Hq, Hkv, D, bs, kv_dtype, max_context_len)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=query.device)

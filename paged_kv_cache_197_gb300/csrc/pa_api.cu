@@ -1,0 +1,261 @@
+// C-ABI entry points: host-side argument checks, planning and kernel launches.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+
+static thread_local char g_last_error[512] = "";
+
+pa_status fail(pa_status status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+pa_status check_launch(const char *what) {
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess)
+        return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+    return PA_OK;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len) {
+    (void)bs;
+    (void)kv_dtype;
+    DecodePlan p{};
+    const int G = Hq / Hkv;
+    p.head_chunks = (G + 7) / 8;
+    // Partitions of 512 tokens: 32 blocks of 16 (or 16 of 32) per CTA, i.e. 8 or 4
+    // tiles for each of the CTA's 4 warps.  Long contexts are split so that a batch
+    // of few sequences still spreads over all SMs; the partial results cost
+    // (D + 2) fp32 per query head and partition, under 3% of the K/V bytes.
+    p.part_tokens = 512;
+    p.max_parts = std::max(1, (max_context_len + p.part_tokens - 1) / p.part_tokens);
+    if (p.max_parts == 1) {
+        p.ws_acc_off = p.ws_ml_off = p.ws_bytes = 0;
+        return p;
+    }
+    const size_t rows = (size_t)S * Hq * p.max_parts;
+    p.ws_acc_off = 0;
+    p.ws_ml_off = align_up(rows * D * sizeof(float), 256);
+    p.ws_bytes = align_up(p.ws_ml_off + rows * 2 * sizeof(float), 256);
+    return p;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 1; }
+
+const char *pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PA_ERR_OUT_OF_RANGE: return "index out of range";
+        case PA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+const char *pa_last_error_string(void) { return g_last_error; }
+
+static pa_status check_cache_shape(const char *fn, int Hkv, int D, int bs, int N) {
+    if (Hkv <= 0 || N <= 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: Hkv (%d) and N (%d) must be positive", fn, Hkv, N);
+    if (D != 64 && D != 128)
+        return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d not supported (64 or 128)", fn, D);
+    if (bs != 16 && bs != 32)
+        return fail(PA_ERR_UNSUPPORTED, "%s: block size %d not supported (16 or 32)", fn, bs);
+    if ((int64_t)N * bs > (int64_t)1 << 40)
+        return fail(PA_ERR_INVALID_ARG, "%s: pool too large", fn);
+    return PA_OK;
+}
+
+pa_status pa_reshape_and_cache(const pa_bf16 *key, const pa_bf16 *value, pa_bf16 *k_cache,
+                               pa_bf16 *v_cache, const int64_t *slot_mapping, int T, int Hkv,
+                               int D, int bs, int N, int *err_flag, void *stream) {
+    const char *fn = "pa_reshape_and_cache";
+    g_last_error[0] = 0;
+    if (T < 0) return fail(PA_ERR_INVALID_ARG, "%s: T = %d is negative", fn, T);
+    pa_status st = check_cache_shape(fn, Hkv, D, bs, N);
+    if (st != PA_OK) return st;
+    if (T == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
+    if ((int64_t)T * Hkv * D > ((int64_t)1 << 40))
+        return fail(PA_ERR_INVALID_ARG, "%s: too many tokens", fn);
+    launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, T, Hkv, D, bs, N,
+                             err_flag, (cudaStream_t)stream);
+    return check_launch(fn);
+}
+
+pa_status pa_quantize_kv(const pa_bf16 *key, const pa_bf16 *value, int8_t *k_cache,
+                         int8_t *v_cache, float *k_scale, float *v_scale,
+                         const int64_t *slot_mapping, int T, int Hkv, int D, int bs, int N,
+                         int *err_flag, void *stream) {
+    const char *fn = "pa_quantize_kv";
+    g_last_error[0] = 0;
+    if (T < 0) return fail(PA_ERR_INVALID_ARG, "%s: T = %d is negative", fn, T);
+    pa_status st = check_cache_shape(fn, Hkv, D, bs, N);
+    if (st != PA_OK) return st;
+    if (T == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(k_scale) || !aligned16(v_scale))
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
+    launch_quantize_kv(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, T, Hkv, D,
+                       bs, N, err_flag, (cudaStream_t)stream);
+    return check_launch(fn);
+}
+
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                         const int64_t *block_mapping, int n, int N, size_t block_bytes,
+                         int scale_elems_per_block, void *stream) {
+    const char *fn = "pa_copy_blocks";
+    g_last_error[0] = 0;
+    if (n < 0 || N <= 0) return fail(PA_ERR_INVALID_ARG, "%s: n = %d, N = %d", fn, n, N);
+    if (n == 0) return PA_OK;
+    if (!k_cache || !v_cache || !block_mapping)
+        return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if ((k_scale == nullptr) != (v_scale == nullptr))
+        return fail(PA_ERR_INVALID_ARG, "%s: give both scale arrays or neither", fn);
+    if ((k_scale == nullptr) != (scale_elems_per_block == 0) || scale_elems_per_block < 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: scale_elems_per_block = %d does not match the scale arrays",
+                    fn, scale_elems_per_block);
+    if (block_bytes == 0 || block_bytes % 16 != 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: block_bytes = %zu must be a positive multiple of 16", fn,
+                    block_bytes);
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "%s: caches must be 16-byte aligned", fn);
+    std::vector<int64_t> dst(n), src(n);
+    for (int i = 0; i < n; ++i) {
+        src[i] = block_mapping[2 * i];
+        dst[i] = block_mapping[2 * i + 1];
+        if (src[i] < 0 || src[i] >= N || dst[i] < 0 || dst[i] >= N)
+            return fail(PA_ERR_OUT_OF_RANGE, "%s: pair %d (%lld -> %lld) outside [0, %d)", fn, i,
+                        (long long)src[i], (long long)dst[i], N);
+    }
+    std::vector<int64_t> ds(dst), ss(src);
+    std::sort(ds.begin(), ds.end());
+    std::sort(ss.begin(), ss.end());
+    for (int i = 1; i < n; ++i)
+        if (ds[i] == ds[i - 1])
+            return fail(PA_ERR_INVALID_ARG, "%s: block %lld is the destination of two pairs", fn,
+                        (long long)ds[i]);
+    for (int i = 0; i < n; ++i)
+        if (std::binary_search(ss.begin(), ss.end(), dst[i]))
+            return fail(PA_ERR_INVALID_ARG, "%s: block %lld is both a source and a destination", fn,
+                        (long long)dst[i]);
+    launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, block_mapping, n, block_bytes,
+                       scale_elems_per_block, (cudaStream_t)stream);
+    return check_launch(fn);
+}
+
+static pa_status check_decode_shape(const char *fn, int S, int Hq, int Hkv, int D, int bs,
+                                    int kv_dtype, int max_context_len) {
+    if (S < 0 || Hq <= 0 || Hkv <= 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: S = %d, Hq = %d, Hkv = %d", fn, S, Hq, Hkv);
+    if (Hq % Hkv != 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: Hq (%d) must be a multiple of Hkv (%d)", fn, Hq, Hkv);
+    if (D != 64 && D != 128)
+        return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d not supported (64 or 128)", fn, D);
+    if (bs != 16 && bs != 32)
+        return fail(PA_ERR_UNSUPPORTED, "%s: block size %d not supported (16 or 32)", fn, bs);
+    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_INT8)
+        return fail(PA_ERR_UNSUPPORTED, "%s: kv dtype %d not supported", fn, kv_dtype);
+    if (max_context_len < 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: max_context_len = %d", fn, max_context_len);
+    if (S > 65535)
+        return fail(PA_ERR_UNSUPPORTED, "%s: at most 65535 sequences per call (got %d)", fn, S);
+    if ((int64_t)Hkv * ((Hq / Hkv + 7) / 8) > 65535)
+        return fail(PA_ERR_UNSUPPORTED, "%s: too many heads", fn);
+    return PA_OK;
+}
+
+size_t pa_decode_workspace_size(int S, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                int max_context_len) {
+    if (check_decode_shape("pa_decode_workspace_size", S, Hq, Hkv, D, bs, kv_dtype,
+                           max_context_len) != PA_OK)
+        return 0;
+    return plan_decode(S, Hq, Hkv, D, bs, kv_dtype, max_context_len).ws_bytes;
+}
+
+pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
+                    const void *v_cache, const float *k_scale, const float *v_scale,
+                    int kv_dtype, const int32_t *block_tables, int M,
+                    const int32_t *context_lens, int S, int Hq, int Hkv, int D, int bs, int N,
+                    float scale, int max_context_len, void *workspace, size_t workspace_bytes,
+                    int *err_flag, void *stream) {
+    const char *fn = "pa_decode";
+    g_last_error[0] = 0;
+    pa_status st = check_decode_shape(fn, S, Hq, Hkv, D, bs, kv_dtype, max_context_len);
+    if (st != PA_OK) return st;
+    if (S == 0) return PA_OK;
+    if (N <= 0 || M <= 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: N = %d, M = %d must be positive", fn, N, M);
+    if ((int64_t)max_context_len > (int64_t)M * bs)
+        return fail(PA_ERR_OUT_OF_RANGE, "%s: max_context_len %d exceeds M * bs = %lld", fn,
+                    max_context_len, (long long)M * bs);
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (kv_dtype == PA_KV_INT8 && (!k_scale || !v_scale))
+        return fail(PA_ERR_INVALID_ARG, "%s: int8 cache needs k_scale and v_scale", fn);
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
+    if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
+        return fail(PA_ERR_INVALID_ARG, "%s: scale must be finite", fn);
+    const DecodePlan plan = plan_decode(S, Hq, Hkv, D, bs, kv_dtype, max_context_len);
+    if (plan.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < plan.ws_bytes)
+            return fail(PA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn,
+                        plan.ws_bytes, workspace ? workspace_bytes : (size_t)0);
+        if (!aligned16(workspace))
+            return fail(PA_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", fn);
+    }
+    DecodeArgs a{};
+    a.out = out;
+    a.q = query;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.ws_acc = plan.ws_bytes ? (float *)((char *)workspace + plan.ws_acc_off) : nullptr;
+    a.ws_ml = plan.ws_bytes ? (float *)((char *)workspace + plan.ws_ml_off) : nullptr;
+    a.err_flag = err_flag;
+    a.M = M;
+    a.S = S;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.N = N;
+    a.head_chunks = plan.head_chunks;
+    a.part_tokens = plan.part_tokens;
+    a.max_parts = plan.max_parts;
+    a.max_context_len = max_context_len;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    launch_decode(a, D, bs, kv_dtype, (cudaStream_t)stream);
+    return check_launch(fn);
+}
+
+}  // extern "C"

@@ -1,0 +1,537 @@
+// Paged decode attention for GB300 (sm_103a).
+//
+// What is computed (deeplearn.tn KV-cache article, "Le compromis fondamental de
+// l'inference"; blog.fabienvernieres.com "Cache KV en production", opening
+// section): for every sequence s and query head h, the new token's query attends
+// over the sequence's cached keys and values,
+//   out[s][h] = sum_t softmax_t(scale * q . K[t]) V[t],
+// with K[t], V[t] gathered from physical block block_tables[s][t / bs] at offset
+// t % bs (gotburnout.io "PagedAttention & Gestion du KV-Cache", section 2
+// block-table figure) from kv head h / G.
+//
+// Design (decode is bound by HBM bandwidth; every K/V byte is read once):
+//   * One CTA of 4 warps per (sequence, kv head, group of <= 8 query heads,
+//     partition of 512 tokens).  Warps take the partition's tiles round-robin and
+//     each keeps its own online-softmax state; the CTA merges its warps in shared
+//     memory.  Longer contexts are split over several CTAs whose partial results
+//     (unnormalised output, running max, running sum) a second kernel merges by
+//     log-sum-exp.
+//   * A tile is 16 tokens (bf16) or a whole block (int8) of one kv head: one
+//     contiguous run of bytes in the [N][Hkv][bs][D] cache.  Each lane loads its
+//     share with 16-byte loads straight into registers, in the layout the tensor-
+//     core fragments need, so no shared-memory staging is required and every
+//     32-byte sector fetched is fully used.  The next tile's loads are issued
+//     before the current tile is consumed.
+//   * q.K^T and P.V of the query-head group run on the tensor cores
+//     (mma.sync m16n8k16, bf16 in, fp32 accumulate): S[16 tokens x 8 heads] =
+//     K_tile . q^T, then O^T[D x 8 heads] += V^T . P^T.  The head dimension order
+//     inside a lane is permuted consistently for q and K (a dot product does not
+//     depend on it), which turns each lane's K loads into whole 16-byte vectors.
+//     P leaves the first product as a C fragment and enters the second as a B
+//     fragment after one movmatrix transpose per 8x8 quarter.
+//   * int8 entries are turned into exact bf16 integers with integer ops; the key
+//     scale multiplies the score, the value scale multiplies the softmax weight.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxPartBlocks = 64;
+constexpr int kHeadsPerCta = 8;
+
+// ------------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void ldg16(uint32_t *w, const void *p) {
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+        : "l"(p));
+}
+
+__device__ __forceinline__ void ldg8(uint32_t *w, const void *p) {
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
+}
+
+template <int NB>
+__device__ __forceinline__ void ldg_bytes(uint32_t *w, const char *p) {
+    static_assert(NB % 8 == 0, "8-byte granules");
+    if constexpr (NB % 16 == 0) {
+#pragma unroll
+        for (int i = 0; i < NB / 16; ++i) ldg16(w + 4 * i, p + 16 * i);
+    } else {
+        ldg8(w, p);
+    }
+}
+
+// D = A . B + D, A 16x16 bf16 (row), B 16x8 bf16 (col), D 16x8 fp32.
+__device__ __forceinline__ void mma_bf16(float *c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 matrix of 16-bit values held one row pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Byte 0 and byte 2 of t hold signed int8 values a and b (bytes 1 and 3 are
+// ignored).  Returns the bf16 pair (a, b), exactly: 128 + (x & 127) and 128 or 256
+// (by the sign bit) are both exact bf16 values, and so is their difference x.
+__device__ __forceinline__ uint32_t i8pair_to_bf16x2(uint32_t t) {
+    const uint32_t mag = (t & 0x007f007fu) | 0x43004300u;
+    const uint32_t bias = (t & 0x00800080u) | 0x43004300u;
+    __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162 *>(&mag);
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&bias);
+    __nv_bfloat162 r = __hsub2(m, b);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ void raise_flag(int *err_flag, int bit) {
+    if (err_flag) atomicOr(err_flag, bit);
+}
+
+// Context length after the range checks: negative -> 0, beyond the table or the
+// planned maximum -> clamped.
+__device__ __forceinline__ int checked_context(const DecodeArgs &a, int s, int bs, bool report) {
+    int ctx = a.context_lens[s];
+    const int lim = min(a.M * bs, a.max_context_len);
+    if (ctx < 0 || ctx > lim) {
+        if (report) raise_flag(a.err_flag, PA_FLAG_CONTEXT_OUT_OF_RANGE);
+        ctx = ctx < 0 ? 0 : lim;
+    }
+    return ctx;
+}
+
+// ---------------------------------------------------------------- tile geometry
+template <typename KV, int D, int TILE>
+struct Geo {
+    static constexpr int ELEM = sizeof(KV);
+    static constexpr int ROW_BYTES = D * ELEM;     // one token of one kv head
+    static constexpr int K_ROWS = TILE / 8;        // K rows per lane: tokens g + 8r
+    static constexpr int K_CHUNKS = ROW_BYTES / 64;  // 16-byte chunks per K row per lane
+    static constexpr int K_WORDS = K_CHUNKS * 4;
+    static constexpr int V_TOKS = TILE / 4;        // V rows per lane
+    static constexpr int V_BYTES = ROW_BYTES / 8;  // bytes of one V row per lane
+    static constexpr int V_WORDS = V_BYTES / 4;
+    static constexpr int KSTEPS = D / 16;          // k-steps of the score product
+    static constexpr int MT = D / 16;              // d tiles of the output product
+    static constexpr int SUB = TILE / 16;          // 16-token sub-tiles
+    static constexpr int QW = D / 8;               // q words per lane
+    static_assert(K_CHUNKS >= 1 && V_BYTES >= 8, "unsupported head_dim / dtype");
+};
+
+template <class GEO>
+struct Tile {
+    uint32_t k[GEO::K_ROWS][GEO::K_WORDS];
+    uint32_t v[GEO::V_TOKS][GEO::V_WORDS];
+    float ks, vs;  // int8: scales of token `lane` of the tile
+    int nvalid;    // tokens of the tile inside the context
+};
+
+// V row j of a lane: sub-tile j / 4, token 2t, 2t+1, 2t+8 or 2t+9 of it.
+__device__ __forceinline__ int v_token(int j, int t) {
+    const int jj = j & 3;
+    return 16 * (j >> 2) + 2 * t + (jj & 1) + ((jj >> 1) << 3);
+}
+
+template <typename KV, int D, int BS, int TILE>
+__device__ __forceinline__ void load_tile(Tile<Geo<KV, D, TILE>> &R, const DecodeArgs &a,
+                                          const int *s_blk, int blk_begin, int tok_begin,
+                                          int tok_end, int i, int kvh, int g, int t, int lane) {
+    using G_ = Geo<KV, D, TILE>;
+    const int tok0 = tok_begin + i * TILE;
+    int blk = s_blk[tok0 / BS - blk_begin];
+    R.nvalid = min(TILE, tok_end - tok0);
+    if (blk < 0) {  // flagged when the table was read: the tile is skipped
+        R.nvalid = 0;
+        blk = 0;
+    }
+    const int off = tok0 % BS;
+    const int64_t row0 = ((int64_t)blk * a.Hkv + kvh) * BS + off;
+    const char *kb = static_cast<const char *>(a.k_cache) + row0 * G_::ROW_BYTES;
+    const char *vb = static_cast<const char *>(a.v_cache) + row0 * G_::ROW_BYTES;
+#pragma unroll
+    for (int r = 0; r < G_::K_ROWS; ++r)
+#pragma unroll
+        for (int c = 0; c < G_::K_CHUNKS; ++c)
+            ldg16(&R.k[r][4 * c], kb + (g + 8 * r) * G_::ROW_BYTES + c * 64 + t * 16);
+#pragma unroll
+    for (int j = 0; j < G_::V_TOKS; ++j) {
+        const char *row = vb + v_token(j, t) * G_::ROW_BYTES;
+        if constexpr (G_::ELEM == 2) {
+            // two runs of D/16 values: d in [h*D/2 + g*D/16, +D/16), h = 0, 1
+            ldg_bytes<G_::V_BYTES / 2>(&R.v[j][0], row + g * (G_::V_BYTES / 2));
+            ldg_bytes<G_::V_BYTES / 2>(&R.v[j][G_::V_WORDS / 2],
+                                       row + G_::ROW_BYTES / 2 + g * (G_::V_BYTES / 2));
+        } else {
+            // one run of D/8 values: d in [g*D/8, +D/8)
+            ldg_bytes<G_::V_BYTES>(&R.v[j][0], row + g * G_::V_BYTES);
+        }
+    }
+    if constexpr (G_::ELEM == 1) {
+        const int64_t srow = row0 + (lane < TILE ? lane : 0);
+        R.ks = __ldg(a.k_scale + srow);
+        R.vs = __ldg(a.v_scale + srow);
+    }
+}
+
+// Head-dim index of the e-th value a lane holds of a K row (and of q): lane quad t
+// owns 16-byte chunks c*64 + t*16 of each K row.
+template <int ELEM>
+__device__ __forceinline__ int k_dim(int e, int t) {
+    constexpr int PER = 16 / ELEM;  // values per 16-byte chunk
+    return (e / PER) * (64 / ELEM) + t * PER + e % PER;
+}
+
+// Head-dim index held in row g (h = 0) or g + 8 (h = 1) of output d-tile mt.
+template <int ELEM, int D>
+__device__ __forceinline__ int out_dim(int mt, int g, int h) {
+    if constexpr (ELEM == 2)
+        return h * (D / 2) + g * (D / 16) + mt;
+    else
+        return g * (D / 8) + 2 * mt + h;
+}
+
+template <typename KV, int D, int TILE>
+struct WarpState {
+    float o[D / 16][4];  // O^T fragments: [d tile][c0..c3]
+    float m[2];          // running max of heads 2t, 2t+1 (log2 units)
+    float l[2];          // running sum, partial over this lane's tokens
+};
+
+template <typename KV, int D, int TILE>
+__device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
+                                             Tile<Geo<KV, D, TILE>> &R, const uint32_t *qw,
+                                             float scale_log2, int g, int t) {
+    using G_ = Geo<KV, D, TILE>;
+    // ---- scores S[token][head] for the tile's 16-token sub-tiles
+    float sc[G_::SUB][4];
+#pragma unroll
+    for (int s = 0; s < G_::SUB; ++s) {
+        sc[s][0] = sc[s][1] = sc[s][2] = sc[s][3] = 0.0f;
+#pragma unroll
+        for (int kc = 0; kc < G_::KSTEPS; ++kc) {
+            uint32_t a0, a1, a2, a3;
+            if constexpr (G_::ELEM == 2) {
+                a0 = R.k[2 * s][2 * kc];
+                a2 = R.k[2 * s][2 * kc + 1];
+                a1 = R.k[2 * s + 1][2 * kc];
+                a3 = R.k[2 * s + 1][2 * kc + 1];
+            } else {
+                const uint32_t w0 = R.k[2 * s][kc], w1 = R.k[2 * s + 1][kc];
+                a0 = i8pair_to_bf16x2(__byte_perm(w0, 0, 0x0100));
+                a2 = i8pair_to_bf16x2(__byte_perm(w0, 0, 0x0302));
+                a1 = i8pair_to_bf16x2(__byte_perm(w1, 0, 0x0100));
+                a3 = i8pair_to_bf16x2(__byte_perm(w1, 0, 0x0302));
+            }
+            mma_bf16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
+        }
+    }
+    // ---- online softmax over the tile (log2 domain)
+    float x[G_::SUB][4];
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int s = 0; s < G_::SUB; ++s)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int tok = 16 * s + g + 8 * (c >> 1);
+            float v = sc[s][c] * scale_log2;
+            if constexpr (G_::ELEM == 1) v *= __shfl_sync(0xffffffffu, R.ks, tok);
+            v = tok < R.nvalid ? v : -INFINITY;
+            x[s][c] = v;
+            mx[c & 1] = fmaxf(mx[c & 1], v);
+        }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+    }
+    float alpha[2], base[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float mnew = fmaxf(st.m[j], mx[j]);
+        base[j] = mnew == -INFINITY ? 0.0f : mnew;
+        alpha[j] = fast_exp2(st.m[j] - base[j]);
+        st.m[j] = mnew;
+    }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+        for (int mt = 0; mt < G_::MT; ++mt) {
+            st.o[mt][0] *= alpha[0];
+            st.o[mt][1] *= alpha[1];
+            st.o[mt][2] *= alpha[0];
+            st.o[mt][3] *= alpha[1];
+        }
+        st.l[0] *= alpha[0];
+        st.l[1] *= alpha[1];
+    }
+    // ---- values: zero rows past the context (they may hold any bit pattern)
+    if (R.nvalid < TILE) {
+#pragma unroll
+        for (int j = 0; j < G_::V_TOKS; ++j)
+            if (v_token(j, t) >= R.nvalid)
+#pragma unroll
+                for (int w = 0; w < G_::V_WORDS; ++w) R.v[j][w] = 0u;
+    }
+#pragma unroll
+    for (int s = 0; s < G_::SUB; ++s) {
+        float p[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            p[c] = fast_exp2(x[s][c] - base[c & 1]);
+            st.l[c & 1] += p[c];
+            if constexpr (G_::ELEM == 1) {
+                const int tok = 16 * s + g + 8 * (c >> 1);
+                const float vsc = __shfl_sync(0xffffffffu, R.vs, tok);
+                p[c] = tok < R.nvalid ? p[c] * vsc : 0.0f;
+            }
+        }
+        // P[head][token] as the B operand: transpose the [token][head] quarters
+        const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
+        const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
+        const int j0 = 4 * s;  // V rows 2t, 2t+1, 2t+8, 2t+9 of this sub-tile
+#pragma unroll
+        for (int mt = 0; mt < G_::MT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            if constexpr (G_::ELEM == 2) {
+                constexpr int HW = G_::V_WORDS / 2;
+                const int w = mt >> 1;
+                const uint32_t sel = (mt & 1) ? 0x7632u : 0x5410u;
+                a0 = __byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel);
+                a1 = __byte_perm(R.v[j0][HW + w], R.v[j0 + 1][HW + w], sel);
+                a2 = __byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel);
+                a3 = __byte_perm(R.v[j0 + 2][HW + w], R.v[j0 + 3][HW + w], sel);
+            } else {
+                const int w = mt >> 1;
+                const uint32_t b = 2u * (mt & 1);
+                const uint32_t sel0 = b | ((4u + b) << 8);
+                const uint32_t sel1 = (b + 1u) | ((5u + b) << 8);
+                a0 = i8pair_to_bf16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel0));
+                a1 = i8pair_to_bf16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel1));
+                a2 = i8pair_to_bf16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel0));
+                a3 = i8pair_to_bf16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel1));
+            }
+            mma_bf16(st.o[mt], a0, a1, a2, a3, b0, b1);
+        }
+    }
+}
+
+template <typename KV, int D, int BS, int TILE>
+__global__ void __launch_bounds__(kThreads)
+paged_decode_kernel(const DecodeArgs a) {
+    using G_ = Geo<KV, D, TILE>;
+    static_assert(BS % TILE == 0, "a tile lies inside one block");
+    __shared__ int s_blk[kMaxPartBlocks];
+    __shared__ float s_m[kWarps][kHeadsPerCta];
+    __shared__ float s_l[kWarps][kHeadsPerCta];
+    __shared__ __align__(16) float s_o[kWarps][kHeadsPerCta][D];
+
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / a.head_chunks;
+    const int chunk = blockIdx.y % a.head_chunks;
+    const int s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t = lane & 3;
+
+    const int ctx = checked_context(a, s, BS, part == 0 && blockIdx.y == 0 && tid == 0);
+    const int nparts = max(1, (ctx + a.part_tokens - 1) / a.part_tokens);
+    if (part >= nparts) return;
+    const int tok_begin = part * a.part_tokens;
+    const int tok_end = min(ctx, tok_begin + a.part_tokens);
+    const int blk_begin = tok_begin / BS;
+    const int nblk = max(0, (tok_end - tok_begin + BS - 1) / BS);
+    const int h0 = kvh * a.G + chunk * kHeadsPerCta;
+    const int nh = min(kHeadsPerCta, a.G - chunk * kHeadsPerCta);
+
+    if (tid < nblk) {
+        int b = a.block_tables[(int64_t)s * a.M + blk_begin + tid];
+        if (b < 0 || b >= a.N) {
+            if (chunk == 0) raise_flag(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
+            b = -1;
+        }
+        s_blk[tid] = b;
+    }
+
+    // q fragments: lane (g, t) holds head g's values at the K-row positions it owns
+    uint32_t qw[G_::QW];
+    if (g < nh) {
+        const char *qrow = reinterpret_cast<const char *>(a.q + ((int64_t)s * a.Hq + h0 + g) * D);
+#pragma unroll
+        for (int c = 0; c < G_::K_CHUNKS; ++c)
+            ldg_bytes<32 / G_::ELEM>(&qw[c * (8 / G_::ELEM)],
+                                     qrow + 2 * k_dim<G_::ELEM>(c * (16 / G_::ELEM), t));
+    } else {
+#pragma unroll
+        for (int i = 0; i < G_::QW; ++i) qw[i] = 0u;
+    }
+    __syncthreads();
+
+    WarpState<KV, D, TILE> st;
+#pragma unroll
+    for (int mt = 0; mt < G_::MT; ++mt) st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.0f;
+
+    const int ntiles = (tok_end - tok_begin + TILE - 1) / TILE;
+    Tile<G_> A, B;
+    int i = warp;
+    if (i < ntiles) load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i, kvh, g, t, lane);
+    while (i < ntiles) {
+        if (i + kWarps < ntiles)
+            load_tile<KV, D, BS, TILE>(B, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
+        consume_tile<KV, D, TILE>(st, A, qw, a.scale_log2, g, t);
+        i += kWarps;
+        if (i >= ntiles) break;
+        if (i + kWarps < ntiles)
+            load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
+        consume_tile<KV, D, TILE>(st, B, qw, a.scale_log2, g, t);
+        i += kWarps;
+    }
+
+    // ---- per-warp totals, then merge the CTA's warps through shared memory
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 4);
+        st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 8);
+        st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
+    }
+    if (g == 0) {
+        s_m[warp][2 * t] = st.m[0];
+        s_m[warp][2 * t + 1] = st.m[1];
+        s_l[warp][2 * t] = st.l[0];
+        s_l[warp][2 * t + 1] = st.l[1];
+    }
+#pragma unroll
+    for (int mt = 0; mt < G_::MT; ++mt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            s_o[warp][2 * t + (c & 1)][out_dim<G_::ELEM, D>(mt, g, c >> 1)] = st.o[mt][c];
+    __syncthreads();
+
+    constexpr int DPT = D / 16;  // output values per thread: 16 threads per head
+    const int hj = tid >> 4;
+    const int d0 = (tid & 15) * DPT;
+    if (hj >= nh) return;
+    float mmax = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_m[w][hj]);
+    const float mbase = mmax == -INFINITY ? 0.0f : mmax;
+    float acc[DPT];
+#pragma unroll
+    for (int e = 0; e < DPT; ++e) acc[e] = 0.0f;
+    float lsum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float f = fast_exp2(s_m[w][hj] - mbase);
+        lsum += f * s_l[w][hj];
+#pragma unroll
+        for (int e = 0; e < DPT; ++e) acc[e] += f * s_o[w][hj][d0 + e];
+    }
+    const int h = h0 + hj;
+    if (nparts == 1) {
+        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+        uint32_t packed[DPT / 2];
+#pragma unroll
+        for (int e = 0; e < DPT / 2; ++e) packed[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+        uint16_t *dst = a.out + ((int64_t)s * a.Hq + h) * D + d0;
+        if constexpr (DPT == 8)
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        else
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+        const int64_t row = ((int64_t)s * a.Hq + h) * a.max_parts + part;
+        float *dst = a.ws_acc + row * D + d0;
+#pragma unroll
+        for (int e = 0; e < DPT; e += 4)
+            *reinterpret_cast<float4 *>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+        if ((tid & 15) == 0) *reinterpret_cast<float2 *>(a.ws_ml + row * 2) = make_float2(mmax, lsum);
+    }
+}
+
+// Log-sum-exp merge of the partitions of each (sequence, query head):
+// out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p, M = max_p m_p.
+// D/4 threads per (sequence, head), 4 output values each.
+template <int D, int BS>
+__global__ void __launch_bounds__(kThreads)
+merge_partitions_kernel(const DecodeArgs a) {
+    constexpr int TPH = D / 4;  // threads per head
+    constexpr int HPC = kThreads / TPH;
+    const int s = blockIdx.y;
+    const int h = blockIdx.x * HPC + threadIdx.x / TPH;
+    const int d0 = (threadIdx.x % TPH) * 4;
+    if (h >= a.Hq) return;
+    const int ctx = checked_context(a, s, BS, false);
+    const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
+    if (nparts <= 1) return;  // the decode kernel wrote the output itself
+    const int64_t row0 = ((int64_t)s * a.Hq + h) * a.max_parts;
+    float mmax = -INFINITY;
+    for (int p = 0; p < nparts; ++p) mmax = fmaxf(mmax, a.ws_ml[(row0 + p) * 2]);
+    const float mbase = mmax == -INFINITY ? 0.0f : mmax;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.0f;
+    for (int p = 0; p < nparts; ++p) {
+        const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + (row0 + p) * 2);
+        const float f = fast_exp2(ml.x - mbase);
+        lsum += f * ml.y;
+        const float4 v = *reinterpret_cast<const float4 *>(a.ws_acc + (row0 + p) * D + d0);
+        acc.x += f * v.x;
+        acc.y += f * v.y;
+        acc.z += f * v.z;
+        acc.w += f * v.w;
+    }
+    const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+    uint16_t *dst = a.out + ((int64_t)s * a.Hq + h) * D + d0;
+    *reinterpret_cast<uint2 *>(dst) =
+        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+}
+
+template <typename KV, int D, int BS, int TILE>
+cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
+    dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
+    paged_decode_kernel<KV, D, BS, TILE><<<grid, kThreads, 0, stream>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || a.max_parts == 1) return err;
+    constexpr int HPC = kThreads / (D / 4);
+    dim3 mgrid((a.Hq + HPC - 1) / HPC, a.S);
+    merge_partitions_kernel<D, BS><<<mgrid, kThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename KV, int D>
+cudaError_t launch_bs(const DecodeArgs &a, int bs, cudaStream_t stream) {
+    constexpr bool INT8 = sizeof(KV) == 1;
+    if (bs == 16) return launch_typed<KV, D, 16, 16>(a, stream);
+    return launch_typed<KV, D, 32, INT8 ? 32 : 16>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
+    static_assert(kMaxPartBlocks * 16 >= 512, "partition block list fits in shared memory");
+    if (kv_dtype == PA_KV_BF16)
+        return D == 128 ? launch_bs<uint16_t, 128>(a, bs, stream) : launch_bs<uint16_t, 64>(a, bs, stream);
+    return D == 128 ? launch_bs<int8_t, 128>(a, bs, stream) : launch_bs<int8_t, 64>(a, bs, stream);
+}
+
+}  // namespace pa

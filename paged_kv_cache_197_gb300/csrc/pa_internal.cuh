@@ -1,0 +1,67 @@
+// Internal declarations shared by the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------- host errors
+// Records a message for pa_last_error_string() and returns `status`.
+pa_status fail(pa_status status, const char *fmt, ...);
+// Turns the result of the launches just made into a status.
+pa_status check_launch(const char *what);
+
+// ------------------------------------------------------------- decode planning
+// Split of each sequence's context into partitions processed by separate CTAs
+// and combined by a log-sum-exp merge.
+struct DecodePlan {
+    int part_tokens;    // tokens per partition (multiple of the block size)
+    int max_parts;      // partitions of the longest allowed context
+    int head_chunks;    // ceil(G / 8): query heads of one kv head are taken 8 at a time
+    size_t ws_acc_off;  // byte offsets of the partial outputs and the (max, sum) pairs
+    size_t ws_ml_off;
+    size_t ws_bytes;    // 0 when max_parts == 1
+};
+
+DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len);
+
+// Parameters of the decode and merge kernels.
+struct DecodeArgs {
+    uint16_t *out;
+    const uint16_t *q;
+    const void *k_cache;
+    const void *v_cache;
+    const float *k_scale;
+    const float *v_scale;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *ws_acc;  // [S][Hq][max_parts][D]
+    float *ws_ml;   // [S][Hq][max_parts][2]
+    int *err_flag;
+    int M, S, Hq, Hkv, G, N;
+    int head_chunks, part_tokens, max_parts;
+    int max_context_len;  // host bound; longer contexts are clamped and flagged
+    float scale_log2;  // softmax scale times log2(e)
+};
+
+// ------------------------------------------------------------------ launchers
+// Each returns the CUDA error of its launch (cudaSuccess when nothing was launched).
+cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *k_cache,
+                                     uint16_t *v_cache, const int64_t *slot_mapping, int T,
+                                     int Hkv, int D, int bs, int N, int *err_flag,
+                                     cudaStream_t stream);
+cudaError_t launch_quantize_kv(const uint16_t *key, const uint16_t *value, int8_t *k_cache,
+                               int8_t *v_cache, float *k_scale, float *v_scale,
+                               const int64_t *slot_mapping, int T, int Hkv, int D, int bs, int N,
+                               int *err_flag, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                               const int64_t *block_mapping, int n, size_t block_bytes,
+                               int scale_elems_per_block, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &args, int D, int bs, int kv_dtype,
+                          cudaStream_t stream);
+
+}  // namespace pa

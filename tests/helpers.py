@@ -1,0 +1,113 @@
+"""Shared test steps: run one decode step through the GPU library, and the same step
+through the CPU oracle, on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads
+
+BF16_MAX_ABS, BF16_MEAN_ABS = 2e-2, 2e-3   # bf16 cache: output vs fp64 oracle
+INT8_MAX_ABS, INT8_MEAN_ABS = 5e-2, 2e-3   # int8 cache: vs the oracle on the same codes
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def int8_pool_rows(pool: torch.Tensor) -> torch.Tensor:
+    """[N][Hkv][bs][D] -> [N*bs][Hkv][D] (rows in slot order) for a quantise-append of a
+    whole pool."""
+    N, Hkv, bs, D = pool.shape
+    return pool.permute(0, 2, 1, 3).reshape(N * bs, Hkv, D).contiguous()
+
+
+def gpu_step(case: workloads.PagedCase, device, max_context_len=None, poison_int8=True):
+    """COW copy, append (or quantise-append), decode on the GPU.
+
+    Returns dict(out, k_cache, v_cache, k_scale, v_scale, flag) on the device."""
+    import paged_kv_cache_197_gb300 as pa
+
+    c = case.to(device)
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    k_scale = v_scale = None
+    if case.kv_dtype == "bf16":
+        k_cache, v_cache = c.k_pool.clone(), c.v_pool.clone()
+    else:
+        N, Hkv, bs, D = case.k_pool.shape
+        k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.int8, device=device)
+        v_cache = torch.empty_like(k_cache)
+        k_scale = torch.empty((N, Hkv, bs), dtype=torch.float32, device=device)
+        v_scale = torch.empty_like(k_scale)
+        slots = torch.arange(N * bs, dtype=torch.int64, device=device)
+        pa.pa_quantize_kv(int8_pool_rows(c.k_pool), int8_pool_rows(c.v_pool), k_cache, v_cache,
+                          k_scale, v_scale, slots, err_flag=flag)
+        if poison_int8:
+            bad = ~workloads.valid_slot_mask(case.meta["content_tables"], case.context_lens - 1,
+                                             case.bs, case.N).to(device)
+            k_scale.permute(0, 2, 1)[bad] = float("nan")
+            v_scale.permute(0, 2, 1)[bad] = float("nan")
+    if case.cow_pairs.shape[0]:
+        pa.pa_copy_blocks(k_cache, v_cache, case.cow_pairs, k_scale=k_scale, v_scale=v_scale)
+    if case.kv_dtype == "bf16":
+        pa.pa_reshape_and_cache(c.new_key, c.new_value, k_cache, v_cache, c.slot_mapping,
+                                err_flag=flag)
+    else:
+        pa.pa_quantize_kv(c.new_key, c.new_value, k_cache, v_cache, k_scale, v_scale,
+                          c.slot_mapping, err_flag=flag)
+    if max_context_len is None:
+        max_context_len = int(case.context_lens.max()) if case.S else 0
+    out = torch.full_like(c.q, float("nan"))
+    ws = pa.decode_workspace(c.q, k_cache, max_context_len)
+    pa.pa_decode(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens, case.scale,
+                 max_context_len, workspace=ws, k_scale=k_scale, v_scale=v_scale, err_flag=flag)
+    torch.cuda.synchronize(device)
+    return dict(out=out, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
+                flag=int(flag.item()))
+
+
+def oracle_caches(case: workloads.PagedCase, orc, poison_int8=True):
+    """The oracle's own caches after COW copy and append (bf16 bits, or int8 codes+scales)."""
+    ks = vs = None
+    if case.kv_dtype == "bf16":
+        kc, vc = bits(case.k_pool), bits(case.v_pool)
+    else:
+        kc, ks = orc.quantize_pool(bits(case.k_pool))
+        vc, vs = orc.quantize_pool(bits(case.v_pool))
+        if poison_int8:
+            bad = ~workloads.valid_slot_mask(case.meta["content_tables"], case.context_lens - 1,
+                                             case.bs, case.N).numpy()
+            ks.transpose(0, 2, 1)[bad] = np.nan
+            vs.transpose(0, 2, 1)[bad] = np.nan
+    if case.cow_pairs.shape[0]:
+        orc.copy_blocks(kc, vc, case.cow_pairs.cpu().numpy(), k_scale=ks, v_scale=vs)
+    slots = case.slot_mapping.cpu().numpy()
+    if case.kv_dtype == "bf16":
+        bad = orc.reshape_and_cache(bits(case.new_key), bits(case.new_value), kc, vc, slots, case.bs)
+    else:
+        bad = orc.quantize_kv(bits(case.new_key), bits(case.new_value), kc, vc, ks, vs, slots, case.bs)
+    assert bad == 0
+    return kc, vc, ks, vs
+
+
+def oracle_out(case, orc, caches, seqs=None) -> np.ndarray:
+    kc, vc, ks, vs = caches
+    q = bits(case.q)
+    tables = case.block_tables.cpu().numpy()
+    lens = case.context_lens.cpu().numpy()
+    if seqs is not None:
+        q = np.ascontiguousarray(q[seqs])
+        tables = np.ascontiguousarray(tables[seqs])
+        lens = np.ascontiguousarray(lens[seqs])
+    return orc.paged_attention(q, kc, vc, tables, lens, case.scale, k_scale=ks, v_scale=vs)
+
+
+def compare(got: torch.Tensor, ref: np.ndarray, kv_dtype: str):
+    g = got.float().cpu().double().numpy()
+    assert np.all(np.isfinite(g)), "non-finite output"
+    err = np.abs(g - ref)
+    max_abs, mean_abs = (BF16_MAX_ABS, BF16_MEAN_ABS) if kv_dtype == "bf16" else (INT8_MAX_ABS, INT8_MEAN_ABS)
+    assert err.max() <= max_abs, f"max abs error {err.max():.3e} > {max_abs}"
+    assert err.mean() <= mean_abs, f"mean abs error {err.mean():.3e} > {mean_abs}"
+    return float(err.max()), float(err.mean())

@@ -1,0 +1,110 @@
+"""The C-ABI library builds, loads and exports every function include/pa.h declares;
+host-side argument checks answer without touching a GPU."""
+import re
+from pathlib import Path
+
+import pytest
+import torch
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_197_gb300 import _build
+
+    _build.build()
+    import paged_kv_cache_197_gb300 as pa
+
+    return pa.load_library()
+
+
+def declared_functions():
+    text = (ROOT / "include" / "pa.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    import paged_kv_cache_197_gb300 as pa
+
+    names = declared_functions()
+    assert names, "no declarations found"
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
+    assert sorted(pa.EXPORTED) == names
+
+
+def test_version_and_strings(lib):
+    assert lib.pa_version() == 1
+    for code in range(5):
+        assert lib.pa_status_string(code)
+
+
+def test_no_extension_fails_loudly(tmp_path):
+    import paged_kv_cache_197_gb300 as pa
+
+    with pytest.raises(RuntimeError):
+        pa.load_library(tmp_path / "missing.so")
+
+
+def test_decode_host_checks(lib):
+    import paged_kv_cache_197_gb300 as pa
+
+    fake = 1 << 20  # never dereferenced: every call below fails its host checks
+
+    def call(S=2, Hq=8, Hkv=2, D=128, bs=16, N=4, M=4, max_ctx=64, kv=pa.PA_KV_BF16,
+             scale=0.1, ws=0, ws_bytes=0, out=fake):
+        return lib.pa_decode(out, fake, fake, fake, None, None, kv, fake, M, fake, S, Hq, Hkv, D,
+                             bs, N, scale, max_ctx, ws, ws_bytes, None, None)
+
+    assert call(D=96) == pa.PA_ERR_UNSUPPORTED
+    assert b"head_dim" in lib.pa_last_error_string()
+    assert call(bs=8) == pa.PA_ERR_UNSUPPORTED
+    assert call(Hq=6, Hkv=4) == pa.PA_ERR_INVALID_ARG
+    assert call(kv=7) == pa.PA_ERR_UNSUPPORTED
+    assert call(max_ctx=-1) == pa.PA_ERR_INVALID_ARG
+    assert call(max_ctx=65, M=4, bs=16) == pa.PA_ERR_OUT_OF_RANGE
+    assert call(kv=pa.PA_KV_INT8) == pa.PA_ERR_INVALID_ARG  # scales missing
+    assert call(out=fake + 2) == pa.PA_ERR_INVALID_ARG  # misaligned
+    assert call(scale=float("nan")) == pa.PA_ERR_INVALID_ARG
+    assert call(max_ctx=4000, M=400) == pa.PA_ERR_INVALID_ARG  # workspace missing
+    assert call(S=0) == pa.PA_OK  # nothing to do, nothing queued
+
+
+def test_workspace_size(lib):
+    import paged_kv_cache_197_gb300 as pa
+
+    assert pa.pa_decode_workspace_size(64, 40, 40, 128, 16, pa.PA_KV_BF16, 512) == 0
+    n = pa.pa_decode_workspace_size(20, 64, 8, 128, 16, pa.PA_KV_BF16, 8000)
+    rows = 20 * 64 * 16  # 16 partitions of 512 tokens
+    assert n >= rows * (128 + 2) * 4 and n % 256 == 0
+    assert pa.pa_decode_workspace_size(1, 3, 2, 128, 16, 0, 100) == 0  # invalid -> 0
+
+
+def test_cache_host_checks(lib):
+    import paged_kv_cache_197_gb300 as pa
+
+    fake = 1 << 20
+    assert lib.pa_reshape_and_cache(fake, fake, fake, fake, fake, 0, 8, 128, 16, 4, None, None) == pa.PA_OK
+    assert lib.pa_reshape_and_cache(fake, fake, fake, fake, fake, 3, 8, 80, 16, 4, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_reshape_and_cache(fake, fake, fake, fake, fake, -1, 8, 128, 16, 4, None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_quantize_kv(fake, fake, fake, fake, None, fake, fake, 2, 8, 128, 32, 4, None, None) == pa.PA_ERR_INVALID_ARG
+
+    def copy(pairs, N=10, block_bytes=4096):
+        t = torch.tensor(pairs, dtype=torch.int64).reshape(-1, 2).contiguous()
+        return lib.pa_copy_blocks(fake, fake, None, None, t.data_ptr(), t.shape[0], N, block_bytes, 0, None)
+
+    assert copy([[1, 2], [3, 2]]) == pa.PA_ERR_INVALID_ARG  # two pairs write block 2
+    assert copy([[1, 2], [2, 3]]) == pa.PA_ERR_INVALID_ARG  # block 2 read and written
+    assert copy([[1, 10]]) == pa.PA_ERR_OUT_OF_RANGE
+    assert copy([[-1, 3]]) == pa.PA_ERR_OUT_OF_RANGE
+    assert copy([[1, 2]], block_bytes=100) == pa.PA_ERR_INVALID_ARG
+
+
+def test_binding_rejects_host_tensors(lib):
+    import paged_kv_cache_197_gb300 as pa
+
+    x = torch.zeros((2, 4, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pa.pa_decode(x, x, x, x, x, x, 0.1, 16)

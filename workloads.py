@@ -93,8 +93,9 @@ def build_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, context_le
     sequence point at the same physical blocks.  With ``cow`` each sequence's
     last logical block gets a (src, dst) copy-on-write pair: the cache content is
     written into src, the decode table already points at dst.  With ``poison``
-    every slot that holds no valid token is filled with bf16 NaN, so a kernel that
-    reads past a context shows up in the results.
+    every slot of a bf16 pool that holds no valid token is filled with bf16 NaN, so a
+    kernel that reads past a context shows up in the results (int8 pools are quantised
+    from a finite source; the tests poison their scales instead).
     """
     meta_gen = _gen(seed)  # small metadata always on the CPU generator
     ctx = torch.as_tensor(context_lens, dtype=torch.int64).clone()
@@ -146,7 +147,7 @@ def build_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, context_le
             pos = c - 1
             slots[s] = int(tables[s, pos // bs]) * bs + pos % bs
 
-    if poison:
+    if poison and kv_dtype == "bf16":  # int8 sources stay finite: tests poison their scales
         valid = valid_slot_mask(content_tables, ctx - 1, bs, N)  # tokens present before the append
         bad = ~valid.to(device)
         nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
@@ -155,9 +156,10 @@ def build_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, context_le
             view[bad] = nan
     return PagedCase(name=name, S=S, Hq=Hq, Hkv=Hkv, D=D, bs=bs, N=N, M=M, kv_dtype=kv_dtype,
                      scale=scale if scale is not None else 1.0 / math.sqrt(D),
-                     q=q, k_pool=k_pool, v_pool=v_pool, block_tables=tables,
-                     context_lens=ctx.to(torch.int32), new_key=new_key, new_value=new_value,
-                     slot_mapping=slots, cow_pairs=cow_t, shared_prefix_blocks=n_shared,
+                     q=q, k_pool=k_pool, v_pool=v_pool, block_tables=tables.to(device),
+                     context_lens=ctx.to(torch.int32).to(device), new_key=new_key,
+                     new_value=new_value, slot_mapping=slots.to(device),
+                     cow_pairs=cow_t.to(device), shared_prefix_blocks=n_shared,
                      meta={"seed": seed, "content_tables": content_tables,
                            "prefix_tokens": prefix_tokens})
 
