@@ -70,6 +70,26 @@ def decode_source_hash() -> str:
     return hashlib.sha256(src.read_bytes()).hexdigest()[:16]
 
 
+# ------------------------------------------------------- replicas across ranks
+def replica_seed(seed: int, rank: int) -> int:
+    """Each rank decodes its own batch of sequences (independent shards, weak scaling)."""
+    return seed + 1000 * rank
+
+
+def slowest_rank(values, device) -> list[float]:
+    """Element-wise maximum over all ranks (the job is as slow as its slowest rank)."""
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized() \
+            and torch.distributed.get_world_size() > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_step_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Bytes all ranks moved per step over the slowest rank's step time, in GB/s."""
+    return bytes_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clock sampler
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 100 ms in the background."""
@@ -151,6 +171,9 @@ class Step:
             pa.pa_quantize_kv(rows(c.k_pool), rows(c.v_pool), self.k_cache, self.v_cache,
                               self.k_scale, self.v_scale, slots, stream=stream)
             torch.cuda.synchronize(device)
+            self.source = (c.k_pool.cpu(), c.v_pool.cpu())  # for the CPU baseline only
+            c.k_pool = c.v_pool = None  # the bf16 source is not part of the step
+            torch.cuda.empty_cache()
         else:
             self.k_cache, self.v_cache = c.k_pool, c.v_pool
             self.k_scale = self.v_scale = None
@@ -205,7 +228,7 @@ def run_ours(args, rank, world, device) -> dict | None:
     stream = torch.cuda.Stream(device)
     maker = workloads.CONFIGS[args.config]
     with torch.cuda.stream(stream):
-        case = maker(seed=args.seed + 1000 * rank, device=device, poison=False)
+        case = maker(seed=replica_seed(args.seed, rank), device=device, poison=False)
         torch.cuda.synchronize(device)
         step = Step(case, device, stream)
     nbytes = step_bytes(case)
@@ -220,10 +243,12 @@ def run_ours(args, rank, world, device) -> dict | None:
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
     time.sleep(0.3)
-    # warm-up: at least W steps and at least half a second, so the clocks settle
+    # warm-up: at least W steps and (unless --quick) at least half a second, so the
+    # clocks settle
     t_w = time.time()
     n = 0
-    while n < args.warmup or time.time() - t_w < 0.5:
+    settle = 0.0 if args.quick else 0.5
+    while n < args.warmup or time.time() - t_w < settle:
         with torch.cuda.stream(stream):
             step.run()
         n += 1
@@ -258,13 +283,10 @@ def run_ours(args, rank, world, device) -> dict | None:
     assert int(step.flag.item()) == 0, f"kernel error flag {int(step.flag.item())}"
 
     # slowest rank sets the job time
-    t = torch.tensor([total_ms, statistics.mean(dec_ms)], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms, dec_mean_ms = float(t[0]), float(t[1])
+    total_ms, dec_mean_ms = slowest_rank([total_ms, statistics.mean(dec_ms)], device)
     ms_per_step = total_ms / args.steps
 
-    e2e = run_e2e(args, step, case, device, stream, world)
+    e2e = None if args.quick else run_e2e(args, step, case, device, stream, world)
     if rank != 0:
         return None
 
@@ -272,7 +294,7 @@ def run_ours(args, rank, world, device) -> dict | None:
     achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
     src_hash = decode_source_hash()
     traffic = NCU_TRAFFIC.get((args.config, src_hash))
-    value = nbytes["total"] * world / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(nbytes["total"], world, ms_per_step)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -299,7 +321,7 @@ def run_ours(args, rank, world, device) -> dict | None:
     if args.config == "prefix":
         res["roofline"]["achieved_unique_bytes"] = round(
             nbytes["decode_unique"] / (dec_mean_ms * 1e-3) / 1e9, 1)
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and not args.quick and world == 1:
         res["cpu_baseline"] = cpu_baseline(args, case, step, budget_s=args.cpu_seconds)
     return res
 
@@ -335,13 +357,9 @@ def run_e2e(args, step, case, device, stream, world) -> dict:
             one()
         b.record(stream)
         torch.cuda.synchronize(device)
-    ms = a.elapsed_time(b) / steps
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(t[0])
+    ms = slowest_rank([a.elapsed_time(b) / steps], device)[0]
     total = step_bytes(case)["total"]
-    return {"value": round(total * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+    return {"value": round(whole_job_gbs(total, world, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
             "steps": steps}
 
@@ -358,8 +376,9 @@ def oracle_sample_inputs(case, step=None):
         import oracle
 
         orc = oracle.load()
-        kc, ks = orc.quantize_pool(bits(case.k_pool))
-        vc, vs = orc.quantize_pool(bits(case.v_pool))
+        k_src, v_src = step.source if step is not None else (case.k_pool, case.v_pool)
+        kc, ks = orc.quantize_pool(bits(k_src))
+        vc, vs = orc.quantize_pool(bits(v_src))
         return bits(case.q), kc, vc, ks, vs
     return bits(case.q), bits(case.k_pool), bits(case.v_pool), None, None
 
@@ -383,6 +402,15 @@ def time_oracle(case, inputs, budget_s: float) -> dict:
         if elapsed >= budget_s / 4 or n >= case.S:
             break
         n = min(case.S, max(n + 1, int(n * min(8.0, (budget_s / 4) / max(elapsed, 1e-3)))))
+    # repeat the sample until about budget_s of CPU time is spent; report the mean
+    reps, total = 1, elapsed
+    while total < budget_s:
+        t0 = time.perf_counter()
+        orc.paged_attention(np.ascontiguousarray(q[:n]), kc, vc, np.ascontiguousarray(tables[:n]),
+                            np.ascontiguousarray(lens[:n]), case.scale, k_scale=ks, v_scale=vs)
+        total += time.perf_counter() - t0
+        reps += 1
+    elapsed = total / reps
     sub = workloads.PagedCase(**{**case.__dict__})
     sub.S = n
     sub.context_lens = case.context_lens[:n].cpu()
@@ -390,7 +418,7 @@ def time_oracle(case, inputs, budget_s: float) -> dict:
     sub.block_tables = case.block_tables[:n].cpu()
     nbytes = workloads.decode_algorithmic_bytes(sub)
     return {"value": round(nbytes / elapsed / 1e9, 4), "unit": UNIT, "cores": orc.num_threads,
-            "kind": "oracle", "seconds": round(elapsed, 3),
+            "kind": "oracle", "seconds": round(elapsed, 3), "repeats": reps,
             "sample": f"decode of the first {n} of {case.S} sequences "
                       f"({int(sub.context_lens.sum())} context tokens), fp64 C oracle, "
                       f"caches resident in host memory"}
@@ -453,6 +481,8 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="exactly W warm-up steps, no end-to-end or CPU legs (for profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
