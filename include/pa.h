@@ -171,6 +171,36 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
                     float scale, int max_context_len, void *workspace, size_t workspace_bytes,
                     int *err_flag, void *stream);
 
+/*
+ * Paged decode without any allocation: the same computation, arguments and
+ * results as pa_decode, for callers that cannot allocate device memory and so
+ * cannot provide pa_decode's workspace (a host application that owns every
+ * allocation, a fixed memory budget, or capture code that may not allocate).
+ * The source pages have no counterpart: this is a packaging of pa_decode.
+ *
+ * The split-K scratch lives in a fixed array inside the library, of
+ * PA_NOALLOC_SCRATCH_BYTES bytes per GPU; every GPU that loads the library holds
+ * it until the process exits.  Sizes whose scratch (pa_decode_workspace_size)
+ * exceeds it are rejected with PA_ERR_UNSUPPORTED before anything is queued; use
+ * pa_decode with a caller-owned workspace for those.  The call allocates nothing
+ * and calls no allocating CUDA or library routine.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and remembers it; make that first call before any stream
+ * capture.  All calls on a device share the one array, so calls that overlap on
+ * the GPU (on different streams, or from different threads without ordering) race
+ * and may corrupt each other's results; order them on one stream.  Nothing in the
+ * array needs to start at zero: each call writes every partial result it reads.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pa_status pa_decode_noalloc(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
+                            const void *v_cache, const float *k_scale, const float *v_scale,
+                            int kv_dtype, const int32_t *block_tables, int M,
+                            const int32_t *context_lens, int S, int Hq, int Hkv, int D, int bs,
+                            int N, float scale, int max_context_len, int *err_flag,
+                            void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,9 @@ PA_FLAG_BLOCK_OUT_OF_RANGE = 2
 PA_FLAG_CONTEXT_OUT_OF_RANGE = 4
 
 EXPORTED = ["pa_version", "pa_status_string", "pa_last_error_string", "pa_reshape_and_cache",
-            "pa_quantize_kv", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode"]
+            "pa_quantize_kv", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",
+            "pa_decode_noalloc"]
+PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class PagedAttentionError(RuntimeError):
@@ -67,6 +69,9 @@ def load_library(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                               i32, f32, i32, vp, sz, vp, vp]
     lib.pa_decode.restype = i32
+    lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
+                                      i32, i32, f32, i32, vp, vp]
+    lib.pa_decode_noalloc.restype = i32
     if path is None:
         _LIB = lib
     return lib
@@ -219,6 +224,38 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: f
                          _ptr(v_scale), kv_dtype, _ptr(block_tables), M, _ptr(context_lens), S, Hq,
                          Hkv, D, bs, N, float(scale), int(max_context_len), _ptr(workspace),
                          ws_bytes, _flag(err_flag), _stream(stream, query.device)))
+
+
+def pa_decode_noalloc(out, query, k_cache, v_cache, block_tables, context_lens, scale: float,
+                      max_context_len: int, k_scale=None, v_scale=None, err_flag=None,
+                      stream=None) -> None:
+    """pa_decode for callers that cannot allocate: the library's own fixed scratch array
+    (PA_NOALLOC_SCRATCH_BYTES per GPU) replaces the workspace.  Calls sharing a device
+    must not overlap on the GPU."""
+    _cuda(out, "out", torch.bfloat16, 3)
+    _cuda(query, "query", torch.bfloat16, 3)
+    kv_dtype = PA_KV_INT8 if k_cache.dtype == torch.int8 else PA_KV_BF16
+    cache_dtype = torch.int8 if kv_dtype == PA_KV_INT8 else torch.bfloat16
+    _cuda(k_cache, "k_cache", cache_dtype, 4)
+    _cuda(v_cache, "v_cache", cache_dtype, 4)
+    _cuda(block_tables, "block_tables", torch.int32, 2)
+    _cuda(context_lens, "context_lens", torch.int32, 1)
+    if kv_dtype == PA_KV_INT8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an int8 cache needs k_scale and v_scale")
+        _cuda(k_scale, "k_scale", torch.float32, 3)
+        _cuda(v_scale, "v_scale", torch.float32, 3)
+    S, Hq, D = query.shape
+    N, Hkv, bs, D2 = k_cache.shape
+    if out.shape != query.shape or v_cache.shape != k_cache.shape or D2 != D \
+            or block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("pa_decode_noalloc: shape mismatch")
+    lib = load_library()
+    _check(lib.pa_decode_noalloc(_ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(k_scale), _ptr(v_scale), kv_dtype, _ptr(block_tables),
+                                 block_tables.shape[1], _ptr(context_lens), S, Hq, Hkv, D, bs, N,
+                                 float(scale), int(max_context_len), _flag(err_flag),
+                                 _stream(stream, query.device)))
 
 
 def decode_workspace(query, k_cache, max_context_len: int) -> torch.Tensor | None:
