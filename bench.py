@@ -182,8 +182,9 @@ class Step:
         self.ws = pa.decode_workspace(c.q, self.k_cache, self.max_ctx)
         self.flag = torch.zeros(1, dtype=torch.int32, device=device)
         self.cow = c.cow_pairs.cpu()
-        plan_parts = math.ceil(self.max_ctx / 512)
-        self.launches = (1 + 1 + (1 if plan_parts > 1 else 0)
+        # append (or quantise-append) + decode (+ merge when split) + COW copies
+        ws_bytes = 0 if self.ws is None else self.ws.numel()
+        self.launches = (1 + 1 + (1 if ws_bytes else 0)
                          + (math.ceil(self.cow.shape[0] / 256) if self.cow.shape[0] else 0))
 
     def write_cache(self, new_key, new_value, slots):

@@ -31,17 +31,31 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Split of long contexts: each CTA handles one partition of one (sequence, kv head,
+// query-head chunk) unit.  A CTA pays a pipeline ramp-up (its first tiles' latency)
+// and a partial result per head, so partitions are taken as long as possible while
+// the grid still holds at least kTargetCtas CTAs (three waves of two 4-warp CTAs on
+// each of GB300's 152 SMs) for the longest context; shorter sequences use fewer
+// partitions.  Measured on the Llama-2-13B-shaped workload: 512-token partitions
+// 6.15 TB/s, one 2048-token partition 6.55 TB/s.
+constexpr int64_t kTargetCtas = 912;
+constexpr int kPartChoices[] = {4096, 2048, 1024, 512, 256};
+
 DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len) {
     (void)bs;
     (void)kv_dtype;
     DecodePlan p{};
     const int G = Hq / Hkv;
     p.head_chunks = (G + 7) / 8;
-    // Partitions of 512 tokens: 32 blocks of 16 (or 16 of 32) per CTA, i.e. 8 or 4
-    // tiles for each of the CTA's 4 warps.  Long contexts are split so that a batch
-    // of few sequences still spreads over all SMs; the partial results cost
-    // (D + 2) fp32 per query head and partition, under 3% of the K/V bytes.
-    p.part_tokens = 512;
+    const int64_t units = (int64_t)S * Hkv * p.head_chunks;
+    p.part_tokens = 256;
+    for (int cand : kPartChoices) {
+        const int64_t parts = (max_context_len + cand - 1) / cand;
+        if (units * std::max<int64_t>(parts, 1) >= kTargetCtas) {
+            p.part_tokens = cand;
+            break;
+        }
+    }
     p.max_parts = std::max(1, (max_context_len + p.part_tokens - 1) / p.part_tokens);
     if (p.max_parts == 1) {
         p.ws_acc_off = p.ws_ml_off = p.ws_bytes = 0;
@@ -219,6 +233,8 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
         return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (kv_dtype == PA_KV_INT8 && (!k_scale || !v_scale))
         return fail(PA_ERR_INVALID_ARG, "%s: int8 cache needs k_scale and v_scale", fn);
+    if (kv_dtype == PA_KV_INT8 && (!aligned16(k_scale) || !aligned16(v_scale)))
+        return fail(PA_ERR_INVALID_ARG, "%s: scales must be 16-byte aligned", fn);
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
     if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())

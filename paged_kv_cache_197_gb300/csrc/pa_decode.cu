@@ -11,7 +11,7 @@
 //
 // Design (decode is bound by HBM bandwidth; every K/V byte is read once):
 //   * One CTA of 4 warps per (sequence, kv head, group of <= 8 query heads,
-//     partition of 512 tokens).  Warps take the partition's tiles round-robin and
+//     partition of 256 to 4096 tokens, chosen on the host).  Warps take the partition's tiles round-robin and
 //     each keeps its own online-softmax state; the CTA merges its warps in shared
 //     memory.  Longer contexts are split over several CTAs whose partial results
 //     (unnormalised output, running max, running sum) a second kernel merges by
@@ -41,7 +41,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxPartBlocks = 64;
+constexpr int kMaxPartBlocks = 256;  // 4096-token partitions of 16-token blocks
 constexpr int kHeadsPerCta = 8;
 
 // ------------------------------------------------------------------- PTX wrappers
@@ -364,13 +364,13 @@ paged_decode_kernel(const DecodeArgs a) {
     const int h0 = kvh * a.G + chunk * kHeadsPerCta;
     const int nh = min(kHeadsPerCta, a.G - chunk * kHeadsPerCta);
 
-    if (tid < nblk) {
-        int b = a.block_tables[(int64_t)s * a.M + blk_begin + tid];
+    for (int i = tid; i < nblk; i += kThreads) {
+        int b = a.block_tables[(int64_t)s * a.M + blk_begin + i];
         if (b < 0 || b >= a.N) {
             if (chunk == 0) raise_flag(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
             b = -1;
         }
-        s_blk[tid] = b;
+        s_blk[i] = b;
     }
 
     // q fragments: lane (g, t) holds head g's values at the K-row positions it owns
@@ -528,7 +528,7 @@ cudaError_t launch_bs(const DecodeArgs &a, int bs, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
-    static_assert(kMaxPartBlocks * 16 >= 512, "partition block list fits in shared memory");
+    static_assert(kMaxPartBlocks * 16 >= 4096, "partition block list fits in shared memory");
     if (kv_dtype == PA_KV_BF16)
         return D == 128 ? launch_bs<uint16_t, 128>(a, bs, stream) : launch_bs<uint16_t, 64>(a, bs, stream);
     return D == 128 ? launch_bs<int8_t, 128>(a, bs, stream) : launch_bs<int8_t, 64>(a, bs, stream);

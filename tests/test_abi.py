@@ -73,12 +73,21 @@ def test_decode_host_checks(lib):
 
 
 def test_workspace_size(lib):
+    """Partitions are as long as possible while the grid keeps >= 912 CTAs; the workspace
+    holds (D + 2) fp32 per query head and partition."""
     import paged_kv_cache_197_gb300 as pa
 
-    assert pa.pa_decode_workspace_size(64, 40, 40, 128, 16, pa.PA_KV_BF16, 512) == 0
+    # 64 x 40 units already fill the GPU: one partition, no workspace
+    assert pa.pa_decode_workspace_size(64, 40, 40, 128, 16, pa.PA_KV_BF16, 2048) == 0
+    # 20 x 8 units of 8000 tokens: 1024-token partitions (1280 CTAs) -> 8 partitions
     n = pa.pa_decode_workspace_size(20, 64, 8, 128, 16, pa.PA_KV_BF16, 8000)
-    rows = 20 * 64 * 16  # 16 partitions of 512 tokens
-    assert n >= rows * (128 + 2) * 4 and n % 256 == 0
+    rows = 20 * 64 * 8
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert n == up(up(rows * 128 * 4) + rows * 2 * 4)
+    # few units: 256-token partitions
+    n = pa.pa_decode_workspace_size(2, 8, 2, 64, 16, pa.PA_KV_BF16, 1000)
+    rows = 2 * 8 * 4
+    assert n == up(up(rows * 64 * 4) + rows * 2 * 4)
     assert pa.pa_decode_workspace_size(1, 3, 2, 128, 16, 0, 100) == 0  # invalid -> 0
 
 

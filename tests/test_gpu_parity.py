@@ -119,15 +119,17 @@ def test_error_flags_and_skips():
     tables = case.block_tables.clone()
     tables[1, 1] = case.N + 100
     out = torch.empty_like(case.q)
+    ws = pa.decode_workspace(case.q, k, 40)
     flag.zero_()
-    pa.pa_decode(out, case.q, k, v, tables, case.context_lens, case.scale, 40, err_flag=flag)
+    pa.pa_decode(out, case.q, k, v, tables, case.context_lens, case.scale, 40, workspace=ws,
+                 err_flag=flag)
     torch.cuda.synchronize()
     assert flag.item() == pa.PA_FLAG_BLOCK_OUT_OF_RANGE
     assert torch.isfinite(out.float()).all()
     # a context longer than max_context_len is clamped and flagged
     flag.zero_()
     pa.pa_decode(out, case.q, k, v, case.block_tables, case.context_lens, case.scale, 33,
-                 err_flag=flag)
+                 workspace=ws, err_flag=flag)
     torch.cuda.synchronize()
     assert flag.item() == pa.PA_FLAG_CONTEXT_OUT_OF_RANGE
 
