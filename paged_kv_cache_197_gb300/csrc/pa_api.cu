@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <vector>
 
 #include "pa_internal.cuh"
@@ -32,14 +33,37 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Split of long contexts: each CTA handles one partition of one (sequence, kv head,
-// query-head chunk) unit.  A CTA pays a pipeline ramp-up (its first tiles' latency)
-// and a partial result per head, so partitions are taken as long as possible while
-// the grid still holds at least kTargetCtas CTAs (three waves of two 4-warp CTAs on
-// each of GB300's 152 SMs) for the longest context; shorter sequences use fewer
-// partitions.  Measured on the Llama-2-13B-shaped workload: 512-token partitions
-// 6.15 TB/s, one 2048-token partition 6.55 TB/s.
-constexpr int64_t kTargetCtas = 912;
-constexpr int kPartChoices[] = {4096, 2048, 1024, 512, 256};
+// query-head chunk) unit.  A CTA pays a pipeline ramp-up (its first tiles' latency,
+// worth about 64 tokens of streaming) and a partial result per head, so long
+// partitions are cheaper; but the grid must hold at least three waves of CTAs
+// (2 resident per SM), and a last wave that is mostly empty wastes the difference.
+// Each candidate length is scored by (fraction of the last wave in use) x
+// (length / (length + 64)) for the longest context, and the best is taken.
+// When the units alone give six waves and contexts are at most 4096 tokens there is
+// no split at all (no merge launch).  Measured on GB300 for Llama-2-13B-shaped decode:
+// 512-token partitions 6.15 TB/s, one 2048-token partition 6.55 TB/s; Llama-3-70B-
+// shaped: 1024 -> 5.67, 768 -> 5.71.
+constexpr int kPartChoices[] = {4096, 3072, 2048, 1536, 1024, 768, 512, 384, 256};
+constexpr int kRampTokens = 64;
+constexpr int kCtasPerSm = 2;
+
+static int device_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();  // no device here: plan for GB300's 152 SMs
+        return 152;
+    }
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 152;
+        }
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
 
 DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len) {
     (void)bs;
@@ -48,12 +72,25 @@ DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int 
     const int G = Hq / Hkv;
     p.head_chunks = (G + 7) / 8;
     const int64_t units = (int64_t)S * Hkv * p.head_chunks;
-    p.part_tokens = 256;
+    const double slots = (double)device_sms() * kCtasPerSm;
+    p.part_tokens = kPartChoices[sizeof(kPartChoices) / sizeof(int) - 1];
+    double best = -1.0;
+    if ((double)units >= 6.0 * slots && max_context_len <= 4096) {
+        // enough units of bounded length to keep every SM busy: no split, no merge
+        p.part_tokens = std::max(max_context_len, 1);
+        best = 1.0;
+    }
     for (int cand : kPartChoices) {
-        const int64_t parts = (max_context_len + cand - 1) / cand;
-        if (units * std::max<int64_t>(parts, 1) >= kTargetCtas) {
+        if (best >= 1.0) break;
+        const int64_t parts = std::max<int64_t>(1, (max_context_len + cand - 1) / cand);
+        const double waves = (double)(units * parts) / slots;
+        if (waves < 3.0) continue;
+        const double fill = waves / std::ceil(waves);
+        const double len = (double)std::min(cand, std::max(max_context_len, 1));
+        const double score = fill * len / (len + kRampTokens);
+        if (score > best + 1e-9) {
+            best = score;
             p.part_tokens = cand;
-            break;
         }
     }
     p.max_parts = std::max(1, (max_context_len + p.part_tokens - 1) / p.part_tokens);

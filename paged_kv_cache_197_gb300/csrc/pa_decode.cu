@@ -32,6 +32,7 @@
 //   * int8 entries are turned into exact bf16 integers with integer ops; the key
 //     scale multiplies the score, the value scale multiplies the softmax weight.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "pa_internal.cuh"
@@ -76,6 +77,16 @@ __device__ __forceinline__ void mma_bf16(float *c, uint32_t a0, uint32_t a1, uin
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A . B + D, A 16x16 fp16 (row), B 16x8 fp16 (col), D 16x8 fp32.
+__device__ __forceinline__ void mma_f16(float *c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Transpose an 8x8 matrix of 16-bit values held one row pair per lane.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
     uint32_t d;
@@ -89,21 +100,41 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Byte 0 and byte 2 of t hold signed int8 values a and b (bytes 1 and 3 are
-// ignored).  Returns the bf16 pair (a, b), exactly: 128 + (x & 127) and 128 or 256
-// (by the sign bit) are both exact bf16 values, and so is their difference x.
-__device__ __forceinline__ uint32_t i8pair_to_bf16x2(uint32_t t) {
-    const uint32_t mag = (t & 0x007f007fu) | 0x43004300u;
-    const uint32_t bias = (t & 0x00800080u) | 0x43004300u;
-    __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162 *>(&mag);
-    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&bias);
-    __nv_bfloat162 r = __hsub2(m, b);
-    return *reinterpret_cast<uint32_t *>(&r);
+// int8 -> fp16, exactly.  The fp16 bit pattern 0x64XX is 1024 + XX for XX in
+// [0, 255]; with XX = x + 128 (the int8 byte with its top bit flipped) the value is
+// 1152 + x, and subtracting 1152 leaves x.
+__device__ __forceinline__ uint32_t biased_to_f16x2(uint32_t t) {
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&t), __half2half2(__ushort_as_half(0x6480)));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+// The four int8 values of word w (one K row) as the fp16 pairs (w0, w1), (w2, w3).
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    lo = biased_to_f16x2(__byte_perm(u, 0x64646464u, 0x4140));
+    hi = biased_to_f16x2(__byte_perm(u, 0x64646464u, 0x4342));
+}
+
+// Byte 0 and byte 2 of t hold int8 values a and b (bytes 1 and 3 are ignored):
+// the fp16 pair (a, b).  One logic op flips the top bits and writes the 0x64 bytes.
+__device__ __forceinline__ uint32_t i8pair_to_f16x2(uint32_t t) {
+    const uint32_t m = 0x00ff00ffu, c = 0x64806480u;
+    return biased_to_f16x2((m & (t ^ c)) | (~m & c));
+}
+
+// Exponent e with |x| < 2^e for a finite, positive x (normal range).
+__device__ __forceinline__ int exponent_above(float x) {
+    return (int)((__float_as_uint(x) >> 23) & 0xffu) - 126;
 }
 
 __device__ __forceinline__ void raise_flag(int *err_flag, int bit) {
@@ -217,6 +248,7 @@ struct WarpState {
     float o[D / 16][4];  // O^T fragments: [d tile][c0..c3]
     float m[2];          // running max of heads 2t, 2t+1 (log2 units)
     float l[2];          // running sum, partial over this lane's tokens
+    int ve;              // int8: O is kept in units of 2^ve (ve >= exponent of every value scale so far)
 };
 
 template <typename KV, int D, int TILE>
@@ -237,14 +269,12 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
                 a2 = R.k[2 * s][2 * kc + 1];
                 a1 = R.k[2 * s + 1][2 * kc];
                 a3 = R.k[2 * s + 1][2 * kc + 1];
+                mma_bf16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
             } else {
-                const uint32_t w0 = R.k[2 * s][kc], w1 = R.k[2 * s + 1][kc];
-                a0 = i8pair_to_bf16x2(__byte_perm(w0, 0, 0x0100));
-                a2 = i8pair_to_bf16x2(__byte_perm(w0, 0, 0x0302));
-                a1 = i8pair_to_bf16x2(__byte_perm(w1, 0, 0x0100));
-                a3 = i8pair_to_bf16x2(__byte_perm(w1, 0, 0x0302));
+                i8x4_to_f16(R.k[2 * s][kc], a0, a2);
+                i8x4_to_f16(R.k[2 * s + 1][kc], a1, a3);
+                mma_f16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
             }
-            mma_bf16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
         }
     }
     // ---- online softmax over the tile (log2 domain)
@@ -286,6 +316,29 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
         st.l[0] *= alpha[0];
         st.l[1] *= alpha[1];
     }
+    // int8: keep the weights p * v_scale below 1 in fp16 by working in units of 2^ve,
+    // ve the exponent of the largest value scale seen so far (O rescaled when it grows)
+    float vmul = 1.0f;
+    if constexpr (G_::ELEM == 1) {
+        float vmax = (int)(threadIdx.x & 31) < R.nvalid ? R.vs : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        if (vmax > 0.0f) {
+            const int e = exponent_above(vmax);
+            if (e > st.ve) {
+                const float f = st.ve < -200 ? 0.0f : ldexpf(1.0f, st.ve - e);
+#pragma unroll
+                for (int mt = 0; mt < G_::MT; ++mt) {
+                    st.o[mt][0] *= f;
+                    st.o[mt][1] *= f;
+                    st.o[mt][2] *= f;
+                    st.o[mt][3] *= f;
+                }
+                st.ve = e;
+            }
+        }
+        vmul = ldexpf(1.0f, -st.ve);
+    }
     // ---- values: zero rows past the context (they may hold any bit pattern)
     if (R.nvalid < TILE) {
 #pragma unroll
@@ -304,12 +357,18 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
             if constexpr (G_::ELEM == 1) {
                 const int tok = 16 * s + g + 8 * (c >> 1);
                 const float vsc = __shfl_sync(0xffffffffu, R.vs, tok);
-                p[c] = tok < R.nvalid ? p[c] * vsc : 0.0f;
+                p[c] = tok < R.nvalid ? p[c] * (vsc * vmul) : 0.0f;
             }
         }
         // P[head][token] as the B operand: transpose the [token][head] quarters
-        const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
-        const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
+        uint32_t b0, b1;
+        if constexpr (G_::ELEM == 2) {
+            b0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
+            b1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
+        } else {
+            b0 = movmatrix_trans(pack_f16x2(p[0], p[1]));
+            b1 = movmatrix_trans(pack_f16x2(p[2], p[3]));
+        }
         const int j0 = 4 * s;  // V rows 2t, 2t+1, 2t+8, 2t+9 of this sub-tile
 #pragma unroll
         for (int mt = 0; mt < G_::MT; ++mt) {
@@ -327,12 +386,15 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
                 const uint32_t b = 2u * (mt & 1);
                 const uint32_t sel0 = b | ((4u + b) << 8);
                 const uint32_t sel1 = (b + 1u) | ((5u + b) << 8);
-                a0 = i8pair_to_bf16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel0));
-                a1 = i8pair_to_bf16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel1));
-                a2 = i8pair_to_bf16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel0));
-                a3 = i8pair_to_bf16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel1));
+                a0 = i8pair_to_f16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel0));
+                a1 = i8pair_to_f16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel1));
+                a2 = i8pair_to_f16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel0));
+                a3 = i8pair_to_f16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel1));
             }
-            mma_bf16(st.o[mt], a0, a1, a2, a3, b0, b1);
+            if constexpr (G_::ELEM == 2)
+                mma_bf16(st.o[mt], a0, a1, a2, a3, b0, b1);
+            else
+                mma_f16(st.o[mt], a0, a1, a2, a3, b0, b1);
         }
     }
 }
@@ -385,6 +447,23 @@ paged_decode_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int i = 0; i < G_::QW; ++i) qw[i] = 0u;
     }
+    float scale_log2 = a.scale_log2;
+    if constexpr (G_::ELEM == 1) {
+        // fp16 q for the int8 products: scaled by 2^sig so the largest |q| of the CTA's
+        // heads lands in [2^13, 2^14); the scores are scaled back by 2^-sig
+        float qmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < G_::QW; ++i)
+            qmax = fmaxf(qmax, fmaxf(fabsf(__uint_as_float(qw[i] << 16)), fabsf(__uint_as_float(qw[i] & 0xffff0000u))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+        const int sig = qmax > 0.0f ? min(100, max(-100, 14 - exponent_above(qmax))) : 0;
+        const float up = ldexpf(1.0f, sig);
+#pragma unroll
+        for (int i = 0; i < G_::QW; ++i)
+            qw[i] = pack_f16x2(__uint_as_float(qw[i] << 16) * up, __uint_as_float(qw[i] & 0xffff0000u) * up);
+        scale_log2 *= ldexpf(1.0f, -sig);
+    }
     __syncthreads();
 
     WarpState<KV, D, TILE> st;
@@ -392,6 +471,7 @@ paged_decode_kernel(const DecodeArgs a) {
     for (int mt = 0; mt < G_::MT; ++mt) st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.0f;
+    st.ve = -1000;  // no value scale seen yet
 
     const int ntiles = (tok_end - tok_begin + TILE - 1) / TILE;
     Tile<G_> A, B;
@@ -400,12 +480,12 @@ paged_decode_kernel(const DecodeArgs a) {
     while (i < ntiles) {
         if (i + kWarps < ntiles)
             load_tile<KV, D, BS, TILE>(B, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE>(st, A, qw, a.scale_log2, g, t);
+        consume_tile<KV, D, TILE>(st, A, qw, scale_log2, g, t);
         i += kWarps;
         if (i >= ntiles) break;
         if (i + kWarps < ntiles)
             load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE>(st, B, qw, a.scale_log2, g, t);
+        consume_tile<KV, D, TILE>(st, B, qw, scale_log2, g, t);
         i += kWarps;
     }
 
@@ -422,11 +502,12 @@ paged_decode_kernel(const DecodeArgs a) {
         s_l[warp][2 * t] = st.l[0];
         s_l[warp][2 * t + 1] = st.l[1];
     }
+    const float oscale = (G_::ELEM == 1 && st.ve > -200) ? ldexpf(1.0f, st.ve) : 1.0f;
 #pragma unroll
     for (int mt = 0; mt < G_::MT; ++mt)
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-            s_o[warp][2 * t + (c & 1)][out_dim<G_::ELEM, D>(mt, g, c >> 1)] = st.o[mt][c];
+            s_o[warp][2 * t + (c & 1)][out_dim<G_::ELEM, D>(mt, g, c >> 1)] = st.o[mt][c] * oscale;
     __syncthreads();
 
     constexpr int DPT = D / 16;  // output values per thread: 16 threads per head

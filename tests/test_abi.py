@@ -73,21 +73,37 @@ def test_decode_host_checks(lib):
 
 
 def test_workspace_size(lib):
-    """Partitions are as long as possible while the grid keeps >= 912 CTAs; the workspace
-    holds (D + 2) fp32 per query head and partition."""
+    """Partition length: no split when the units alone give 6 waves of 2 CTAs per SM (152
+    SMs without a GPU) and contexts are <= 4096 tokens; else the best of (last-wave fill)
+    x (len / (len + 64)) among lengths giving >= 3 waves.  The workspace holds (D + 2)
+    fp32 per query head and partition."""
+    import math
+
     import paged_kv_cache_197_gb300 as pa
 
-    # 64 x 40 units already fill the GPU: one partition, no workspace
-    assert pa.pa_decode_workspace_size(64, 40, 40, 128, 16, pa.PA_KV_BF16, 2048) == 0
-    # 20 x 8 units of 8000 tokens: 1024-token partitions (1280 CTAs) -> 8 partitions
-    n = pa.pa_decode_workspace_size(20, 64, 8, 128, 16, pa.PA_KV_BF16, 8000)
-    rows = 20 * 64 * 8
+    def parts(units, max_ctx, slots=304):
+        if units >= 6 * slots and max_ctx <= 4096:
+            return 1
+        best, best_p = -1.0, 256
+        for cand in (4096, 3072, 2048, 1536, 1024, 768, 512, 384, 256):
+            n = max(1, -(-max_ctx // cand))
+            waves = units * n / slots
+            if waves < 3:
+                continue
+            ln = min(cand, max(max_ctx, 1))
+            score = waves / math.ceil(waves) * ln / (ln + 64)
+            if score > best + 1e-9:
+                best, best_p = score, cand
+        return max(1, -(-max_ctx // best_p))
+
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    assert n == up(up(rows * 128 * 4) + rows * 2 * 4)
-    # few units: 256-token partitions
-    n = pa.pa_decode_workspace_size(2, 8, 2, 64, 16, pa.PA_KV_BF16, 1000)
-    rows = 2 * 8 * 4
-    assert n == up(up(rows * 64 * 4) + rows * 2 * 4)
+    for S, Hq, Hkv, D, max_ctx in [(64, 40, 40, 128, 2048), (64, 40, 40, 128, 200), (20, 64, 8, 128, 8000), (256, 32, 8, 128, 32768), (2, 8, 2, 64, 1000),
+                                   (50, 32, 8, 128, 2512)]:
+        P = parts(S * Hkv * ((Hq // Hkv + 7) // 8), max_ctx)
+        rows = S * Hq * P
+        expect = 0 if P == 1 else up(up(rows * D * 4) + rows * 2 * 4)
+        assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, 16, pa.PA_KV_BF16, max_ctx) == expect
+    assert parts(160, 8000) == 11  # 768-token partitions for the 70B-shaped workload
     assert pa.pa_decode_workspace_size(1, 3, 2, 128, 16, 0, 100) == 0  # invalid -> 0
 
 
