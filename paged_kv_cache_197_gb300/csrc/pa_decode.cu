@@ -14,8 +14,8 @@
 //     partition of 256 to 4096 tokens, chosen on the host).  Warps take the partition's tiles round-robin and
 //     each keeps its own online-softmax state; the CTA merges its warps in shared
 //     memory.  Longer contexts are split over several CTAs whose partial results
-//     (unnormalised output, running max, running sum) a second kernel merges by
-//     log-sum-exp.
+//     (unnormalised output, running max, running sum) a second kernel, launched as a
+//     programmatic dependent, merges by log-sum-exp.
 //   * A tile is 16 tokens (bf16) or a whole block (int8) of one kv head: one
 //     contiguous run of bytes in the [N][Hkv][bs][D] cache.  Each lane loads its
 //     share with 16-byte loads straight into registers, in the layout the tensor-
@@ -489,6 +489,10 @@ paged_decode_kernel(const DecodeArgs a) {
         i += kWarps;
     }
 
+    // the dependent merge grid may launch once every CTA got here (it still waits for
+    // this grid to finish before reading)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // ---- per-warp totals, then merge the CTA's warps through shared memory
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -552,39 +556,66 @@ paged_decode_kernel(const DecodeArgs a) {
 
 // Log-sum-exp merge of the partitions of each (sequence, query head):
 // out = sum_p 2^(m_p - M) acc_p / sum_p 2^(m_p - M) l_p, M = max_p m_p.
-// D/4 threads per (sequence, head), 4 output values each.
+// One warp per (sequence, head): lane p holds partition p's (max, sum), 32 partitions
+// at a time, so the maximum and the weights come from shuffles, and every
+// partition's partial row is loaded independently of the others (no chain of
+// dependent loads).  Launched as a programmatic dependent of the decode kernel: its
+// launch overlaps the decode tail and it waits for the decode results here.
 template <int D, int BS>
-__global__ void __launch_bounds__(kThreads)
-merge_partitions_kernel(const DecodeArgs a) {
-    constexpr int TPH = D / 4;  // threads per head
-    constexpr int HPC = kThreads / TPH;
-    const int s = blockIdx.y;
-    const int h = blockIdx.x * HPC + threadIdx.x / TPH;
-    const int d0 = (threadIdx.x % TPH) * 4;
-    if (h >= a.Hq) return;
+__global__ void __launch_bounds__(128) merge_partitions_kernel(const __grid_constant__ DecodeArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int PER = D / 32;  // output values per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t pair = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // s * Hq + h
+    if (pair >= (int64_t)a.S * a.Hq) return;
+    const int s = (int)(pair / a.Hq);
     const int ctx = checked_context(a, s, BS, false);
     const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
     if (nparts <= 1) return;  // the decode kernel wrote the output itself
-    const int64_t row0 = ((int64_t)s * a.Hq + h) * a.max_parts;
+    const int64_t row0 = pair * a.max_parts;
     float mmax = -INFINITY;
-    for (int p = 0; p < nparts; ++p) mmax = fmaxf(mmax, a.ws_ml[(row0 + p) * 2]);
+    for (int p = lane; p < nparts; p += 32) mmax = fmaxf(mmax, a.ws_ml[(row0 + p) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
     const float mbase = mmax == -INFINITY ? 0.0f : mmax;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
     float lsum = 0.0f;
-    for (int p = 0; p < nparts; ++p) {
-        const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + (row0 + p) * 2);
-        const float f = fast_exp2(ml.x - mbase);
-        lsum += f * ml.y;
-        const float4 v = *reinterpret_cast<const float4 *>(a.ws_acc + (row0 + p) * D + d0);
-        acc.x += f * v.x;
-        acc.y += f * v.y;
-        acc.z += f * v.z;
-        acc.w += f * v.w;
+    for (int p0 = 0; p0 < nparts; p0 += 32) {
+        float f = 0.0f;
+        if (p0 + lane < nparts) {
+            const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + (row0 + p0 + lane) * 2);
+            f = fast_exp2(ml.x - mbase);
+            lsum += f * ml.y;
+        }
+        const int cnt = min(32, nparts - p0);
+#pragma unroll 4
+        for (int q = 0; q < cnt; ++q) {
+            const float fq = __shfl_sync(0xffffffffu, f, q);
+            const float *src = a.ws_acc + (row0 + p0 + q) * D + lane * PER;
+            if constexpr (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] += fq * v.x;
+                acc[1] += fq * v.y;
+                acc[2] += fq * v.z;
+                acc[3] += fq * v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                acc[0] += fq * v.x;
+                acc[1] += fq * v.y;
+            }
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-    uint16_t *dst = a.out + ((int64_t)s * a.Hq + h) * D + d0;
-    *reinterpret_cast<uint2 *>(dst) =
-        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    uint16_t *dst = a.out + pair * D + lane * PER;
+    if constexpr (PER == 4)
+        *reinterpret_cast<uint2 *>(dst) =
+            make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+    else
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
 }
 
 template <typename KV, int D, int BS, int TILE>
@@ -593,10 +624,17 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     paged_decode_kernel<KV, D, BS, TILE><<<grid, kThreads, 0, stream>>>(a);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || a.max_parts == 1) return err;
-    constexpr int HPC = kThreads / (D / 4);
-    dim3 mgrid((a.Hq + HPC - 1) / HPC, a.S);
-    merge_partitions_kernel<D, BS><<<mgrid, kThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(((int64_t)a.S * a.Hq + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_partitions_kernel<D, BS>, a);
 }
 
 template <typename KV, int D>
