@@ -54,7 +54,8 @@ typedef enum pa_status {
     PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad alignment, shape mismatch */
     PA_ERR_UNSUPPORTED = 2, /* head_dim, block size or kv dtype not compiled in */
     PA_ERR_OUT_OF_RANGE = 3, /* a host-visible index (block id, length) out of range */
-    PA_ERR_CUDA = 4          /* a CUDA launch failed; see pa_last_error_string() */
+    PA_ERR_CUDA = 4,         /* a CUDA launch failed; see pa_last_error_string() */
+    PA_ERR_NO_SPACE = 5      /* the block pool cannot hold the request (pa_blocks.h) */
 } pa_status;
 
 enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1 };

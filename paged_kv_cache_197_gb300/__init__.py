@@ -267,3 +267,110 @@ def decode_workspace(query, k_cache, max_context_len: int) -> torch.Tensor | Non
     if n == 0:
         return None
     return torch.empty(n, dtype=torch.uint8, device=query.device)
+
+
+# ------------------------------------------------------------------ block manager
+PA_ERR_NO_SPACE = 5
+BLOCK_MANAGER_EXPORTED = ["pa_bm_create", "pa_bm_destroy", "pa_bm_add_sequence", "pa_bm_append",
+                          "pa_bm_fork", "pa_bm_free", "pa_bm_block_table", "pa_bm_get_stats"]
+
+
+class BlockManagerStats(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int64) for name in (
+        "num_blocks", "free_blocks", "cached_blocks", "used_blocks", "used_slots", "cow_copies",
+        "prefix_lookup_blocks", "prefix_hit_blocks", "evictions")]
+
+    def as_dict(self) -> dict:
+        return {name: int(getattr(self, name)) for name, _ in self._fields_}
+
+
+def _bm_lib() -> ctypes.CDLL:
+    lib = load_library()
+    if not getattr(lib, "_bm_ready", False):
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        lib.pa_bm_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
+        lib.pa_bm_create.restype = i32
+        lib.pa_bm_destroy.argtypes = [vp]
+        lib.pa_bm_destroy.restype = None
+        lib.pa_bm_add_sequence.argtypes = [vp, i64, vp, i32, ctypes.POINTER(i32)]
+        lib.pa_bm_add_sequence.restype = i32
+        lib.pa_bm_append.argtypes = [vp, i64, vp, i32, vp, vp, i32, ctypes.POINTER(i32)]
+        lib.pa_bm_append.restype = i32
+        lib.pa_bm_fork.argtypes = [vp, i64, i64]
+        lib.pa_bm_fork.restype = i32
+        lib.pa_bm_free.argtypes = [vp, i64]
+        lib.pa_bm_free.restype = i32
+        lib.pa_bm_block_table.argtypes = [vp, i64, vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i64)]
+        lib.pa_bm_block_table.restype = i32
+        lib.pa_bm_get_stats.argtypes = [vp, ctypes.POINTER(BlockManagerStats)]
+        lib.pa_bm_get_stats.restype = i32
+        lib._bm_ready = True
+    return lib
+
+
+class BlockManager:
+    """Host block manager of include/pa_blocks.h (pool, tables, copy-on-write, prefix
+    cache, LRU eviction).  Token ids and slots are plain Python ints / lists."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = _bm_lib()
+        self._h = ctypes.c_void_p()
+        _check(self._lib.pa_bm_create(num_blocks, block_size, ctypes.byref(self._h)))
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pa_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+    @staticmethod
+    def _ids(tokens):
+        if tokens is None:
+            return None, 0
+        arr = (ctypes.c_int32 * len(tokens))(*tokens)
+        return arr, len(tokens)
+
+    def add_sequence(self, seq_id: int, prompt=None) -> int:
+        """Register a sequence; returns the number of prompt tokens found cached."""
+        arr, n = self._ids(prompt)
+        cached = ctypes.c_int(0)
+        _check(self._lib.pa_bm_add_sequence(self._h, seq_id, arr, n, ctypes.byref(cached)))
+        return cached.value
+
+    def append(self, seq_id: int, n: int | None = None, tokens=None):
+        """Append tokens (ids optional); returns (slots, cow_pairs)."""
+        if tokens is not None:
+            n = len(tokens)
+        arr, _ = self._ids(tokens)
+        slots = (ctypes.c_int64 * max(n, 1))()
+        cow = (ctypes.c_int64 * 2)()
+        n_cow = ctypes.c_int(0)
+        _check(self._lib.pa_bm_append(self._h, seq_id, arr, n, slots, cow, 1, ctypes.byref(n_cow)))
+        pairs = [(cow[0], cow[1])] if n_cow.value else []
+        return list(slots)[:n], pairs
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(self._lib.pa_bm_fork(self._h, parent, child))
+
+    def free(self, seq_id: int) -> None:
+        _check(self._lib.pa_bm_free(self._h, seq_id))
+
+    def block_table(self, seq_id: int):
+        n = ctypes.c_int(0)
+        length = ctypes.c_int64(0)
+        _check(self._lib.pa_bm_block_table(self._h, seq_id, None, 0, ctypes.byref(n), ctypes.byref(length)))
+        table = (ctypes.c_int32 * max(n.value, 1))()
+        _check(self._lib.pa_bm_block_table(self._h, seq_id, table, n.value, ctypes.byref(n),
+                                           ctypes.byref(length)))
+        return list(table)[: n.value], length.value
+
+    def stats(self) -> dict:
+        out = BlockManagerStats()
+        _check(self._lib.pa_bm_get_stats(self._h, ctypes.byref(out)))
+        return out.as_dict()

@@ -120,6 +120,7 @@ const char *pa_status_string(pa_status status) {
         case PA_ERR_UNSUPPORTED: return "unsupported configuration";
         case PA_ERR_OUT_OF_RANGE: return "index out of range";
         case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_NO_SPACE: return "block pool exhausted";
     }
     return "unknown status";
 }

@@ -134,6 +134,62 @@ def test_error_flags_and_skips():
     assert flag.item() == pa.PA_FLAG_CONTEXT_OUT_OF_RANGE
 
 
+def test_block_manager_plan_on_gpu(oracle):
+    """A prefix reuse, a fork and a copy-on-write planned by the host block manager and
+    executed by the CUDA library match the oracle executing the same plan."""
+    import paged_kv_cache_197_gb300 as pa
+
+    rng = np.random.default_rng(5)
+    bs, Hkv, Hq, D, N = 16, 4, 16, 128, 96
+    bm = pa.BlockManager(N, bs)
+    kc_h = np.zeros((N, Hkv, bs, D), dtype=np.uint16)
+    vc_h = np.zeros_like(kc_h)
+    kc = torch.zeros((N, Hkv, bs, D), dtype=torch.bfloat16, device=DEV)
+    vc = torch.zeros_like(kc)
+
+    def write(sid, n, tokens=None):
+        slots, pairs = bm.append(sid, n=n, tokens=tokens)
+        if pairs:
+            oracle.copy_blocks(kc_h, vc_h, np.array(pairs, dtype=np.int64))
+            pa.pa_copy_blocks(kc, vc, pairs)
+        k = helpers.bits(torch.randn((n, Hkv, D)).to(torch.bfloat16))
+        v = helpers.bits(torch.randn((n, Hkv, D)).to(torch.bfloat16))
+        sl = np.array(slots, dtype=np.int64)
+        oracle.reshape_and_cache(k, v, kc_h, vc_h, sl, bs)
+        kt = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).to(DEV)
+        vt = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(DEV)
+        pa.pa_reshape_and_cache(kt, vt, kc, vc, torch.from_numpy(sl).to(DEV))
+
+    prompt = list(range(600))
+    bm.add_sequence(0, prompt)
+    write(0, 600, prompt)
+    write(0, 9)
+    assert bm.add_sequence(1, prompt) == 592
+    write(1, 20)
+    bm.fork(0, 2)
+    write(2, 30)
+    write(0, 1)
+    tables = [bm.block_table(s) for s in (0, 1, 2)]
+    M = max(len(t) for t, _ in tables)
+    tab = np.zeros((3, M), dtype=np.int32)
+    for i, (t, _) in enumerate(tables):
+        tab[i, :len(t)] = t
+    lens = np.array([n for _, n in tables], dtype=np.int32)
+    q = helpers.bits(torch.randn((3, Hq, D)).to(torch.bfloat16))
+    torch.cuda.synchronize()
+    assert np.array_equal(helpers.bits(kc), kc_h) and np.array_equal(helpers.bits(vc), vc_h)
+    ref = oracle.paged_attention(q, kc_h, vc_h, tab, lens, 0.088)
+    qt = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(DEV)
+    out = torch.empty_like(qt)
+    tab_t, lens_t = torch.from_numpy(tab).to(DEV), torch.from_numpy(lens).to(DEV)
+    max_ctx = int(lens.max())
+    ws = pa.decode_workspace(qt, kc, max_ctx)
+    pa.pa_decode(out, qt, kc, vc, tab_t, lens_t, 0.088, max_ctx, workspace=ws)
+    torch.cuda.synchronize()
+    helpers.compare(out, ref, "bf16")
+    del rng
+
+
 def test_copy_blocks_rejects_overlap():
     import paged_kv_cache_197_gb300 as pa
 
