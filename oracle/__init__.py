@@ -24,6 +24,7 @@ LIBRARY = HERE / "liboracle.so"
 
 KV_BF16 = 0
 KV_INT8 = 1
+KV_FP8 = 2
 
 _BASE_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
 
@@ -84,6 +85,14 @@ class Oracle:
         lib.oracle_quantize_kv.restype = i64
         lib.oracle_quantize_pool.argtypes = [vp, vp, vp, i64, i32]
         lib.oracle_quantize_pool.restype = None
+        lib.oracle_quantize_kv_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i64]
+        lib.oracle_quantize_kv_fp8.restype = i64
+        lib.oracle_quantize_pool_fp8.argtypes = [vp, vp, vp, i64, i32]
+        lib.oracle_quantize_pool_fp8.restype = None
+        lib.oracle_fp8_encode.argtypes = [ctypes.c_float]
+        lib.oracle_fp8_encode.restype = ctypes.c_uint8
+        lib.oracle_fp8_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_fp8_decode.restype = dbl
         lib.oracle_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i64, i32]
         lib.oracle_copy_blocks.restype = i32
         lib.oracle_paged_attention.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp,
@@ -130,17 +139,40 @@ class Oracle:
             _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
             _ptr(slot_mapping), T, Hkv, D, int(bs), N))
 
-    def quantize_pool(self, src: np.ndarray):
+    def quantize_pool(self, src: np.ndarray, fp8: bool = False):
         """Quantise every D-row of a bf16 array (uint16 bits, last axis D).
 
-        Returns (codes int8 of the same shape, scales float32 of shape[:-1])."""
+        Returns (codes of the same shape -- int8, or uint8 e4m3 with fp8 --, scales
+        float32 of shape[:-1])."""
         _need(src, np.uint16, "src")
         D = src.shape[-1]
         rows = src.size // D
-        codes = np.empty(src.shape, dtype=np.int8)
+        codes = np.empty(src.shape, dtype=np.uint8 if fp8 else np.int8)
         scales = np.empty(src.shape[:-1], dtype=np.float32)
-        self.lib.oracle_quantize_pool(_ptr(src), _ptr(codes), _ptr(scales), rows, D)
+        fn = self.lib.oracle_quantize_pool_fp8 if fp8 else self.lib.oracle_quantize_pool
+        fn(_ptr(src), _ptr(codes), _ptr(scales), rows, D)
         return codes, scales
+
+    def quantize_kv_fp8(self, key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, bs: int) -> int:
+        """In-place fp8 (e4m3) quantise-and-append of bf16 rows [T][Hkv][D]."""
+        _need(key, np.uint16, "key")
+        _need(value, np.uint16, "value")
+        _need(k_cache, np.uint8, "k_cache")
+        _need(v_cache, np.uint8, "v_cache")
+        _need(k_scale, np.float32, "k_scale")
+        _need(v_scale, np.float32, "v_scale")
+        _need(slot_mapping, np.int64, "slot_mapping")
+        T, Hkv, D = key.shape
+        N = k_cache.shape[0]
+        return int(self.lib.oracle_quantize_kv_fp8(
+            _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            _ptr(slot_mapping), T, Hkv, D, int(bs), N))
+
+    def fp8_encode(self, x: float) -> int:
+        return int(self.lib.oracle_fp8_encode(float(x)))
+
+    def fp8_decode(self, code: int) -> float:
+        return float(self.lib.oracle_fp8_decode(int(code)))
 
     # -------------------------------------------------------------------- COW
     def copy_blocks(self, k_cache, v_cache, block_mapping, k_scale=None, v_scale=None) -> None:
@@ -162,12 +194,12 @@ class Oracle:
         _need(q, np.uint16, "q")
         _need(block_tables, np.int32, "block_tables")
         _need(context_lens, np.int32, "context_lens")
-        kv_dtype = KV_INT8 if k_cache.dtype == np.int8 else KV_BF16
+        kv_dtype = {np.dtype(np.int8): KV_INT8, np.dtype(np.uint8): KV_FP8}.get(k_cache.dtype, KV_BF16)
         if kv_dtype == KV_BF16:
             _need(k_cache, np.uint16, "k_cache")
             _need(v_cache, np.uint16, "v_cache")
         else:
-            _need(v_cache, np.int8, "v_cache")
+            _need(v_cache, k_cache.dtype, "v_cache")
             _need(k_scale, np.float32, "k_scale")
             _need(v_scale, np.float32, "v_scale")
         S, Hq, D = q.shape
@@ -185,7 +217,7 @@ class Oracle:
 
     def attention_weights(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                           s: int, h: int, k_scale=None, v_scale=None) -> np.ndarray:
-        kv_dtype = KV_INT8 if k_cache.dtype == np.int8 else KV_BF16
+        kv_dtype = {np.dtype(np.int8): KV_INT8, np.dtype(np.uint8): KV_FP8}.get(k_cache.dtype, KV_BF16)
         S, Hq, D = q.shape
         _, Hkv, bs, _ = k_cache.shape
         M = block_tables.shape[1]

@@ -39,6 +39,11 @@
  *    in IEEE fp32: scale = absmax / 127 (1 when absmax is 0),
  *    q = clamp(rint(x / scale), -127, 127), round half to even; dequantised value
  *    is q * scale.
+ *  - fp8 (e4m3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest
+ *    finite value 448, no infinities): the same dynamic per-(token, kv head) scheme
+ *    with scale = absmax / 448 and code = e4m3(x / scale), rounded to nearest, ties
+ *    to an even mantissa, magnitudes above 448 saturated to 448 ([iavox]: fp8 KV
+ *    cache on recent GPUs; [vernieres]: int8 or fp8 entries).
  *
  * All attention arithmetic is fp64.  The quantiser is fp32 on purpose: its output
  * is an integer decided by floating point, so both sides take that decision in
@@ -53,7 +58,7 @@
 #endif
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_NO_MEMORY = 2 };
-enum { ORACLE_KV_BF16 = 0, ORACLE_KV_INT8 = 1 };
+enum { ORACLE_KV_BF16 = 0, ORACLE_KV_INT8 = 1, ORACLE_KV_FP8 = 2 };
 
 /* bf16 is the upper half of an IEEE binary32; widening is exact. */
 static float bf16_to_float(uint16_t bits)
@@ -148,6 +153,92 @@ static void quantize_row(const uint16_t *x, int D, int8_t *q, float *scale_out)
     *scale_out = scale;
 }
 
+/* Value of an e4m3 code: subnormal m * 2^-9 (exponent field 0), else
+ * (1 + m/8) * 2^(e - 7).  The code 0x7f / 0xff (NaN) is never produced here. */
+double oracle_fp8_decode(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Nearest e4m3 code of x (finite), ties to an even mantissa, |x| > 448 -> 448. */
+uint8_t oracle_fp8_encode(float x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs((double)x);
+    if (a == 0.0)
+        return sign;
+    int e2;
+    frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1): floor(log2 a) = e2 - 1 */
+    int E = e2 - 1;
+    double quantum = E < -6 ? ldexp(1.0, -9) : ldexp(1.0, E - 3);
+    double v = rint(a / quantum) * quantum; /* a / quantum is exact; rint: ties to even */
+    if (v > 448.0)
+        v = 448.0;
+    if (v == 0.0)
+        return sign;
+    if (v < ldexp(1.0, -6))
+        return sign | (uint8_t)(v / ldexp(1.0, -9)); /* subnormal */
+    frexp(v, &e2);
+    E = e2 - 1;
+    int m = (int)(v / ldexp(1.0, E) * 8.0) - 8;
+    return sign | (uint8_t)((E + 7) << 3) | (uint8_t)m;
+}
+
+/* Dynamic per-token fp8 quantisation of one row: scale = absmax / 448 (1 when the
+ * row is zero), codes e4m3(x / scale) with the division in IEEE fp32. */
+static void quantize_row_fp8(const uint16_t *x, int D, uint8_t *q, float *scale_out)
+{
+    float absmax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float a = fabsf(bf16_to_float(x[d]));
+        if (a > absmax)
+            absmax = a;
+    }
+    float scale = (absmax > 0.0f) ? absmax / 448.0f : 1.0f;
+    for (int d = 0; d < D; ++d)
+        q[d] = oracle_fp8_encode(bf16_to_float(x[d]) / scale);
+    *scale_out = scale;
+}
+
+/* fp8 quantise-and-append, as oracle_quantize_kv with e4m3 codes. */
+int64_t oracle_quantize_kv_fp8(const uint16_t *key, const uint16_t *value,
+                               uint8_t *k_cache, uint8_t *v_cache, float *k_scale,
+                               float *v_scale, const int64_t *slot_mapping, int T,
+                               int Hkv, int D, int bs, int64_t N)
+{
+    int64_t bad = 0;
+    for (int t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= N * bs) {
+            ++bad;
+            continue;
+        }
+        int64_t b = slot / bs;
+        int o = (int)(slot % bs);
+        for (int h = 0; h < Hkv; ++h) {
+            int64_t src = ((int64_t)t * Hkv + h) * D;
+            int64_t dst = cache_row(b, h, o, Hkv, bs, D);
+            int64_t si = scale_index(b, h, o, Hkv, bs);
+            quantize_row_fp8(key + src, D, k_cache + dst, &k_scale[si]);
+            quantize_row_fp8(value + src, D, v_cache + dst, &v_scale[si]);
+        }
+    }
+    return bad;
+}
+
+/* fp8 counterpart of oracle_quantize_pool. */
+void oracle_quantize_pool_fp8(const uint16_t *src, uint8_t *codes, float *scales,
+                              int64_t rows, int D)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        quantize_row_fp8(src + r * D, D, codes + r * D, &scales[r]);
+}
+
 /* Quantise-and-append: for each new token t and kv head h, quantise the K row and
  * the V row separately and store codes in the int8 caches [N][Hkv][bs][D] and
  * scales in [N][Hkv][bs].  Slot rules as in oracle_reshape_and_cache. */
@@ -224,6 +315,9 @@ static double cache_value(const void *cache, const float *scales, int kv_dtype,
     int64_t idx = cache_row(b, h, o, Hkv, bs, D) + d;
     if (kv_dtype == ORACLE_KV_BF16)
         return bf16_to_double(((const uint16_t *)cache)[idx]);
+    if (kv_dtype == ORACLE_KV_FP8)
+        return oracle_fp8_decode(((const uint8_t *)cache)[idx]) *
+               (double)scales[scale_index(b, h, o, Hkv, bs)];
     return (double)((const int8_t *)cache)[idx] *
            (double)scales[scale_index(b, h, o, Hkv, bs)];
 }
@@ -289,7 +383,7 @@ static int check_attention_args(int S, int Hq, int Hkv, int D, int bs, int M,
         return ORACLE_BAD_ARG;
     if (Hq % Hkv != 0)
         return ORACLE_BAD_ARG;
-    if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_INT8)
+    if (kv_dtype != ORACLE_KV_BF16 && kv_dtype != ORACLE_KV_INT8 && kv_dtype != ORACLE_KV_FP8)
         return ORACLE_BAD_ARG;
     for (int s = 0; s < S; ++s)
         if (context_lens[s] < 0 || (int64_t)context_lens[s] > (int64_t)M * bs)
@@ -302,7 +396,7 @@ static int check_attention_args(int S, int Hq, int Hkv, int D, int bs, int M,
  *   sequence s, K_s and V_s gathered through block_tables[s] ([M] entries) from
  *   kv head h / (Hq / Hkv).
  * q is [S][Hq][D] bf16, out is [S][Hq][D] fp64.  Caches are [N][Hkv][bs][D]
- * (bf16, or int8 with fp32 scales [N][Hkv][bs]). */
+ * (bf16, or int8 / fp8 e4m3 with fp32 scales [N][Hkv][bs]). */
 int oracle_paged_attention(double *out, const uint16_t *q, const void *k_cache,
                            const void *v_cache, const float *k_scale,
                            const float *v_scale, int kv_dtype,

@@ -342,9 +342,91 @@ def pin_copy_blocks(orc):
         assert np.array_equal(arr, expect)
 
 
+def _e4m3_value(code: int) -> float:
+    """Value of an e4m3 code from the format's definition: sign bit, 4-bit exponent with
+    bias 7 (field 0: subnormal m * 2^-9), 3-bit mantissa."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 15, code & 7
+    return sign * (m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+
+
+def pin_fp8_hand_values(orc):
+    """e4m3 by hand: 1 -> 0x38, 448 (largest) -> 0x7e, -2 -> 0xc0, 2^-4 -> 0x18, 2^-9
+    (smallest subnormal) -> 0x01; ties go to the even mantissa (1 + 1/16 -> 1.0,
+    1 + 3/16 -> 1.25, 232 -> 224, 3 * 2^-10 -> 2^-8, 2^-10 -> 0); beyond 448
+    saturates."""
+    cases = {1.0: 0x38, 448.0: 0x7E, -2.0: 0xC0, 0.0625: 0x18, 2.0 ** -9: 0x01,
+             1.0625: 0x38, 1.1875: 0x3A, 232.0: 0x76, 3 * 2.0 ** -10: 0x02, 2.0 ** -10: 0x00,
+             464.0: 0x7E, 1e9: 0x7E, -1e9: 0xFE, 0.0: 0x00, 7.5 * 2.0 ** -9: 0x08}
+    for x, code in cases.items():
+        assert orc.fp8_encode(x) == code, (x, hex(orc.fp8_encode(x)), hex(code))
+
+
+def pin_fp8_round_trip_and_ties(orc):
+    """Every finite code decodes to its format value and encodes back to itself; the
+    midpoint of two neighbours goes to the one with the even mantissa, and anything
+    off the midpoint to the nearer one."""
+    finite = [c for c in range(256) if (c & 0x7F) != 0x7F]
+    for c in finite:
+        assert orc.fp8_decode(c) == _e4m3_value(c), hex(c)
+        assert orc.fp8_encode(_e4m3_value(c)) == c, hex(c)
+    pos = sorted((_e4m3_value(c), c) for c in finite if c < 0x80)
+    for (v0, c0), (v1, c1) in zip(pos, pos[1:]):
+        mid = (v0 + v1) / 2
+        assert orc.fp8_encode(mid) == (c0 if c0 % 2 == 0 else c1), (v0, v1)
+        assert orc.fp8_encode(v0 + (v1 - v0) * 0.49) == c0
+        assert orc.fp8_encode(v0 + (v1 - v0) * 0.51) == c1
+
+
+def pin_fp8_quantizer(orc):
+    """fp8 rows: scale = absmax / 448, so the absmax element maps to +-448 exactly; an
+    all-zero row gets scale 1."""
+    rng = np.random.default_rng(8)
+    src = to_bf16_bits(rng.standard_normal((32, 64)) * rng.uniform(0.01, 100, size=(32, 1)))
+    codes, scales = orc.quantize_pool(src, fp8=True)
+    x = bf16_bits_to_f64(src)
+    idx = np.abs(x).argmax(axis=1)
+    assert np.all((codes[np.arange(32), idx] & 0x7F) == 0x7E)
+    dq = np.vectorize(_e4m3_value)(codes) * scales[:, None]
+    # relative error of e4m3 (3 mantissa bits) is at most 2^-4, subnormals aside
+    big = np.abs(x) > 2.0 ** -6 * scales[:, None]
+    assert np.all(np.abs(dq - x)[big] <= 2.0 ** -4 * np.abs(x)[big] + 1e-12)
+    zero = np.zeros((1, 1, 8), dtype=np.uint16)
+    kc = np.zeros((1, 1, 4, 8), dtype=np.uint8)
+    ks = np.zeros((1, 1, 4), dtype=np.float32)
+    assert orc.quantize_kv_fp8(zero, zero, kc, kc.copy(), ks, ks.copy(), np.array([1], dtype=np.int64), 4) == 0
+    assert ks[0, 0, 1] == 1.0 and not kc.any()
+
+
+def pin_brute_force_fp8(orc):
+    """fp8 cache: attention over e4m3 value x scale, against 40-digit brute force."""
+    rng = np.random.default_rng(17)
+    S, Hq, Hkv, D, bs, N = 2, 4, 2, 8, 4, 8
+    ctx = [5, 10]
+    tables = np.array([[6, 2, 0], [1, 7, 4]], dtype=np.int32)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    ck = rng.choice(finite, size=(N, Hkv, bs, D)).astype(np.uint8)
+    cv = rng.choice(finite, size=(N, Hkv, bs, D)).astype(np.uint8)
+    sk = rng.uniform(0.001, 0.01, size=(N, Hkv, bs)).astype(np.float32)
+    sv = rng.uniform(0.001, 0.01, size=(N, Hkv, bs)).astype(np.float32)
+    q = to_bf16_bits(rng.standard_normal((S, Hq, D)))
+    out = orc.paged_attention(q, ck, cv, tables, np.array(ctx, dtype=np.int32), 0.3, k_scale=sk, v_scale=sv)
+    G = Hq // Hkv
+    qf = bf16_bits_to_f64(q)
+    for s in range(S):
+        for h in range(Hq):
+            hk = h // G
+            rows = [(tables[s][t // bs], t % bs) for t in range(ctx[s])]
+            K = np.array([[_e4m3_value(int(ck[b, hk, o, d])) * float(sk[b, hk, o]) for d in range(D)] for b, o in rows])
+            V = np.array([[_e4m3_value(int(cv[b, hk, o, d])) * float(sv[b, hk, o]) for d in range(D)] for b, o in rows])
+            ref = brute_attention(qf[s, h], K, V, 0.3)
+            assert np.allclose(out[s, h], ref, rtol=1e-12, atol=1e-13), (s, h)
+
+
 ALL_PINS = [pin_slot_figure, pin_append_places_rows, pin_brute_force_bf16, pin_brute_force_int8,
             pin_closed_forms, pin_block_permutation_invariance, pin_prefix_shared_equals_copied,
-            pin_softmax_weights, pin_quantizer_hand_values, pin_copy_blocks]
+            pin_softmax_weights, pin_quantizer_hand_values, pin_copy_blocks, pin_fp8_hand_values,
+            pin_fp8_round_trip_and_ties, pin_fp8_quantizer, pin_brute_force_fp8]
 
 
 def run_all(orc) -> list[str]:

@@ -46,6 +46,10 @@ MUTANTS = {
                           "                (void)0;"),
     "query_head_index": ("const uint16_t *qs = q + ((int64_t)s * Hq + h) * D;\n                    for",
                          "const uint16_t *qs = q + ((int64_t)s * Hq + (h ^ 1)) * D;\n                    for"),
+    "fp8_ties_away": ("double v = rint(a / quantum) * quantum;", "double v = round(a / quantum) * quantum;"),
+    "fp8_decode_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "fp8_no_saturation": ("    if (v > 448.0)\n        v = 448.0;\n", ""),
+    "fp8_scale_127": ("absmax / 448.0f", "absmax / 127.0f"),
     "empty_context_garbage": ("    for (int d = 0; d < D; ++d)\n        out[d] = 0.0;\n    if (ctx == 0)",
                               "    for (int d = 0; d < D; ++d)\n        out[d] = 1.0;\n    if (ctx == 0)"),
 }
