@@ -48,6 +48,7 @@ DESCRIPTIONS = {
               "32/8 heads, head_dim 128, block 16, COW copy of each seq's last block",
     "int8": "int8 KV decode: Llama-3-8B shape 32/8 heads, head_dim 128, block 32, 256 seqs, "
             "ctx log-uniform [128,32768], 1-token quantise+append per seq",
+    "fp8": "fp8 (e4m3) KV decode: the int8 workload's shape with an fp8 cache and per-token scales",
 }
 FLUSH_L2 = {"tiny", "prefix"}
 L2_BYTES = 126 * 1024 * 1024
@@ -159,17 +160,19 @@ class Step:
         self.dev = device
         self.stream = stream
         c = case
-        self.int8 = c.kv_dtype == "int8"
+        self.int8 = c.kv_dtype in ("int8", "fp8")  # quantised cache with per-token scales
+        self.quant = pa.pa_quantize_kv_fp8 if c.kv_dtype == "fp8" else pa.pa_quantize_kv
         if self.int8:
             N, Hkv, bs, D = c.k_pool.shape
-            self.k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.int8, device=device)
+            self.k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.uint8 if c.kv_dtype == "fp8" else torch.int8,
+                                       device=device)
             self.v_cache = torch.empty_like(self.k_cache)
             self.k_scale = torch.empty((N, Hkv, bs), dtype=torch.float32, device=device)
             self.v_scale = torch.empty_like(self.k_scale)
             slots = torch.arange(N * bs, dtype=torch.int64, device=device)
             rows = lambda p: p.permute(0, 2, 1, 3).reshape(N * bs, Hkv, D).contiguous()  # noqa: E731
-            pa.pa_quantize_kv(rows(c.k_pool), rows(c.v_pool), self.k_cache, self.v_cache,
-                              self.k_scale, self.v_scale, slots, stream=stream)
+            self.quant(rows(c.k_pool), rows(c.v_pool), self.k_cache, self.v_cache,
+                       self.k_scale, self.v_scale, slots, stream=stream)
             torch.cuda.synchronize(device)
             self.source = (c.k_pool.cpu(), c.v_pool.cpu())  # for the CPU baseline only
             c.k_pool = c.v_pool = None  # the bf16 source is not part of the step
@@ -192,8 +195,8 @@ class Step:
             self.pa.pa_copy_blocks(self.k_cache, self.v_cache, self.cow, k_scale=self.k_scale,
                                    v_scale=self.v_scale, stream=self.stream)
         if self.int8:
-            self.pa.pa_quantize_kv(new_key, new_value, self.k_cache, self.v_cache, self.k_scale,
-                                   self.v_scale, slots, err_flag=self.flag, stream=self.stream)
+            self.quant(new_key, new_value, self.k_cache, self.v_cache, self.k_scale,
+                       self.v_scale, slots, err_flag=self.flag, stream=self.stream)
         else:
             self.pa.pa_reshape_and_cache(new_key, new_value, self.k_cache, self.v_cache, slots,
                                          err_flag=self.flag, stream=self.stream)
@@ -218,7 +221,7 @@ def step_bytes(case) -> dict:
     app = workloads.append_algorithmic_bytes(case)
     cow = 0
     if case.cow_pairs.shape[0]:
-        per_block = case.Hkv * case.bs * case.D * (1 if case.kv_dtype == "int8" else 2) * 2
+        per_block = case.Hkv * case.bs * case.D * (1 if case.kv_dtype in ("int8", "fp8") else 2) * 2
         cow = case.cow_pairs.shape[0] * per_block * 2
     return {"decode": dec, "append": app, "cow": cow, "total": dec + app + cow,
             "decode_unique": workloads.decode_algorithmic_bytes(case, unique_blocks=True)}
@@ -300,7 +303,7 @@ def run_ours(args, rank, world, device) -> dict | None:
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8" if case.kv_dtype == "int8" else "bf16", "data": "synthetic (seeded N(0,1))",
+        "dtype": case.kv_dtype, "data": "synthetic (seeded N(0,1))",
         "config": {"workload": DESCRIPTIONS[args.config], "name": args.config, "S": case.S,
                    "Hq": case.Hq, "Hkv": case.Hkv, "head_dim": case.D, "block_size": case.bs,
                    "pool_blocks": case.N, "total_context_tokens": int(case.context_lens.sum()),
@@ -373,13 +376,13 @@ def oracle_sample_inputs(case, step=None):
     def bits(t):
         return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
-    if case.kv_dtype == "int8":
+    if case.kv_dtype in ("int8", "fp8"):
         import oracle
 
         orc = oracle.load()
         k_src, v_src = step.source if step is not None else (case.k_pool, case.v_pool)
-        kc, ks = orc.quantize_pool(bits(k_src))
-        vc, vs = orc.quantize_pool(bits(v_src))
+        kc, ks = orc.quantize_pool(bits(k_src), fp8=case.kv_dtype == "fp8")
+        vc, vs = orc.quantize_pool(bits(v_src), fp8=case.kv_dtype == "fp8")
         return bits(case.q), kc, vc, ks, vs
     return bits(case.q), bits(case.k_pool), bits(case.v_pool), None, None
 

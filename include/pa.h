@@ -58,7 +58,7 @@ typedef enum pa_status {
     PA_ERR_NO_SPACE = 5      /* the block pool cannot hold the request (pa_blocks.h) */
 } pa_status;
 
-enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1 };
+enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1, PA_KV_FP8 = 2 };
 
 /* Bits OR-ed into *err_flag by the kernels. */
 enum {
@@ -116,6 +116,21 @@ pa_status pa_quantize_kv(const pa_bf16 *key, const pa_bf16 *value, int8_t *k_cac
                          int *err_flag, void *stream);
 
 /*
+ * Quantise-and-append into an fp8 (e4m3) cache with a dynamic per-(token, kv head)
+ * scale: the same rule as pa_quantize_kv with scale = absmax / 448 (1 if absmax is
+ * 0) and code = e4m3(x / scale) (IEEE fp32 division; round to nearest, ties to the
+ * even mantissa, saturating at +-448).  The pages recommend fp8 KV caches on recent
+ * GPUs (ia-vox-magazine, "Quantization du KV cache"; blog.fabienvernieres.com,
+ * "Reduire le poids par token").  Caches hold raw e4m3 bytes, [N][Hkv][bs][D];
+ * scales [N][Hkv][bs] fp32.  Bit-identical to the CPU statement of the rule for
+ * finite inputs.
+ */
+pa_status pa_quantize_kv_fp8(const pa_bf16 *key, const pa_bf16 *value, uint8_t *k_cache,
+                             uint8_t *v_cache, float *k_scale, float *v_scale,
+                             const int64_t *slot_mapping, int T, int Hkv, int D, int bs, int N,
+                             int *err_flag, void *stream);
+
+/*
  * Copy-on-write block copy (gotburnout.io section 3.01): for each pair
  * (src, dst) copy the whole physical block src onto block dst, in the K cache and
  * in the V cache, and, when k_scale / v_scale are given, the block's scales.
@@ -147,12 +162,13 @@ size_t pa_decode_workspace_size(int S, int Hq, int Hkv, int D, int bs, int kv_dt
  * and query head h
  *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_s[t]) V_s[t],  t < context_lens[s],
  * where K_s[t], V_s[t] are read from physical block block_tables[s][t / bs] at
- * offset t % bs, kv head h / (Hq / Hkv); int8 entries are code * scale.  A
+ * offset t % bs, kv head h / (Hq / Hkv); int8 and fp8 entries are value * scale.  A
  * sequence with context length 0 gets an all-zero output.
  *   out             [S][Hq][D] bf16, device (written).
  *   query           [S][Hq][D] bf16, device.
- *   k_cache,v_cache [N][Hkv][bs][D], bf16 (kv_dtype PA_KV_BF16) or int8 (PA_KV_INT8).
- *   k_scale,v_scale [N][Hkv][bs] fp32 for int8; ignored (may be NULL) for bf16.
+ *   k_cache,v_cache [N][Hkv][bs][D], bf16 (kv_dtype PA_KV_BF16), int8 (PA_KV_INT8)
+ *                   or e4m3 bytes (PA_KV_FP8).
+ *   k_scale,v_scale [N][Hkv][bs] fp32 for int8 and fp8; ignored (may be NULL) for bf16.
  *   block_tables    [S][M] int32, device; entries past a sequence's last block are
  *                   never read.
  *   context_lens    [S] int32, device.

@@ -22,13 +22,13 @@ PKG = Path(__file__).resolve().parent
 LIBRARY = PKG / "libpa.so"
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_OUT_OF_RANGE, PA_ERR_CUDA = range(5)
-PA_KV_BF16, PA_KV_INT8 = 0, 1
+PA_KV_BF16, PA_KV_INT8, PA_KV_FP8 = 0, 1, 2
 PA_FLAG_SLOT_OUT_OF_RANGE = 1
 PA_FLAG_BLOCK_OUT_OF_RANGE = 2
 PA_FLAG_CONTEXT_OUT_OF_RANGE = 4
 
 EXPORTED = ["pa_version", "pa_status_string", "pa_last_error_string", "pa_reshape_and_cache",
-            "pa_quantize_kv", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",
+            "pa_quantize_kv", "pa_quantize_kv_fp8", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_noalloc"]
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -62,6 +62,8 @@ def load_library(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pa_reshape_and_cache.restype = i32
     lib.pa_quantize_kv.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
     lib.pa_quantize_kv.restype = i32
+    lib.pa_quantize_kv_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    lib.pa_quantize_kv_fp8.restype = i32
     lib.pa_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, sz, i32, vp]
     lib.pa_copy_blocks.restype = i32
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
@@ -157,13 +159,50 @@ def pa_quantize_kv(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                               _stream(stream, key.device)))
 
 
+FP8_DTYPES = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def kv_dtype_of(cache: torch.Tensor) -> int:
+    """PA_KV_* code of a cache tensor: bf16, int8, or fp8 e4m3 bytes (uint8 or float8_e4m3fn)."""
+    if cache.dtype == torch.bfloat16:
+        return PA_KV_BF16
+    if cache.dtype == torch.int8:
+        return PA_KV_INT8
+    if cache.dtype in FP8_DTYPES:
+        return PA_KV_FP8
+    raise TypeError(f"unsupported cache dtype {cache.dtype}")
+
+
+def pa_quantize_kv_fp8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, err_flag=None,
+                       stream=None) -> None:
+    """Quantise bf16 rows [T][Hkv][D] to fp8 e4m3 with a per-(token, kv head) scale and append."""
+    for t, n in ((key, "key"), (value, "value")):
+        _cuda(t, n, torch.bfloat16, 3)
+    if k_cache.dtype not in FP8_DTYPES:
+        raise TypeError("fp8 caches are uint8 or float8_e4m3fn tensors")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _cuda(t, n, k_cache.dtype, 4)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _cuda(t, n, torch.float32, 3)
+    _cuda(slot_mapping, "slot_mapping", torch.int64, 1)
+    T, Hkv, D = key.shape
+    N, Hkv2, bs, D2 = k_cache.shape
+    if value.shape != key.shape or v_cache.shape != k_cache.shape or (Hkv2, D2) != (Hkv, D) \
+            or tuple(k_scale.shape) != (N, Hkv, bs) or v_scale.shape != k_scale.shape \
+            or slot_mapping.shape[0] != T:
+        raise ValueError("pa_quantize_kv_fp8: shape mismatch")
+    lib = load_library()
+    _check(lib.pa_quantize_kv_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                  _ptr(v_scale), _ptr(slot_mapping), T, Hkv, D, bs, N, _flag(err_flag),
+                                  _stream(stream, key.device)))
+
+
 def pa_copy_blocks(k_cache, v_cache, block_mapping, k_scale=None, v_scale=None,
                    stream=None) -> None:
     """Copy whole physical blocks (src, dst) of both caches (and scales, if given).
 
     block_mapping is a HOST sequence of (src, dst) pairs (tensor, ndarray or list)."""
-    if k_cache.dtype not in (torch.bfloat16, torch.int8):
-        raise TypeError("k_cache must be bf16 or int8")
+    kv_dtype_of(k_cache)
     _cuda(k_cache, "k_cache", k_cache.dtype)
     _cuda(v_cache, "v_cache", k_cache.dtype)
     if v_cache.shape != k_cache.shape:
@@ -198,15 +237,14 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale: f
     """Paged decode attention; writes out [S][Hq][D] bf16."""
     _cuda(out, "out", torch.bfloat16, 3)
     _cuda(query, "query", torch.bfloat16, 3)
-    kv_dtype = PA_KV_INT8 if k_cache.dtype == torch.int8 else PA_KV_BF16
-    cache_dtype = torch.int8 if kv_dtype == PA_KV_INT8 else torch.bfloat16
-    _cuda(k_cache, "k_cache", cache_dtype, 4)
-    _cuda(v_cache, "v_cache", cache_dtype, 4)
+    kv_dtype = kv_dtype_of(k_cache)
+    _cuda(k_cache, "k_cache", k_cache.dtype, 4)
+    _cuda(v_cache, "v_cache", k_cache.dtype, 4)
     _cuda(block_tables, "block_tables", torch.int32, 2)
     _cuda(context_lens, "context_lens", torch.int32, 1)
-    if kv_dtype == PA_KV_INT8:
+    if kv_dtype != PA_KV_BF16:
         if k_scale is None or v_scale is None:
-            raise ValueError("an int8 cache needs k_scale and v_scale")
+            raise ValueError("an int8 or fp8 cache needs k_scale and v_scale")
         _cuda(k_scale, "k_scale", torch.float32, 3)
         _cuda(v_scale, "v_scale", torch.float32, 3)
     S, Hq, D = query.shape
@@ -234,15 +272,14 @@ def pa_decode_noalloc(out, query, k_cache, v_cache, block_tables, context_lens, 
     must not overlap on the GPU."""
     _cuda(out, "out", torch.bfloat16, 3)
     _cuda(query, "query", torch.bfloat16, 3)
-    kv_dtype = PA_KV_INT8 if k_cache.dtype == torch.int8 else PA_KV_BF16
-    cache_dtype = torch.int8 if kv_dtype == PA_KV_INT8 else torch.bfloat16
-    _cuda(k_cache, "k_cache", cache_dtype, 4)
-    _cuda(v_cache, "v_cache", cache_dtype, 4)
+    kv_dtype = kv_dtype_of(k_cache)
+    _cuda(k_cache, "k_cache", k_cache.dtype, 4)
+    _cuda(v_cache, "v_cache", k_cache.dtype, 4)
     _cuda(block_tables, "block_tables", torch.int32, 2)
     _cuda(context_lens, "context_lens", torch.int32, 1)
-    if kv_dtype == PA_KV_INT8:
+    if kv_dtype != PA_KV_BF16:
         if k_scale is None or v_scale is None:
-            raise ValueError("an int8 cache needs k_scale and v_scale")
+            raise ValueError("an int8 or fp8 cache needs k_scale and v_scale")
         _cuda(k_scale, "k_scale", torch.float32, 3)
         _cuda(v_scale, "v_scale", torch.float32, 3)
     S, Hq, D = query.shape
@@ -262,7 +299,7 @@ def decode_workspace(query, k_cache, max_context_len: int) -> torch.Tensor | Non
     """Allocate (with torch) the scratch pa_decode needs for these shapes, or None."""
     S, Hq, D = query.shape
     N, Hkv, bs, _ = k_cache.shape
-    kv_dtype = PA_KV_INT8 if k_cache.dtype == torch.int8 else PA_KV_BF16
+    kv_dtype = kv_dtype_of(k_cache)
     n = pa_decode_workspace_size(S, Hq, Hkv, D, bs, kv_dtype, max_context_len)
     if n == 0:
         return None

@@ -179,6 +179,26 @@ pa_status pa_quantize_kv(const pa_bf16 *key, const pa_bf16 *value, int8_t *k_cac
     return check_launch(fn);
 }
 
+pa_status pa_quantize_kv_fp8(const pa_bf16 *key, const pa_bf16 *value, uint8_t *k_cache,
+                             uint8_t *v_cache, float *k_scale, float *v_scale,
+                             const int64_t *slot_mapping, int T, int Hkv, int D, int bs, int N,
+                             int *err_flag, void *stream) {
+    const char *fn = "pa_quantize_kv_fp8";
+    g_last_error[0] = 0;
+    if (T < 0) return fail(PA_ERR_INVALID_ARG, "%s: T = %d is negative", fn, T);
+    pa_status st = check_cache_shape(fn, Hkv, D, bs, N);
+    if (st != PA_OK) return st;
+    if (T == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(k_scale) || !aligned16(v_scale))
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
+    launch_quantize_kv_fp8(key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, T, Hkv, D,
+                           bs, N, err_flag, (cudaStream_t)stream);
+    return check_launch(fn);
+}
+
 pa_status pa_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                          const int64_t *block_mapping, int n, int N, size_t block_bytes,
                          int scale_elems_per_block, void *stream) {
@@ -232,7 +252,7 @@ static pa_status check_decode_shape(const char *fn, int S, int Hq, int Hkv, int 
         return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d not supported (64 or 128)", fn, D);
     if (bs != 16 && bs != 32)
         return fail(PA_ERR_UNSUPPORTED, "%s: block size %d not supported (16 or 32)", fn, bs);
-    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_INT8)
+    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_INT8 && kv_dtype != PA_KV_FP8)
         return fail(PA_ERR_UNSUPPORTED, "%s: kv dtype %d not supported", fn, kv_dtype);
     if (max_context_len < 0)
         return fail(PA_ERR_INVALID_ARG, "%s: max_context_len = %d", fn, max_context_len);
@@ -269,9 +289,9 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
                     max_context_len, (long long)M * bs);
     if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
         return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
-    if (kv_dtype == PA_KV_INT8 && (!k_scale || !v_scale))
-        return fail(PA_ERR_INVALID_ARG, "%s: int8 cache needs k_scale and v_scale", fn);
-    if (kv_dtype == PA_KV_INT8 && (!aligned16(k_scale) || !aligned16(v_scale)))
+    if (kv_dtype != PA_KV_BF16 && (!k_scale || !v_scale))
+        return fail(PA_ERR_INVALID_ARG, "%s: int8 / fp8 caches need k_scale and v_scale", fn);
+    if (kv_dtype != PA_KV_BF16 && (!aligned16(k_scale) || !aligned16(v_scale)))
         return fail(PA_ERR_INVALID_ARG, "%s: scales must be 16-byte aligned", fn);
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);

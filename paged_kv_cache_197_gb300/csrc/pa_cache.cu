@@ -2,6 +2,7 @@
 // copy-on-write block copy.  All three move whole 16-byte vectors; they are bound by
 // launch latency at decode batch sizes and by HBM bandwidth beyond that.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "pa_internal.cuh"
 
@@ -48,9 +49,10 @@ reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict_
 }
 
 // One warp quantises one row (token t, kv head h, K or V) of D values: each lane
-// holds D/32 consecutive values.  IEEE division and rintf keep the codes identical
-// to the CPU statement of the rule.
-template <int D>
+// holds D/32 consecutive values.  IEEE division and rintf (int8) or the round-to-
+// nearest-even saturating e4m3 conversion (fp8) keep the codes identical to the CPU
+// statement of the rule.
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads)
 quantize_kv_kernel(const uint16_t *__restrict__ key, const uint16_t *__restrict__ value,
                    int8_t *__restrict__ k_cache, int8_t *__restrict__ v_cache,
@@ -90,13 +92,23 @@ quantize_kv_kernel(const uint16_t *__restrict__ key, const uint16_t *__restrict_
         for (int j = 0; j < PER_LANE; ++j) amax = fmaxf(amax, fabsf(x[j]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float scale = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+        const float scale = amax > 0.0f ? __fdiv_rn(amax, FP8 ? 448.0f : 127.0f) : 1.0f;
         uint32_t packed = 0;
+        if constexpr (FP8) {
 #pragma unroll
-        for (int j = 0; j < PER_LANE; ++j) {
-            float qv = rintf(__fdiv_rn(x[j], scale));
-            qv = fminf(fmaxf(qv, -127.0f), 127.0f);
-            packed |= ((uint32_t)(int)qv & 0xffu) << (8 * j);
+            for (int j = 0; j < PER_LANE; j += 2) {
+                const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(x[j], scale), __fdiv_rn(x[j + 1], scale)), __NV_SATFINITE,
+                    __NV_E4M3);
+                packed |= (uint32_t)two << (8 * j);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < PER_LANE; ++j) {
+                float qv = rintf(__fdiv_rn(x[j], scale));
+                qv = fminf(fmaxf(qv, -127.0f), 127.0f);
+                packed |= ((uint32_t)(int)qv & 0xffu) << (8 * j);
+            }
         }
         const int64_t blk = slot / bs;
         const int off = (int)(slot % bs);
@@ -166,11 +178,27 @@ cudaError_t launch_quantize_kv(const uint16_t *key, const uint16_t *value, int8_
     const int64_t warps = (int64_t)T * Hkv * 2;
     const int grid = grid_for(warps, kThreads / 32);
     if (D == 128)
-        quantize_kv_kernel<128><<<grid, kThreads, 0, stream>>>(
+        quantize_kv_kernel<128, false><<<grid, kThreads, 0, stream>>>(
             key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
     else
-        quantize_kv_kernel<64><<<grid, kThreads, 0, stream>>>(
+        quantize_kv_kernel<64, false><<<grid, kThreads, 0, stream>>>(
             key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_kv_fp8(const uint16_t *key, const uint16_t *value, uint8_t *k_cache,
+                                   uint8_t *v_cache, float *k_scale, float *v_scale,
+                                   const int64_t *slot_mapping, int T, int Hkv, int D, int bs,
+                                   int N, int *err_flag, cudaStream_t stream) {
+    const int64_t warps = (int64_t)T * Hkv * 2;
+    const int grid = grid_for(warps, kThreads / 32);
+    int8_t *kc = reinterpret_cast<int8_t *>(k_cache), *vc = reinterpret_cast<int8_t *>(v_cache);
+    if (D == 128)
+        quantize_kv_kernel<128, true><<<grid, kThreads, 0, stream>>>(
+            key, value, kc, vc, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
+    else
+        quantize_kv_kernel<64, true><<<grid, kThreads, 0, stream>>>(
+            key, value, kc, vc, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
     return cudaGetLastError();
 }
 

@@ -35,6 +35,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "pa_internal.cuh"
 
 namespace pa {
@@ -130,6 +132,41 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &
 __device__ __forceinline__ uint32_t i8pair_to_f16x2(uint32_t t) {
     const uint32_t m = 0x00ff00ffu, c = 0x64806480u;
     return biased_to_f16x2((m & (t ^ c)) | (~m & c));
+}
+
+// fp8 (e4m3) cache entries: every e4m3 value is exactly an fp16 value, and the
+// hardware converts a pair with one instruction (low byte -> low half).
+struct e4m3_t {
+    uint8_t bits;
+};
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(out)
+        : "r"(pair16));
+    return out;
+}
+
+// The four 8-bit entries of word w (one K row, d = 4t .. 4t+3 of a 16-wide step) as
+// the fp16 pairs (w0, w1), (w2, w3).
+template <typename KV>
+__device__ __forceinline__ void k8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    if constexpr (sizeof(KV) == 1 && !std::is_same<KV, e4m3_t>::value) {
+        i8x4_to_f16(w, lo, hi);
+    } else {
+        lo = e4m3x2_to_f16x2(w & 0xffffu);
+        hi = e4m3x2_to_f16x2(w >> 16);
+    }
+}
+
+// The fp16 pair (A.byte j, B.byte j): entry j of two V rows (two tokens).
+template <typename KV>
+__device__ __forceinline__ uint32_t v8_pair_to_f16(uint32_t A, uint32_t B, uint32_t j) {
+    if constexpr (std::is_same<KV, e4m3_t>::value)
+        return e4m3x2_to_f16x2(__byte_perm(A, B, j | ((4u + j) << 4)));
+    else
+        return i8pair_to_f16x2(__byte_perm(A, B, j | ((4u + j) << 8)));
 }
 
 // Exponent e with |x| < 2^e for a finite, positive x (normal range).
@@ -271,8 +308,8 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
                 a3 = R.k[2 * s + 1][2 * kc + 1];
                 mma_bf16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
             } else {
-                i8x4_to_f16(R.k[2 * s][kc], a0, a2);
-                i8x4_to_f16(R.k[2 * s + 1][kc], a1, a3);
+                k8x4_to_f16<KV>(R.k[2 * s][kc], a0, a2);
+                k8x4_to_f16<KV>(R.k[2 * s + 1][kc], a1, a3);
                 mma_f16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
             }
         }
@@ -384,12 +421,10 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
             } else {
                 const int w = mt >> 1;
                 const uint32_t b = 2u * (mt & 1);
-                const uint32_t sel0 = b | ((4u + b) << 8);
-                const uint32_t sel1 = (b + 1u) | ((5u + b) << 8);
-                a0 = i8pair_to_f16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel0));
-                a1 = i8pair_to_f16x2(__byte_perm(R.v[j0][w], R.v[j0 + 1][w], sel1));
-                a2 = i8pair_to_f16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel0));
-                a3 = i8pair_to_f16x2(__byte_perm(R.v[j0 + 2][w], R.v[j0 + 3][w], sel1));
+                a0 = v8_pair_to_f16<KV>(R.v[j0][w], R.v[j0 + 1][w], b);
+                a1 = v8_pair_to_f16<KV>(R.v[j0][w], R.v[j0 + 1][w], b + 1u);
+                a2 = v8_pair_to_f16<KV>(R.v[j0 + 2][w], R.v[j0 + 3][w], b);
+                a3 = v8_pair_to_f16<KV>(R.v[j0 + 2][w], R.v[j0 + 3][w], b + 1u);
             }
             if constexpr (G_::ELEM == 2)
                 mma_bf16(st.o[mt], a0, a1, a2, a3, b0, b1);
@@ -639,9 +674,9 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
 
 template <typename KV, int D>
 cudaError_t launch_bs(const DecodeArgs &a, int bs, cudaStream_t stream) {
-    constexpr bool INT8 = sizeof(KV) == 1;
+    constexpr bool ONE_BYTE = sizeof(KV) == 1;  // int8 and fp8: a tile is a whole 32-token block
     if (bs == 16) return launch_typed<KV, D, 16, 16>(a, stream);
-    return launch_typed<KV, D, 32, INT8 ? 32 : 16>(a, stream);
+    return launch_typed<KV, D, 32, ONE_BYTE ? 32 : 16>(a, stream);
 }
 
 }  // namespace
@@ -650,6 +685,8 @@ cudaError_t launch_decode(const DecodeArgs &a, int D, int bs, int kv_dtype, cuda
     static_assert(kMaxPartBlocks * 16 >= 4096, "partition block list fits in shared memory");
     if (kv_dtype == PA_KV_BF16)
         return D == 128 ? launch_bs<uint16_t, 128>(a, bs, stream) : launch_bs<uint16_t, 64>(a, bs, stream);
+    if (kv_dtype == PA_KV_FP8)
+        return D == 128 ? launch_bs<e4m3_t, 128>(a, bs, stream) : launch_bs<e4m3_t, 64>(a, bs, stream);
     return D == 128 ? launch_bs<int8_t, 128>(a, bs, stream) : launch_bs<int8_t, 64>(a, bs, stream);
 }
 

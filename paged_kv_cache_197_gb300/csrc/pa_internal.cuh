@@ -58,6 +58,10 @@ cudaError_t launch_quantize_kv(const uint16_t *key, const uint16_t *value, int8_
                                int8_t *v_cache, float *k_scale, float *v_scale,
                                const int64_t *slot_mapping, int T, int Hkv, int D, int bs, int N,
                                int *err_flag, cudaStream_t stream);
+cudaError_t launch_quantize_kv_fp8(const uint16_t *key, const uint16_t *value, uint8_t *k_cache,
+                                   uint8_t *v_cache, float *k_scale, float *v_scale,
+                                   const int64_t *slot_mapping, int T, int Hkv, int D, int bs,
+                                   int N, int *err_flag, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                                const int64_t *block_mapping, int n, size_t block_bytes,
                                int scale_elems_per_block, cudaStream_t stream);

@@ -8,7 +8,7 @@ import torch
 import workloads
 
 BF16_MAX_ABS, BF16_MEAN_ABS = 2e-2, 2e-3   # bf16 cache: output vs fp64 oracle
-INT8_MAX_ABS, INT8_MEAN_ABS = 5e-2, 2e-3   # int8 cache: vs the oracle on the same codes
+INT8_MAX_ABS, INT8_MEAN_ABS = 5e-2, 2e-3   # int8 / fp8 cache: vs the oracle on the same codes
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
@@ -36,13 +36,15 @@ def gpu_step(case: workloads.PagedCase, device, max_context_len=None, poison_int
         k_cache, v_cache = c.k_pool.clone(), c.v_pool.clone()
     else:
         N, Hkv, bs, D = case.k_pool.shape
-        k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.int8, device=device)
+        fp8 = case.kv_dtype == "fp8"
+        quant = pa.pa_quantize_kv_fp8 if fp8 else pa.pa_quantize_kv
+        k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.uint8 if fp8 else torch.int8, device=device)
         v_cache = torch.empty_like(k_cache)
         k_scale = torch.empty((N, Hkv, bs), dtype=torch.float32, device=device)
         v_scale = torch.empty_like(k_scale)
         slots = torch.arange(N * bs, dtype=torch.int64, device=device)
-        pa.pa_quantize_kv(int8_pool_rows(c.k_pool), int8_pool_rows(c.v_pool), k_cache, v_cache,
-                          k_scale, v_scale, slots, err_flag=flag)
+        quant(int8_pool_rows(c.k_pool), int8_pool_rows(c.v_pool), k_cache, v_cache,
+              k_scale, v_scale, slots, err_flag=flag)
         if poison_int8:
             bad = ~workloads.valid_slot_mask(case.meta["content_tables"], case.context_lens - 1,
                                              case.bs, case.N).to(device)
@@ -54,8 +56,9 @@ def gpu_step(case: workloads.PagedCase, device, max_context_len=None, poison_int
         pa.pa_reshape_and_cache(c.new_key, c.new_value, k_cache, v_cache, c.slot_mapping,
                                 err_flag=flag)
     else:
-        pa.pa_quantize_kv(c.new_key, c.new_value, k_cache, v_cache, k_scale, v_scale,
-                          c.slot_mapping, err_flag=flag)
+        quant = pa.pa_quantize_kv_fp8 if case.kv_dtype == "fp8" else pa.pa_quantize_kv
+        quant(c.new_key, c.new_value, k_cache, v_cache, k_scale, v_scale, c.slot_mapping,
+              err_flag=flag)
     if max_context_len is None:
         max_context_len = int(case.context_lens.max()) if case.S else 0
     out = torch.full_like(c.q, float("nan"))
@@ -73,8 +76,9 @@ def oracle_caches(case: workloads.PagedCase, orc, poison_int8=True):
     if case.kv_dtype == "bf16":
         kc, vc = bits(case.k_pool), bits(case.v_pool)
     else:
-        kc, ks = orc.quantize_pool(bits(case.k_pool))
-        vc, vs = orc.quantize_pool(bits(case.v_pool))
+        fp8 = case.kv_dtype == "fp8"
+        kc, ks = orc.quantize_pool(bits(case.k_pool), fp8=fp8)
+        vc, vs = orc.quantize_pool(bits(case.v_pool), fp8=fp8)
         if poison_int8:
             bad = ~workloads.valid_slot_mask(case.meta["content_tables"], case.context_lens - 1,
                                              case.bs, case.N).numpy()
@@ -85,6 +89,8 @@ def oracle_caches(case: workloads.PagedCase, orc, poison_int8=True):
     slots = case.slot_mapping.cpu().numpy()
     if case.kv_dtype == "bf16":
         bad = orc.reshape_and_cache(bits(case.new_key), bits(case.new_value), kc, vc, slots, case.bs)
+    elif case.kv_dtype == "fp8":
+        bad = orc.quantize_kv_fp8(bits(case.new_key), bits(case.new_value), kc, vc, ks, vs, slots, case.bs)
     else:
         bad = orc.quantize_kv(bits(case.new_key), bits(case.new_value), kc, vc, ks, vs, slots, case.bs)
     assert bad == 0

@@ -45,7 +45,7 @@ def test_tiny(oracle):
     _check_case(workloads.tiny(), oracle)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (16, 2), (20, 2), (32, 2)])
@@ -58,7 +58,7 @@ def test_shapes(oracle, kv_dtype, D, bs, Hq, Hkv):
     _check_case(case, oracle)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
 def test_prefix_and_cow(oracle, kv_dtype):
     """Sequences sharing a prefix's physical blocks, each with a copy-on-write last block."""
     own = [64, 65, 80, 130, 511, 512]
@@ -209,6 +209,7 @@ FULL = {
     "gqa70b": (workloads.gqa70b, [0, 7, 19]),
     "prefix": (workloads.prefix, [0, 1, 25, 49]),
     "int8": (workloads.int8, [0, 3, 100, 200, 255]),
+    "fp8": (workloads.fp8, [0, 5, 128, 255]),
 }
 
 
@@ -219,7 +220,7 @@ def test_full_size_sampled(oracle, name):
     times; the oracle checks a sample of sequences (all their heads), and append, copy
     and quantisation are compared over the whole pool."""
     make, seqs = FULL[name]
-    case = make(device=DEV, poison=(name != "int8"))
+    case = make(device=DEV, poison=(name not in ("int8", "fp8")))
     # the sample always holds the longest and the shortest sequence
     lens = case.context_lens.cpu()
     seqs = sorted(set(seqs) | {int(lens.argmax()), int(lens.argmin())})

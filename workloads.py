@@ -19,6 +19,7 @@ Workloads (shapes and distributions of the benchmark configurations):
           one copy-on-write block pair per sequence.
   int8    Llama-3-8B-shaped layer with an int8 cache: 256 sequences, 32 / 8 heads,
           head_dim 128, block size 32, context lengths log-uniform in [128, 32768].
+  fp8     the int8 workload's shape with an fp8 (e4m3) cache.
 All values (queries, cached keys and values, the new token's key and value) are
 N(0, 1) rounded to bf16.  context_lens count the token appended in this step: the
 new token sits at position context_len - 1.
@@ -43,7 +44,7 @@ class PagedCase:
     bs: int
     N: int
     M: int
-    kv_dtype: str  # "bf16" or "int8"
+    kv_dtype: str  # "bf16", "int8" or "fp8"
     scale: float
     q: torch.Tensor  # [S][Hq][D] bf16
     k_pool: torch.Tensor  # [N][Hkv][bs][D] bf16 (int8 workloads: the bf16 source to quantise)
@@ -147,7 +148,7 @@ def build_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, context_le
             pos = c - 1
             slots[s] = int(tables[s, pos // bs]) * bs + pos % bs
 
-    if poison and kv_dtype == "bf16":  # int8 sources stay finite: tests poison their scales
+    if poison and kv_dtype == "bf16":  # quantised sources stay finite: tests poison their scales
         valid = valid_slot_mask(content_tables, ctx - 1, bs, N)  # tokens present before the append
         bad = ~valid.to(device)
         nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
@@ -213,7 +214,13 @@ def int8(seed: int = 4, device="cpu", poison=False) -> PagedCase:
                       seed=seed, kv_dtype="int8", poison=poison, device=device)
 
 
-CONFIGS = {"tiny": tiny, "mha13b": mha13b, "gqa70b": gqa70b, "prefix": prefix, "int8": int8}
+def fp8(seed: int = 5, device="cpu", poison=False) -> PagedCase:
+    """The int8 workload's shape with an fp8 (e4m3) cache."""
+    return build_case("fp8", S=256, Hq=32, Hkv=8, D=128, bs=32, context_lens=int8_lengths(256, seed),
+                      seed=seed, kv_dtype="fp8", poison=poison, device=device)
+
+
+CONFIGS = {"tiny": tiny, "mha13b": mha13b, "gqa70b": gqa70b, "prefix": prefix, "int8": int8, "fp8": fp8}
 
 
 # ------------------------------------------------------------------ byte accounting
@@ -230,9 +237,10 @@ def decode_algorithmic_bytes(case: PagedCase, unique_blocks: bool = False) -> in
     sequence's context once (int8: plus one fp32 scale per token, kv head and K/V), the
     queries, the outputs, the block-table entries and the context lengths.  With
     ``unique_blocks`` a physical block shared by several tables counts once."""
-    e = 1 if case.kv_dtype == "int8" else 2
+    quant = case.kv_dtype in ("int8", "fp8")
+    e = 1 if quant else 2
     ctx = case.context_lens.long().cpu()
-    per_token = case.Hkv * case.D * e * 2 + (case.Hkv * 2 * 4 if case.kv_dtype == "int8" else 0)
+    per_token = case.Hkv * case.D * e * 2 + (case.Hkv * 2 * 4 if quant else 0)
     if unique_blocks:
         seen = {}
         tabs = case.block_tables.cpu()
@@ -255,7 +263,7 @@ def append_algorithmic_bytes(case: PagedCase) -> int:
     """Bytes of one append of case.S new tokens: read K and V rows, write them (int8: codes
     and one fp32 scale per row), plus the slot numbers."""
     rows = case.S * case.Hkv
-    if case.kv_dtype == "int8":
+    if case.kv_dtype in ("int8", "fp8"):
         return rows * 2 * (case.D * 2 + case.D + 4) + case.S * 8
     return rows * 2 * case.D * 2 * 2 + case.S * 8
 
