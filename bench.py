@@ -152,7 +152,7 @@ class ClockSampler:
 class Step:
     """The device buffers and the calls of one decode step of one workload."""
 
-    def __init__(self, case: workloads.PagedCase, device, stream):
+    def __init__(self, case: workloads.PagedCase, device, stream, shared_prefix=False):
         import paged_kv_cache_197_gb300 as pa
 
         self.pa = pa
@@ -182,13 +182,26 @@ class Step:
             self.k_scale = self.v_scale = None
         self.max_ctx = int(c.context_lens.max())
         self.out = torch.empty_like(c.q)
-        self.ws = pa.decode_workspace(c.q, self.k_cache, self.max_ctx)
         self.flag = torch.zeros(1, dtype=torch.int32, device=device)
         self.cow = c.cow_pairs.cpu()
-        # append (or quantise-append) + decode (+ merge when split) + COW copies
-        ws_bytes = 0 if self.ws is None else self.ws.numel()
-        self.launches = (1 + 1 + (1 if ws_bytes else 0)
-                         + (math.ceil(self.cow.shape[0] / 256) if self.cow.shape[0] else 0))
+        cow_launches = math.ceil(self.cow.shape[0] / 256) if self.cow.shape[0] else 0
+        self.prefix = int(c.meta.get("prefix_tokens", 0)) if shared_prefix else 0
+        if shared_prefix and not self.prefix:
+            raise SystemExit("--shared-prefix needs a workload with a shared prefix")
+        if self.prefix:
+            # one group: every sequence of the batch shares the prompt's blocks
+            self.group_start = torch.tensor([0, c.S], dtype=torch.int32, device=device)
+            self.group_prefix = torch.tensor([self.prefix], dtype=torch.int32, device=device)
+            n = pa.pa_decode_shared_prefix_workspace_size(c.S, c.Hq, c.Hkv, c.D, c.bs,
+                                                          pa.kv_dtype_of(self.k_cache),
+                                                          self.max_ctx, c.S, self.prefix)
+            self.ws = torch.empty(n, dtype=torch.uint8, device=device)
+            # append + COW copies + setup, grouped prefix, own-token decode, merge
+            self.launches = 1 + cow_launches + 4
+        else:
+            self.ws = pa.decode_workspace(c.q, self.k_cache, self.max_ctx)
+            # append (or quantise-append) + decode (+ merge when split) + COW copies
+            self.launches = 1 + 1 + (1 if self.ws is not None else 0) + cow_launches
 
     def write_cache(self, new_key, new_value, slots):
         if self.cow.shape[0]:
@@ -202,6 +215,13 @@ class Step:
                                          err_flag=self.flag, stream=self.stream)
 
     def decode(self, q, tables, lens, out):
+        if self.prefix:
+            self.pa.pa_decode_shared_prefix(out, q, self.k_cache, self.v_cache, tables, lens,
+                                            self.case.scale, self.max_ctx, self.group_start,
+                                            self.group_prefix, self.case.S, self.prefix,
+                                            workspace=self.ws, err_flag=self.flag,
+                                            stream=self.stream)
+            return
         self.pa.pa_decode(out, q, self.k_cache, self.v_cache, tables, lens, self.case.scale,
                           self.max_ctx, workspace=self.ws, k_scale=self.k_scale,
                           v_scale=self.v_scale, err_flag=self.flag, stream=self.stream)
@@ -234,7 +254,7 @@ def run_ours(args, rank, world, device) -> dict | None:
     with torch.cuda.stream(stream):
         case = maker(seed=replica_seed(args.seed, rank), device=device, poison=False)
         torch.cuda.synchronize(device)
-        step = Step(case, device, stream)
+        step = Step(case, device, stream, shared_prefix=args.shared_prefix)
     nbytes = step_bytes(case)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) \
         if args.config in FLUSH_L2 else None
@@ -295,7 +315,15 @@ def run_ours(args, rank, world, device) -> dict | None:
         return None
 
     peaks = measured_peaks()
-    achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
+    if step.prefix:
+        # the grouped path must move each shared block once: the unique bytes are its
+        # algorithmic bytes (the per-sequence count stays in bytes_per_step)
+        achieved = nbytes["decode_unique"] / (dec_mean_ms * 1e-3) / 1e9
+        kernel_name = ("pa_decode_shared_prefix call (setup, grouped prefix, own-token "
+                       "decode, merge); algorithmic bytes count each shared block once")
+    else:
+        achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
+        kernel_name = "pa_decode call (decode + partition merge)"
     src_hash = decode_source_hash()
     traffic = NCU_TRAFFIC.get((args.config, src_hash))
     value = whole_job_gbs(nbytes["total"], world, ms_per_step)
@@ -315,14 +343,18 @@ def run_ours(args, rank, world, device) -> dict | None:
         "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "kernel": "pa_decode call (decode + partition merge)",
+                     "traffic": traffic, "kernel": kernel_name,
                      "peak_source": peaks["source"], "mean_decode_us": round(dec_mean_ms * 1e3, 2)},
         "e2e": e2e,
         "gpu_launches": step.launches * args.steps,
         "clocks": clocks,
         "kernel_source": src_hash,
     }
-    if args.config == "prefix":
+    if step.prefix:
+        res["config"]["decode_path"] = "shared-prefix (one group of all sequences)"
+        res["roofline"]["achieved_per_sequence_bytes"] = round(
+            nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9, 1)
+    elif args.config == "prefix":
         res["roofline"]["achieved_unique_bytes"] = round(
             nbytes["decode_unique"] / (dec_mean_ms * 1e-3) / 1e9, 1)
     if not args.no_cpu_baseline and not args.quick and world == 1:
@@ -485,6 +517,8 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared-prefix", action="store_true",
+                    help="decode through pa_decode_shared_prefix (workloads with a shared prefix)")
     ap.add_argument("--quick", action="store_true",
                     help="exactly W warm-up steps, no end-to-end or CPU legs (for profiler runs)")
     args = ap.parse_args()

@@ -64,8 +64,11 @@ enum { PA_KV_BF16 = 0, PA_KV_INT8 = 1, PA_KV_FP8 = 2 };
 enum {
     PA_FLAG_SLOT_OUT_OF_RANGE = 1,    /* slot_mapping[t] >= N * bs: token not written   */
     PA_FLAG_BLOCK_OUT_OF_RANGE = 2,   /* block_tables entry outside [0, N): block skipped */
-    PA_FLAG_CONTEXT_OUT_OF_RANGE = 4  /* context_lens[s] < 0, > M * bs or > max_context_len:
+    PA_FLAG_CONTEXT_OUT_OF_RANGE = 4, /* context_lens[s] < 0, > M * bs or > max_context_len:
                                          clamped to the valid range                        */
+    PA_FLAG_PREFIX_MISMATCH = 8       /* pa_decode_shared_prefix: a group or member did not
+                                         meet the prefix preconditions and was decoded on
+                                         its own (the result is still correct)            */
 };
 
 /* Version of this ABI (bumped on any signature change). */
@@ -187,6 +190,43 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
                     const int32_t *context_lens, int S, int Hq, int Hkv, int D, int bs, int N,
                     float scale, int max_context_len, void *workspace, size_t workspace_bytes,
                     int *err_flag, void *stream);
+
+/*
+ * Prefix-aware paged decode.  Same results as pa_decode (same arguments, same
+ * tolerance), for a batch in which groups of consecutive sequences share a prefix:
+ * the same physical blocks at the head of every member's block table, as prefix
+ * caching and branching produce (ia-vox-magazine, "PagedAttention : la revolution de
+ * l'allocation memoire": a shared 2000-token prompt is stored once; gotburnout.io,
+ * sections 3.01 and 3.02).  Each shared block is read from HBM once per kv head for
+ * the whole group instead of once per member.
+ *   group_start       device [n_groups + 1] int32, non-decreasing: group g is
+ *                     sequences [group_start[g], group_start[g + 1]).  Sequences in
+ *                     no group are decoded as by pa_decode.
+ *   group_prefix_len  device [n_groups] int32: shared prefix tokens of group g, a
+ *                     positive multiple of bs, at most max_prefix_len; every member's
+ *                     first group_prefix_len / bs table entries equal the first
+ *                     member's, and every member's context is at least that long.
+ *                     A group or member that fails these checks is decoded on its
+ *                     own and PA_FLAG_PREFIX_MISMATCH is raised.
+ *   max_group_size    host bound of the group sizes; max_prefix_len host bound of the
+ *                     prefixes (multiple of bs, <= max_context_len).
+ *   workspace         pa_decode_shared_prefix_workspace_size(...) bytes; contents
+ *                     not preserved.
+ * bf16 caches only (PA_ERR_UNSUPPORTED otherwise).
+ */
+size_t pa_decode_shared_prefix_workspace_size(int S, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                              int max_context_len, int max_group_size,
+                                              int max_prefix_len);
+
+pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
+                                  const void *v_cache, const float *k_scale, const float *v_scale,
+                                  int kv_dtype, const int32_t *block_tables, int M,
+                                  const int32_t *context_lens, int S, int Hq, int Hkv, int D, int bs,
+                                  int N, float scale, int max_context_len,
+                                  const int32_t *group_start, const int32_t *group_prefix_len,
+                                  int n_groups, int max_group_size, int max_prefix_len,
+                                  void *workspace, size_t workspace_bytes, int *err_flag,
+                                  void *stream);
 
 /*
  * Paged decode without any allocation: the same computation, arguments and

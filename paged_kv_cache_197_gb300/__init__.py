@@ -26,10 +26,11 @@ PA_KV_BF16, PA_KV_INT8, PA_KV_FP8 = 0, 1, 2
 PA_FLAG_SLOT_OUT_OF_RANGE = 1
 PA_FLAG_BLOCK_OUT_OF_RANGE = 2
 PA_FLAG_CONTEXT_OUT_OF_RANGE = 4
+PA_FLAG_PREFIX_MISMATCH = 8
 
 EXPORTED = ["pa_version", "pa_status_string", "pa_last_error_string", "pa_reshape_and_cache",
             "pa_quantize_kv", "pa_quantize_kv_fp8", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",
-            "pa_decode_noalloc"]
+            "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix"]
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -74,6 +75,12 @@ def load_library(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
                                       i32, i32, f32, i32, vp, vp]
     lib.pa_decode_noalloc.restype = i32
+    lib.pa_decode_shared_prefix_workspace_size.argtypes = [i32] * 9
+    lib.pa_decode_shared_prefix_workspace_size.restype = sz
+    lib.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
+                                            i32, i32, i32, f32, i32, vp, vp, i32, i32, i32, vp, sz,
+                                            vp, vp]
+    lib.pa_decode_shared_prefix.restype = i32
     if path is None:
         _LIB = lib
     return lib
@@ -293,6 +300,52 @@ def pa_decode_noalloc(out, query, k_cache, v_cache, block_tables, context_lens, 
                                  block_tables.shape[1], _ptr(context_lens), S, Hq, Hkv, D, bs, N,
                                  float(scale), int(max_context_len), _flag(err_flag),
                                  _stream(stream, query.device)))
+
+
+def pa_decode_shared_prefix_workspace_size(S: int, Hq: int, Hkv: int, D: int, bs: int,
+                                           kv_dtype: int, max_context_len: int,
+                                           max_group_size: int, max_prefix_len: int) -> int:
+    return int(load_library().pa_decode_shared_prefix_workspace_size(
+        S, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_group_size, max_prefix_len))
+
+
+def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_lens,
+                            scale: float, max_context_len: int, group_start, group_prefix_len,
+                            max_group_size: int, max_prefix_len: int, workspace=None,
+                            err_flag=None, stream=None) -> None:
+    """Paged decode of a batch whose groups of consecutive sequences share prefix blocks;
+    the same result as pa_decode.  group_start [n_groups + 1] and group_prefix_len
+    [n_groups] are int32 device tensors; workspace defaults to a fresh allocation."""
+    _cuda(out, "out", torch.bfloat16, 3)
+    _cuda(query, "query", torch.bfloat16, 3)
+    kv_dtype = kv_dtype_of(k_cache)
+    _cuda(k_cache, "k_cache", k_cache.dtype, 4)
+    _cuda(v_cache, "v_cache", k_cache.dtype, 4)
+    _cuda(block_tables, "block_tables", torch.int32, 2)
+    _cuda(context_lens, "context_lens", torch.int32, 1)
+    _cuda(group_start, "group_start", torch.int32, 1)
+    _cuda(group_prefix_len, "group_prefix_len", torch.int32, 1)
+    S, Hq, D = query.shape
+    N, Hkv, bs, D2 = k_cache.shape
+    M = block_tables.shape[1]
+    n_groups = group_prefix_len.shape[0]
+    if out.shape != query.shape or v_cache.shape != k_cache.shape or D2 != D \
+            or block_tables.shape[0] != S or context_lens.shape[0] != S \
+            or group_start.shape[0] != n_groups + 1:
+        raise ValueError("pa_decode_shared_prefix: shape mismatch")
+    if workspace is None:
+        n = pa_decode_shared_prefix_workspace_size(S, Hq, Hkv, D, bs, kv_dtype, max_context_len,
+                                                   max_group_size, max_prefix_len)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=query.device)
+    _cuda(workspace, "workspace", workspace.dtype)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    lib = load_library()
+    _check(lib.pa_decode_shared_prefix(
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), None, None, kv_dtype,
+        _ptr(block_tables), M, _ptr(context_lens), S, Hq, Hkv, D, bs, N, float(scale),
+        int(max_context_len), _ptr(group_start), _ptr(group_prefix_len), n_groups,
+        int(max_group_size), int(max_prefix_len), _ptr(workspace), ws_bytes, _flag(err_flag),
+        _stream(stream, query.device)))
 
 
 def decode_workspace(query, k_cache, max_context_len: int) -> torch.Tensor | None:

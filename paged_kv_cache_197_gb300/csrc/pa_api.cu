@@ -332,4 +332,141 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
     return check_launch(fn);
 }
 
+// Workspace of the shared-prefix decode: per-sequence start and group, prefix
+// partials per 128-token chunk, own-token partials per partition.
+struct PrefixPlan {
+    DecodePlan own;
+    int PP, CB, MP;
+    size_t start_off, group_off, pacc_off, pml_off, acc_off, ml_off, bytes;
+};
+
+static PrefixPlan plan_prefix(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len,
+                              int max_group_size, int max_prefix_len) {
+    PrefixPlan p{};
+    // the own tokens of a member of a group with the longest prefix number at most
+    // max_context_len - max_prefix_len: partitions are sized for that length; longer
+    // own ranges (shorter prefixes, sequences in no group) just take more partitions
+    const int own_len = std::max(1, max_context_len - max_prefix_len);
+    p.own = plan_decode(S, Hq, Hkv, D, bs, kv_dtype, own_len);
+    p.own.part_tokens = (int)align_up((size_t)p.own.part_tokens, 64);  // whole tiles and blocks
+    p.MP = std::max(1, (max_context_len + p.own.part_tokens - 1) / p.own.part_tokens);
+    const int chunk = prefix_chunk_tokens();
+    p.PP = (max_prefix_len + chunk - 1) / chunk;
+    p.CB = std::max(1, (max_group_size * (Hq / Hkv) + prefix_cols_per_cta() - 1) / prefix_cols_per_cta());
+    const size_t rows_pre = (size_t)S * Hq * p.PP, rows_own = (size_t)S * Hq * p.MP;
+    p.start_off = 0;
+    p.group_off = align_up((size_t)S * sizeof(int32_t), 256);
+    p.pacc_off = align_up(p.group_off + (size_t)S * sizeof(int32_t), 256);
+    p.pml_off = align_up(p.pacc_off + rows_pre * D * sizeof(float), 256);
+    p.acc_off = align_up(p.pml_off + rows_pre * 2 * sizeof(float), 256);
+    p.ml_off = align_up(p.acc_off + rows_own * D * sizeof(float), 256);
+    p.bytes = align_up(p.ml_off + rows_own * 2 * sizeof(float), 256);
+    return p;
+}
+
+static pa_status check_prefix_args(const char *fn, int S, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                   int max_context_len, int n_groups, int max_group_size,
+                                   int max_prefix_len) {
+    pa_status st = check_decode_shape(fn, S, Hq, Hkv, D, bs, kv_dtype, max_context_len);
+    if (st != PA_OK) return st;
+    if (kv_dtype != PA_KV_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "%s: only bf16 caches are supported", fn);
+    if (n_groups < 0 || n_groups > 65535)
+        return fail(PA_ERR_INVALID_ARG, "%s: n_groups = %d", fn, n_groups);
+    if (max_prefix_len < 0 || max_prefix_len % bs != 0 || max_prefix_len > max_context_len)
+        return fail(PA_ERR_INVALID_ARG, "%s: max_prefix_len = %d must be a multiple of %d within max_context_len",
+                    fn, max_prefix_len, bs);
+    if (max_group_size < 1 || max_group_size > S)
+        return fail(PA_ERR_INVALID_ARG, "%s: max_group_size = %d", fn, max_group_size);
+    const int64_t cb = ((int64_t)max_group_size * (Hq / Hkv) + prefix_cols_per_cta() - 1) / prefix_cols_per_cta();
+    if ((int64_t)Hkv * cb > 65535) return fail(PA_ERR_UNSUPPORTED, "%s: groups too large", fn);
+    return PA_OK;
+}
+
+size_t pa_decode_shared_prefix_workspace_size(int S, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                              int max_context_len, int max_group_size,
+                                              int max_prefix_len) {
+    if (check_prefix_args("pa_decode_shared_prefix_workspace_size", S, Hq, Hkv, D, bs, kv_dtype,
+                          max_context_len, 0, max_group_size, max_prefix_len) != PA_OK)
+        return 0;
+    return plan_prefix(S, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_group_size, max_prefix_len).bytes;
+}
+
+pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
+                                  const void *v_cache, const float *k_scale, const float *v_scale,
+                                  int kv_dtype, const int32_t *block_tables, int M,
+                                  const int32_t *context_lens, int S, int Hq, int Hkv, int D, int bs,
+                                  int N, float scale, int max_context_len,
+                                  const int32_t *group_start, const int32_t *group_prefix_len,
+                                  int n_groups, int max_group_size, int max_prefix_len,
+                                  void *workspace, size_t workspace_bytes, int *err_flag,
+                                  void *stream) {
+    const char *fn = "pa_decode_shared_prefix";
+    g_last_error[0] = 0;
+    (void)k_scale;
+    (void)v_scale;
+    if (S == 0) return PA_OK;
+    pa_status st = check_prefix_args(fn, S, Hq, Hkv, D, bs, kv_dtype, max_context_len, n_groups,
+                                      max_group_size, max_prefix_len);
+    if (st != PA_OK) return st;
+    if (N <= 0 || M <= 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: N = %d, M = %d must be positive", fn, N, M);
+    if ((int64_t)max_context_len > (int64_t)M * bs)
+        return fail(PA_ERR_OUT_OF_RANGE, "%s: max_context_len %d exceeds M * bs = %lld", fn,
+                    max_context_len, (long long)M * bs);
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (n_groups > 0 && (!group_start || !group_prefix_len))
+        return fail(PA_ERR_INVALID_ARG, "%s: group arrays missing", fn);
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
+    if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
+        return fail(PA_ERR_INVALID_ARG, "%s: scale must be finite", fn);
+    const PrefixPlan plan = plan_prefix(S, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_group_size,
+                                        max_prefix_len);
+    if (!workspace || workspace_bytes < plan.bytes)
+        return fail(PA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, plan.bytes,
+                    workspace ? workspace_bytes : (size_t)0);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
+    char *ws = static_cast<char *>(workspace);
+    DecodeArgs a{};
+    a.out = out;
+    a.q = query;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.ws_acc = (float *)(ws + plan.acc_off);
+    a.ws_ml = (float *)(ws + plan.ml_off);
+    a.err_flag = err_flag;
+    a.M = M;
+    a.S = S;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.N = N;
+    a.head_chunks = plan.own.head_chunks;
+    a.part_tokens = plan.own.part_tokens;
+    a.max_parts = plan.MP;
+    a.max_context_len = max_context_len;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.start_tokens = (const int32_t *)(ws + plan.start_off);
+    a.partials_only = 1;
+    PrefixArgs p{};
+    p.group_start = group_start;
+    p.group_prefix = group_prefix_len;
+    p.n_groups = n_groups;
+    p.max_group_size = max_group_size;
+    p.max_prefix = max_prefix_len;
+    p.seq_start = (int32_t *)(ws + plan.start_off);
+    p.seq_group = (int32_t *)(ws + plan.group_off);
+    p.pacc = (float *)(ws + plan.pacc_off);
+    p.pml = (float *)(ws + plan.pml_off);
+    p.PP = plan.PP;
+    p.CB = plan.CB;
+    launch_decode_shared_prefix(a, p, D, bs, (cudaStream_t)stream);
+    return check_launch(fn);
+}
+
 }  // extern "C"

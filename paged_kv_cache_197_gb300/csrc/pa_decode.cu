@@ -452,9 +452,12 @@ paged_decode_kernel(const DecodeArgs a) {
     const int g = lane >> 2, t = lane & 3;
 
     const int ctx = checked_context(a, s, BS, part == 0 && blockIdx.y == 0 && tid == 0);
-    const int nparts = max(1, (ctx + a.part_tokens - 1) / a.part_tokens);
+    // tokens before `start` (a shared prefix, attended by the grouped prefix kernel)
+    // are skipped; start is a multiple of the block size
+    const int start = a.start_tokens ? min(a.start_tokens[s], ctx) : 0;
+    const int nparts = max(1, (ctx - start + a.part_tokens - 1) / a.part_tokens);
     if (part >= nparts) return;
-    const int tok_begin = part * a.part_tokens;
+    const int tok_begin = start + part * a.part_tokens;
     const int tok_end = min(ctx, tok_begin + a.part_tokens);
     const int blk_begin = tok_begin / BS;
     const int nblk = max(0, (tok_end - tok_begin + BS - 1) / BS);
@@ -569,7 +572,7 @@ paged_decode_kernel(const DecodeArgs a) {
         for (int e = 0; e < DPT; ++e) acc[e] += f * s_o[w][hj][d0 + e];
     }
     const int h = h0 + hj;
-    if (nparts == 1) {
+    if (nparts == 1 && !a.partials_only) {
         const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
         uint32_t packed[DPT / 2];
 #pragma unroll
@@ -658,7 +661,7 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
     paged_decode_kernel<KV, D, BS, TILE><<<grid, kThreads, 0, stream>>>(a);
     cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess || a.max_parts == 1) return err;
+    if (err != cudaSuccess || a.max_parts == 1 || a.partials_only) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((int64_t)a.S * a.Hq + 3) / 4));
     cfg.blockDim = dim3(128);

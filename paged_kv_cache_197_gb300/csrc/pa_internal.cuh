@@ -46,7 +46,28 @@ struct DecodeArgs {
     int head_chunks, part_tokens, max_parts;
     int max_context_len;  // host bound; longer contexts are clamped and flagged
     float scale_log2;  // softmax scale times log2(e)
+    const int32_t *start_tokens;  // nullable [S]: tokens to skip (a shared prefix)
+    int partials_only;            // write partial results even for a single partition
 };
+
+// Shared-prefix decode: groups of consecutive sequences whose block tables start with
+// the same prefix blocks.
+struct PrefixArgs {
+    const int32_t *group_start;   // [n_groups + 1]: group g = sequences [start[g], start[g+1])
+    const int32_t *group_prefix;  // [n_groups]: shared prefix tokens (multiple of bs)
+    int n_groups, max_group_size, max_prefix;
+    int32_t *seq_start;           // [S] workspace: prefix tokens each sequence skips
+    int32_t *seq_group;           // [S] workspace: its group, or -1
+    float *pacc;                  // [S][Hq][PP][D] prefix partials
+    float *pml;                   // [S][Hq][PP][2]
+    int PP;                       // prefix chunks of the longest prefix
+    int CB;                       // blocks of 128 query columns per kv head
+};
+
+int prefix_chunk_tokens();
+int prefix_cols_per_cta();
+cudaError_t launch_decode_shared_prefix(const DecodeArgs &a, const PrefixArgs &p, int D, int bs,
+                                        cudaStream_t stream);
 
 // ------------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing was launched).

@@ -23,9 +23,12 @@ def int8_pool_rows(pool: torch.Tensor) -> torch.Tensor:
     return pool.permute(0, 2, 1, 3).reshape(N * bs, Hkv, D).contiguous()
 
 
-def gpu_step(case: workloads.PagedCase, device, max_context_len=None, poison_int8=True):
+def gpu_step(case: workloads.PagedCase, device, max_context_len=None, poison_int8=True,
+             groups=None):
     """COW copy, append (or quantise-append), decode on the GPU.
 
+    ``groups`` = (group_start, group_prefix_len, max_group_size, max_prefix_len) decodes
+    through pa_decode_shared_prefix instead of pa_decode.
     Returns dict(out, k_cache, v_cache, k_scale, v_scale, flag) on the device."""
     import paged_kv_cache_197_gb300 as pa
 
@@ -62,9 +65,18 @@ def gpu_step(case: workloads.PagedCase, device, max_context_len=None, poison_int
     if max_context_len is None:
         max_context_len = int(case.context_lens.max()) if case.S else 0
     out = torch.full_like(c.q, float("nan"))
-    ws = pa.decode_workspace(c.q, k_cache, max_context_len)
-    pa.pa_decode(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens, case.scale,
-                 max_context_len, workspace=ws, k_scale=k_scale, v_scale=v_scale, err_flag=flag)
+    if groups is not None:
+        starts, plens, max_group, max_prefix = groups
+        gs = torch.as_tensor(starts, dtype=torch.int32).to(device)
+        gp = torch.as_tensor(plens, dtype=torch.int32).to(device)
+        pa.pa_decode_shared_prefix(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens,
+                                   case.scale, max_context_len, gs, gp, max_group, max_prefix,
+                                   err_flag=flag)
+    else:
+        ws = pa.decode_workspace(c.q, k_cache, max_context_len)
+        pa.pa_decode(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens, case.scale,
+                     max_context_len, workspace=ws, k_scale=k_scale, v_scale=v_scale,
+                     err_flag=flag)
     torch.cuda.synchronize(device)
     return dict(out=out, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
                 flag=int(flag.item()))

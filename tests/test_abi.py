@@ -74,6 +74,25 @@ def test_decode_host_checks(lib):
     assert call(S=0) == pa.PA_OK  # nothing to do, nothing queued
 
 
+def part_tokens(units, max_ctx, slots=304):
+    """The partition length pa_decode chooses (a model of its policy)."""
+    import math
+
+    if units >= 6 * slots and max_ctx <= 4096:
+        return max(max_ctx, 1)
+    best, best_p = -1.0, 256
+    for cand in (4096, 3072, 2048, 1536, 1024, 768, 512, 384, 256):
+        n = max(1, -(-max_ctx // cand))
+        waves = units * n / slots
+        if waves < 3:
+            continue
+        ln = min(cand, max(max_ctx, 1))
+        score = waves / math.ceil(waves) * ln / (ln + 64)
+        if score > best + 1e-9:
+            best, best_p = score, cand
+    return best_p
+
+
 def test_workspace_size(lib):
     """Partition length: no split when the units alone give 6 waves of 2 CTAs per SM (152
     SMs without a GPU) and contexts are <= 4096 tokens; else the best of (last-wave fill)
@@ -84,19 +103,7 @@ def test_workspace_size(lib):
     import paged_kv_cache_197_gb300 as pa
 
     def parts(units, max_ctx, slots=304):
-        if units >= 6 * slots and max_ctx <= 4096:
-            return 1
-        best, best_p = -1.0, 256
-        for cand in (4096, 3072, 2048, 1536, 1024, 768, 512, 384, 256):
-            n = max(1, -(-max_ctx // cand))
-            waves = units * n / slots
-            if waves < 3:
-                continue
-            ln = min(cand, max(max_ctx, 1))
-            score = waves / math.ceil(waves) * ln / (ln + 64)
-            if score > best + 1e-9:
-                best, best_p = score, cand
-        return max(1, -(-max_ctx // best_p))
+        return max(1, -(-max_ctx // part_tokens(units, max_ctx, slots)))
 
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     for S, Hq, Hkv, D, max_ctx in [(64, 40, 40, 128, 2048), (64, 40, 40, 128, 200), (20, 64, 8, 128, 8000), (256, 32, 8, 128, 32768), (2, 8, 2, 64, 1000),
@@ -107,6 +114,58 @@ def test_workspace_size(lib):
         assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, 16, pa.PA_KV_BF16, max_ctx) == expect
     assert parts(160, 8000) == 11  # 768-token partitions for the 70B-shaped workload
     assert pa.pa_decode_workspace_size(1, 3, 2, 128, 16, 0, 100) == 0  # invalid -> 0
+
+
+def test_shared_prefix_workspace_and_checks(lib):
+    """Workspace of the prefix-aware decode: S int32 group ids and S start offsets, then
+    (D + 2) fp32 per query head and 128-token prefix chunk, then (D + 2) fp32 per query
+    head and own-token partition; partitions sized for max_context_len - max_prefix_len
+    (rounded up to 64 tokens), counted over max_context_len; each region 256-byte
+    aligned.  Host checks refuse what the kernels do not take."""
+    import paged_kv_cache_197_gb300 as pa
+
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for S, Hq, Hkv, D, bs, max_ctx, max_group, max_prefix in [
+            (50, 32, 8, 128, 16, 2512, 50, 2000), (8, 4, 4, 64, 32, 1372, 8, 672),
+            (5, 8, 2, 128, 16, 9000, 1, 0), (56, 64, 16, 64, 32, 1005, 40, 640)]:
+        units = S * Hkv * ((Hq // Hkv + 7) // 8)
+        pt = -(-part_tokens(units, max(1, max_ctx - max_prefix)) // 64) * 64
+        MP = max(1, -(-max_ctx // pt))
+        PP = -(-max_prefix // 128)
+        pre, own = S * Hq * PP, S * Hq * MP
+        size = up(S * 4) + S * 4
+        size = up(size) + pre * D * 4
+        size = up(size) + pre * 2 * 4
+        size = up(size) + own * D * 4
+        size = up(up(size) + own * 2 * 4)
+        got = pa.pa_decode_shared_prefix_workspace_size(S, Hq, Hkv, D, bs, pa.PA_KV_BF16, max_ctx,
+                                                        max_group, max_prefix)
+        assert got == size, (S, got, size)
+    ws = lambda **k: pa.pa_decode_shared_prefix_workspace_size(  # noqa: E731
+        **{**dict(S=4, Hq=8, Hkv=2, D=128, bs=16, kv_dtype=0, max_context_len=512,
+                  max_group_size=4, max_prefix_len=256), **k})
+    assert ws() > 0
+    assert ws(kv_dtype=pa.PA_KV_INT8) == 0      # bf16 caches only
+    assert ws(max_prefix_len=200) == 0          # not whole blocks
+    assert ws(max_prefix_len=1024) == 0         # longer than any context
+    assert ws(max_group_size=0) == 0
+    assert ws(max_group_size=5) == 0            # more members than sequences
+
+    fake = 1 << 20
+
+    def call(S=2, kv=pa.PA_KV_BF16, n_groups=1, gs=fake, max_group=2, max_prefix=32, ws=fake,
+             ws_bytes=1 << 30):
+        return lib.pa_decode_shared_prefix(fake, fake, fake, fake, None, None, kv, fake, 4, fake, S,
+                                           8, 2, 128, 16, 4, 0.1, 64, gs, fake, n_groups,
+                                           max_group, max_prefix, ws, ws_bytes, None, None)
+
+    assert call(kv=pa.PA_KV_FP8) == pa.PA_ERR_UNSUPPORTED
+    assert call(gs=None) == pa.PA_ERR_INVALID_ARG
+    assert call(n_groups=-1) == pa.PA_ERR_INVALID_ARG
+    assert call(max_prefix=48 + 8) == pa.PA_ERR_INVALID_ARG
+    assert call(ws_bytes=64) == pa.PA_ERR_INVALID_ARG
+    assert call(ws=fake + 16) == pa.PA_ERR_INVALID_ARG  # not 256-byte aligned
+    assert call(S=0) == pa.PA_OK
 
 
 def test_cache_host_checks(lib):
