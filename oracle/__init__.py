@@ -101,6 +101,9 @@ class Oracle:
         lib.oracle_attention_weights.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp,
                                                  i32, i32, i32, i32, i32, dbl, i32, i32]
         lib.oracle_attention_weights.restype = i32
+        lib.oracle_paged_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32,
+                                             i32, i32, i32, i32, i32, dbl]
+        lib.oracle_paged_prefill.restype = i32
         self.lib = lib
 
     @property
@@ -213,6 +216,40 @@ class Oracle:
             kv_dtype, _ptr(block_tables), M, _ptr(context_lens), S, Hq, Hkv, D, bs, float(scale))
         if rc != 0:
             raise RuntimeError(f"oracle_paged_attention failed: {rc}")
+        return out
+
+    def paged_prefill(self, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                      scale: float, k_scale=None, v_scale=None) -> np.ndarray:
+        """fp64 output [T][Hq][D] of multi-token paged attention: the rows
+        query_start[s] .. query_start[s+1]-1 are sequence s's newest tokens, each
+        attending the tokens up to its own position."""
+        _need(q, np.uint16, "q")
+        _need(block_tables, np.int32, "block_tables")
+        _need(context_lens, np.int32, "context_lens")
+        _need(query_start, np.int32, "query_start")
+        kv_dtype = {np.dtype(np.int8): KV_INT8, np.dtype(np.uint8): KV_FP8}.get(k_cache.dtype, KV_BF16)
+        if kv_dtype == KV_BF16:
+            _need(k_cache, np.uint16, "k_cache")
+            _need(v_cache, np.uint16, "v_cache")
+        else:
+            _need(v_cache, k_cache.dtype, "v_cache")
+            _need(k_scale, np.float32, "k_scale")
+            _need(v_scale, np.float32, "v_scale")
+        T, Hq, D = q.shape
+        S = context_lens.shape[0]
+        if query_start.shape[0] != S + 1:
+            raise ValueError("query_start must hold S + 1 offsets")
+        _, Hkv, bs, D2 = k_cache.shape
+        if D2 != D:
+            raise ValueError("head_dim mismatch between q and cache")
+        M = block_tables.shape[1] if block_tables.ndim == 2 else 0
+        out = np.zeros((T, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_paged_prefill(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            kv_dtype, _ptr(block_tables), M, _ptr(context_lens), _ptr(query_start), S, T, Hq,
+            Hkv, D, bs, float(scale))
+        if rc != 0:
+            raise RuntimeError(f"oracle_paged_prefill failed: {rc}")
         return out
 
     def attention_weights(self, q, k_cache, v_cache, block_tables, context_lens, scale: float,

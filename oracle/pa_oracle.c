@@ -442,6 +442,80 @@ int oracle_paged_attention(double *out, const uint16_t *q, const void *k_cache,
     return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
+/* Multi-token paged attention: the step that attends several new tokens of a
+ * sequence at once -- a chunk of a long prompt (chunked prefill: deeplearn.tn, "Les
+ * leviers d'optimisation en production"; gaiatechstar.com discussion, the reply on
+ * chunked prefill) or the draft tokens a large model checks in one pass
+ * (speculative decoding, same deeplearn.tn section).
+ *
+ * Sequence s brings L_s = query_start[s + 1] - query_start[s] new tokens whose K and
+ * V are already in the cache at logical positions ctx_s - L_s .. ctx_s - 1
+ * (ctx_s = context_lens[s] counts them).  New token i (query row
+ * query_start[s] + i) sits at position p = ctx_s - L_s + i and attends every token
+ * up to and including its own:
+ *   out[row][h] = attention(q[row][h], K_s[0..p], V_s[0..p]),
+ * which is exactly what one decode step per token, in order, would give (reading:
+ * a token never sees the tokens after it; with L_s = 1 this is the decode step).
+ * q and out are [T][Hq][D] (bf16 in, fp64 out); rows outside every
+ * [query_start[s], query_start[s + 1]) are set to zero. */
+int oracle_paged_prefill(double *out, const uint16_t *q, const void *k_cache,
+                         const void *v_cache, const float *k_scale,
+                         const float *v_scale, int kv_dtype,
+                         const int32_t *block_tables, int M,
+                         const int32_t *context_lens, const int32_t *query_start,
+                         int S, int T, int Hq, int Hkv, int D, int bs, double scale)
+{
+    int rc = check_attention_args(S, Hq, Hkv, D, bs, M, context_lens, kv_dtype);
+    if (rc != ORACLE_OK)
+        return rc;
+    if (T < 0 || query_start[0] < 0 || query_start[S] > T)
+        return ORACLE_BAD_ARG;
+    for (int s = 0; s < S; ++s) {
+        int L = query_start[s + 1] - query_start[s];
+        if (L < 0 || L > context_lens[s])
+            return ORACLE_BAD_ARG;
+    }
+    memset(out, 0, (size_t)T * (size_t)Hq * (size_t)D * sizeof(double));
+    int G = Hq / Hkv;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1) collapse(2) reduction(| : failed)
+    for (int s = 0; s < S; ++s) {
+        for (int hk = 0; hk < Hkv; ++hk) {
+            int ctx = context_lens[s];
+            int L = query_start[s + 1] - query_start[s];
+            size_t n = (size_t)(ctx > 0 ? ctx : 1);
+            double *K = malloc(n * (size_t)D * sizeof(double));
+            double *V = malloc(n * (size_t)D * sizeof(double));
+            double *w = malloc(n * sizeof(double));
+            double *qd = malloc((size_t)D * sizeof(double));
+            if (!K || !V || !w || !qd) {
+                failed = 1;
+            } else {
+                gather_sequence(K, V, k_cache, v_cache, k_scale, v_scale,
+                                kv_dtype, block_tables + (int64_t)s * M, ctx,
+                                hk, Hkv, D, bs);
+                for (int i = 0; i < L; ++i) {
+                    int64_t row = (int64_t)query_start[s] + i;
+                    int visible = ctx - L + i + 1; /* positions 0 .. ctx - L + i */
+                    for (int g = 0; g < G; ++g) {
+                        int h = hk * G + g;
+                        const uint16_t *qs = q + (row * Hq + h) * D;
+                        for (int d = 0; d < D; ++d)
+                            qd[d] = bf16_to_double(qs[d]);
+                        attend(out + (row * Hq + h) * D, w, qd, K, V, visible, D,
+                               scale);
+                    }
+                }
+            }
+            free(K);
+            free(V);
+            free(w);
+            free(qd);
+        }
+    }
+    return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
 /* Softmax weights of one (sequence s, query head h) pair, in logical token
  * order; w receives context_lens[s] values. */
 int oracle_attention_weights(double *w, const uint16_t *q, const void *k_cache,

@@ -423,10 +423,73 @@ def pin_brute_force_fp8(orc):
             assert np.allclose(out[s, h], ref, rtol=1e-12, atol=1e-13), (s, h)
 
 
+def _prefill_case(rng):
+    """Three sequences with new-token chunks of 3, 1 and 3 (the last one's whole
+    context is its chunk), query rows packed from row 1 on; rows 0 and 8 belong to
+    no sequence."""
+    S, Hq, Hkv, D, bs, N = 3, 4, 2, 8, 4, 16
+    ctx = [7, 12, 3]
+    qs = np.array([1, 4, 5, 8], dtype=np.int32)
+    T = 9
+    _, lk, lv, kp, vp, tables, lens = _tiny_random_case(rng, S, Hq, Hkv, D, bs, ctx, N)
+    q = to_bf16_bits(rng.standard_normal((T, Hq, D)))
+    return q, lk, lv, kp, vp, tables, lens, qs, Hq // Hkv
+
+
+def pin_brute_force_prefill(orc):
+    """Multi-token attention: new token i of sequence s (row query_start[s] + i) equals
+    40-digit softmax attention over the unpaged logical K/V up to and including its
+    own position ctx_s - L_s + i; rows of no sequence are zero."""
+    rng = np.random.default_rng(21)
+    q, lk, lv, kp, vp, tables, lens, qs, G = _prefill_case(rng)
+    scale = 0.41
+    out = orc.paged_prefill(q, kp, vp, tables, lens, qs, scale)
+    qf = bf16_bits_to_f64(q)
+    covered = set()
+    for s in range(len(lens)):
+        L = qs[s + 1] - qs[s]
+        for i in range(L):
+            row, pos = qs[s] + i, lens[s] - L + i
+            covered.add(row)
+            for h in range(q.shape[1]):
+                K = bf16_bits_to_f64(lk[s][: pos + 1, h // G, :])
+                V = bf16_bits_to_f64(lv[s][: pos + 1, h // G, :])
+                ref = brute_attention(qf[row, h], K, V, scale)
+                assert np.allclose(out[row, h], ref, rtol=1e-12, atol=1e-13), (s, i, h)
+    for row in range(q.shape[0]):
+        if row not in covered:
+            assert np.array_equal(out[row], np.zeros_like(out[row]))
+
+
+def pin_prefill_causality(orc):
+    """A new token never reads a later position: NaN written into every slot after
+    token i's position leaves row i bit-identical (and finite).  The first token of a
+    chunk that is the whole context sees one token: its output is that value row."""
+    rng = np.random.default_rng(22)
+    q, lk, lv, kp, vp, tables, lens, qs, G = _prefill_case(rng)
+    bs = kp.shape[2]
+    base = orc.paged_prefill(q, kp, vp, tables, lens, qs, 0.8)
+    for s in range(len(lens)):
+        L = qs[s + 1] - qs[s]
+        for i in range(L):
+            pos = lens[s] - L + i
+            kq, vq = kp.copy(), vp.copy()
+            for t in range(pos + 1, lens[s]):
+                kq[tables[s][t // bs], :, t % bs, :] = 0x7FC0
+                vq[tables[s][t // bs], :, t % bs, :] = 0x7FC0
+            out = orc.paged_prefill(q, kq, vq, tables, lens, qs, 0.8)
+            row = qs[s] + i
+            assert np.all(np.isfinite(out[row])) and np.array_equal(out[row], base[row]), (s, i)
+    s = 2  # context == chunk: the first new token attends itself only
+    for h in range(q.shape[1]):
+        assert np.array_equal(base[qs[s], h], bf16_bits_to_f64(lv[s][0, h // G, :]))
+
+
 ALL_PINS = [pin_slot_figure, pin_append_places_rows, pin_brute_force_bf16, pin_brute_force_int8,
             pin_closed_forms, pin_block_permutation_invariance, pin_prefix_shared_equals_copied,
             pin_softmax_weights, pin_quantizer_hand_values, pin_copy_blocks, pin_fp8_hand_values,
-            pin_fp8_round_trip_and_ties, pin_fp8_quantizer, pin_brute_force_fp8]
+            pin_fp8_round_trip_and_ties, pin_fp8_quantizer, pin_brute_force_fp8,
+            pin_brute_force_prefill, pin_prefill_causality]
 
 
 def run_all(orc) -> list[str]:

@@ -50,6 +50,11 @@ MUTANTS = {
     "fp8_decode_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
     "fp8_no_saturation": ("    if (v > 448.0)\n        v = 448.0;\n", ""),
     "fp8_scale_127": ("absmax / 448.0f", "absmax / 127.0f"),
+    "prefill_mask_excludes_self": ("int visible = ctx - L + i + 1;", "int visible = ctx - L + i;"),
+    "prefill_no_causal_mask": ("int visible = ctx - L + i + 1;", "int visible = ctx;"),
+    "prefill_row_ignores_start": ("int64_t row = (int64_t)query_start[s] + i;", "int64_t row = (int64_t)i;"),
+    "prefill_gqa_grouping": ("                        int h = hk * G + g;\n                        const uint16_t *qs = q + (row * Hq + h) * D;",
+                             "                        int h = g * Hkv + hk;\n                        const uint16_t *qs = q + (row * Hq + h) * D;"),
     "empty_context_garbage": ("    for (int d = 0; d < D; ++d)\n        out[d] = 0.0;\n    if (ctx == 0)",
                               "    for (int d = 0; d < D; ++d)\n        out[d] = 1.0;\n    if (ctx == 0)"),
 }
