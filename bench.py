@@ -49,8 +49,12 @@ DESCRIPTIONS = {
     "int8": "int8 KV decode: Llama-3-8B shape 32/8 heads, head_dim 128, block 32, 256 seqs, "
             "ctx log-uniform [128,32768], 1-token quantise+append per seq",
     "fp8": "fp8 (e4m3) KV decode: the int8 workload's shape with an fp8 cache and per-token scales",
+    "verify70b": "draft verification, Llama-3-70B-shaped GQA: 20 seqs x 8000 tokens, 4 new tokens each "
+                 "(causal among them), 64/8 heads, head_dim 128, block 16",
+    "prefill8b": "chunked prefill, Llama-3-8B shape: 4 seqs x 512-token chunk on 3584 cached tokens, "
+                 "32/8 heads, head_dim 128, block 16",
 }
-FLUSH_L2 = {"tiny", "prefix"}
+FLUSH_L2 = {"tiny", "prefix", "prefill8b"}
 L2_BYTES = 126 * 1024 * 1024
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one decode launch, from an ncu capture
@@ -62,8 +66,9 @@ def measured_peaks() -> dict:
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
         d = json.loads(p.read_text())
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 def decode_source_hash() -> str:
@@ -185,10 +190,19 @@ class Step:
         self.flag = torch.zeros(1, dtype=torch.int32, device=device)
         self.cow = c.cow_pairs.cpu()
         cow_launches = math.ceil(self.cow.shape[0] / 256) if self.cow.shape[0] else 0
+        self.multi = c.query_start is not None  # several new tokens per sequence
         self.prefix = int(c.meta.get("prefix_tokens", 0)) if shared_prefix else 0
         if shared_prefix and not self.prefix:
             raise SystemExit("--shared-prefix needs a workload with a shared prefix")
-        if self.prefix:
+        if self.multi:
+            self.max_q = max(c.meta["query_lens"])
+            n = pa.pa_multi_token_workspace_size(c.S, c.q.shape[0], c.Hq, c.Hkv, c.D, c.bs,
+                                                 pa.kv_dtype_of(self.k_cache), self.max_ctx,
+                                                 self.max_q)
+            self.ws = torch.empty(n, dtype=torch.uint8, device=device) if n else None
+            # append + attention (+ merge when split) + COW copies
+            self.launches = 1 + 1 + (1 if self.ws is not None else 0) + cow_launches
+        elif self.prefix:
             # one group: every sequence of the batch shares the prompt's blocks
             self.group_start = torch.tensor([0, c.S], dtype=torch.int32, device=device)
             self.group_prefix = torch.tensor([self.prefix], dtype=torch.int32, device=device)
@@ -214,7 +228,13 @@ class Step:
             self.pa.pa_reshape_and_cache(new_key, new_value, self.k_cache, self.v_cache, slots,
                                          err_flag=self.flag, stream=self.stream)
 
-    def decode(self, q, tables, lens, out):
+    def decode(self, q, tables, lens, out, query_start=None):
+        if self.multi:
+            self.pa.pa_multi_token_attention(
+                out, q, self.k_cache, self.v_cache, tables, lens,
+                self.case.query_start if query_start is None else query_start, self.case.scale,
+                self.max_ctx, self.max_q, workspace=self.ws, err_flag=self.flag, stream=self.stream)
+            return
         if self.prefix:
             self.pa.pa_decode_shared_prefix(out, q, self.k_cache, self.v_cache, tables, lens,
                                             self.case.scale, self.max_ctx, self.group_start,
@@ -315,7 +335,11 @@ def run_ours(args, rank, world, device) -> dict | None:
         return None
 
     peaks = measured_peaks()
-    if step.prefix:
+    flops = workloads.multi_token_flops(case) if step.multi else 0
+    if step.multi:
+        kernel_name = "pa_multi_token_attention call (attention + partition merge)"
+        achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
+    elif step.prefix:
         # the grouped path must move each shared block once: the unique bytes are its
         # algorithmic bytes (the per-sequence count stays in bytes_per_step)
         achieved = nbytes["decode_unique"] / (dec_mean_ms * 1e-3) / 1e9
@@ -350,6 +374,21 @@ def run_ours(args, rank, world, device) -> dict | None:
         "clocks": clocks,
         "kernel_source": src_hash,
     }
+    if step.multi:
+        tflops = flops / (dec_mean_ms * 1e-3) / 1e12
+        res["config"]["new_tokens_per_seq"] = step.max_q
+        res["config"]["query_rows"] = int(case.q.shape[0])
+        res["flops_per_step"] = flops
+        res["tflops"] = round(tflops, 1)
+        # bound: whichever of the two rooflines the step is closer to
+        tpeak = peaks["bf16_tflops"]
+        if tflops / tpeak > achieved / peaks["hbm_gbs"]:
+            res["roofline"].update({"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
+                                    "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
+                                    "peak_source": peaks["source"] + " (cuBLAS bf16 burst)",
+                                    "hbm_gbs": round(achieved, 1)})
+        else:
+            res["roofline"]["tflops"] = round(tflops, 1)
     if step.prefix:
         res["config"]["decode_path"] = "shared-prefix (one group of all sequences)"
         res["roofline"]["achieved_per_sequence_bytes"] = round(
@@ -366,8 +405,10 @@ def run_e2e(args, step, case, device, stream, world) -> dict:
     """Same step through the public API with the step's inputs in pinned host memory:
     host->device copies of queries, new K/V, slots, tables and lengths, and the
     device->host copy of the output, all inside the timed region."""
-    host = {k: getattr(case, k).cpu().pin_memory() for k in
-            ("q", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens")}
+    keys = ["q", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens"]
+    if step.multi:
+        keys.append("query_start")
+    host = {k: getattr(case, k).cpu().pin_memory() for k in keys}
     dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
     out_host = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -378,7 +419,8 @@ def run_e2e(args, step, case, device, stream, world) -> dict:
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
         step.write_cache(dev["new_key"], dev["new_value"], dev["slot_mapping"])
-        step.decode(dev["q"], dev["block_tables"], dev["context_lens"], step.out)
+        step.decode(dev["q"], dev["block_tables"], dev["context_lens"], step.out,
+                    query_start=dev.get("query_start"))
         out_host.copy_(step.out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -419,21 +461,49 @@ def oracle_sample_inputs(case, step=None):
     return bits(case.q), bits(case.k_pool), bits(case.v_pool), None, None
 
 
-def time_oracle(case, inputs, budget_s: float) -> dict:
-    """Oracle decode over the first n sequences, n grown until the run takes ~budget_s."""
+def first_sequences(case, n):
+    """The case cut to its first n sequences (for byte accounting of a sample)."""
+    sub = workloads.PagedCase(**{**case.__dict__})
+    sub.S = n
+    sub.context_lens = case.context_lens[:n].cpu()
+    sub.block_tables = case.block_tables[:n].cpu()
+    if case.query_start is not None:
+        qs = case.query_start.cpu()
+        sub.query_start = qs[: n + 1]
+        sub.q = case.q[: int(qs[n])]
+    else:
+        sub.q = case.q[:n]
+    return sub
+
+
+def oracle_runner(orc, case, inputs):
+    """A call of the oracle over the first n sequences of the case."""
     import numpy as np
 
-    import oracle
-
-    orc = oracle.load()
     q, kc, vc, ks, vs = inputs
     tables = case.block_tables.cpu().numpy()
     lens = case.context_lens.cpu().numpy()
+    if case.query_start is None:
+        return lambda n: orc.paged_attention(
+            np.ascontiguousarray(q[:n]), kc, vc, np.ascontiguousarray(tables[:n]),
+            np.ascontiguousarray(lens[:n]), case.scale, k_scale=ks, v_scale=vs)
+    qs = case.query_start.cpu().numpy()
+    return lambda n: orc.paged_prefill(
+        np.ascontiguousarray(q[: qs[n]]), kc, vc, np.ascontiguousarray(tables[:n]),
+        np.ascontiguousarray(lens[:n]), np.ascontiguousarray(qs[: n + 1]), case.scale,
+        k_scale=ks, v_scale=vs)
+
+
+def time_oracle(case, inputs, budget_s: float) -> dict:
+    """Oracle decode over the first n sequences, n grown until the run takes ~budget_s."""
+    import oracle
+
+    orc = oracle.load()
     n, elapsed = 1, 0.0
+    run = oracle_runner(orc, case, inputs)
     while True:
         t0 = time.perf_counter()
-        orc.paged_attention(np.ascontiguousarray(q[:n]), kc, vc, np.ascontiguousarray(tables[:n]),
-                            np.ascontiguousarray(lens[:n]), case.scale, k_scale=ks, v_scale=vs)
+        run(n)
         elapsed = time.perf_counter() - t0
         if elapsed >= budget_s / 4 or n >= case.S:
             break
@@ -442,20 +512,16 @@ def time_oracle(case, inputs, budget_s: float) -> dict:
     reps, total = 1, elapsed
     while total < budget_s:
         t0 = time.perf_counter()
-        orc.paged_attention(np.ascontiguousarray(q[:n]), kc, vc, np.ascontiguousarray(tables[:n]),
-                            np.ascontiguousarray(lens[:n]), case.scale, k_scale=ks, v_scale=vs)
+        run(n)
         total += time.perf_counter() - t0
         reps += 1
     elapsed = total / reps
-    sub = workloads.PagedCase(**{**case.__dict__})
-    sub.S = n
-    sub.context_lens = case.context_lens[:n].cpu()
-    sub.q = case.q[:n]
-    sub.block_tables = case.block_tables[:n].cpu()
+    sub = first_sequences(case, n)
     nbytes = workloads.decode_algorithmic_bytes(sub)
+    what = "multi-token attention" if case.query_start is not None else "decode"
     return {"value": round(nbytes / elapsed / 1e9, 4), "unit": UNIT, "cores": orc.num_threads,
-            "kind": "oracle", "seconds": round(elapsed, 3), "repeats": reps,
-            "sample": f"decode of the first {n} of {case.S} sequences "
+            "kind": "oracle", "seconds": round(elapsed, 3), "repeats": reps, "sequences": n,
+            "sample": f"{what} of the first {n} of {case.S} sequences "
                       f"({int(sub.context_lens.sum())} context tokens), fp64 C oracle, "
                       f"caches resident in host memory"}
 
@@ -470,8 +536,6 @@ def run_reference(args, rank, world) -> dict | None:
 
     The sample (the first n sequences) is sized once so that W + K steps take about
     two minutes in all, at most 3 s a step."""
-    import numpy as np
-
     import oracle
 
     if rank != 0:
@@ -480,19 +544,14 @@ def run_reference(args, rank, world) -> dict | None:
     inputs = oracle_sample_inputs(case)
     per_step = min(3.0, 120.0 / (args.warmup + args.steps))
     info = time_oracle(case, inputs, budget_s=4 * per_step)  # calibrates n
-    n = int(info["sample"].split()[4])
+    n = info["sequences"]
     orc = oracle.load()
-    q, kc, vc, ks, vs = inputs
-    qn = np.ascontiguousarray(q[:n])
-    tables = np.ascontiguousarray(case.block_tables[:n].numpy())
-    lens = np.ascontiguousarray(case.context_lens[:n].numpy())
-    sub = workloads.PagedCase(**{**case.__dict__})
-    sub.S, sub.q, sub.block_tables, sub.context_lens = n, case.q[:n], case.block_tables[:n], case.context_lens[:n]
-    nbytes = workloads.decode_algorithmic_bytes(sub)
+    run = oracle_runner(orc, case, inputs)
+    nbytes = workloads.decode_algorithmic_bytes(first_sequences(case, n))
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        orc.paged_attention(qn, kc, vc, tables, lens, case.scale, k_scale=ks, v_scale=vs)
+        run(n)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     ms_per_step = 1e3 * sum(times) / len(times)

@@ -66,9 +66,13 @@ enum {
     PA_FLAG_BLOCK_OUT_OF_RANGE = 2,   /* block_tables entry outside [0, N): block skipped */
     PA_FLAG_CONTEXT_OUT_OF_RANGE = 4, /* context_lens[s] < 0, > M * bs or > max_context_len:
                                          clamped to the valid range                        */
-    PA_FLAG_PREFIX_MISMATCH = 8       /* pa_decode_shared_prefix: a group or member did not
+    PA_FLAG_PREFIX_MISMATCH = 8,      /* pa_decode_shared_prefix: a group or member did not
                                          meet the prefix preconditions and was decoded on
                                          its own (the result is still correct)            */
+    PA_FLAG_QUERY_OUT_OF_RANGE = 16   /* pa_multi_token_attention: query offsets of a
+                                         sequence outside [0, T], decreasing, longer than
+                                         its context or than max_query_len: its rows are
+                                         not written                                      */
 };
 
 /* Version of this ABI (bumped on any signature change). */
@@ -227,6 +231,43 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
                                   int n_groups, int max_group_size, int max_prefix_len,
                                   void *workspace, size_t workspace_bytes, int *err_flag,
                                   void *stream);
+
+/*
+ * Multi-token paged attention: several new tokens per sequence attend the paged
+ * cache in one call -- a chunk of a long prompt (chunked prefill) or the draft
+ * tokens a large model verifies in one pass (speculative decoding): deeplearn.tn,
+ * "Les leviers d'optimisation en production"; the gaiatechstar.com discussion, reply
+ * on chunked prefill.  The new tokens' K and V must already be in the cache
+ * (pa_reshape_and_cache with one slot per new token).
+ *   query           [T][Hq][D] bf16, device: sequence s owns rows
+ *                   query_start[s] .. query_start[s + 1] - 1, its L_s newest tokens in
+ *                   order (varlen packing; rows of no sequence are not written).
+ *   query_start     [S + 1] int32, device.
+ *   context_lens    [S] int32, device: tokens in the cache including the L_s new ones.
+ *   out             [T][Hq][D] bf16, device.
+ *   New token i of sequence s sits at position p = context_lens[s] - L_s + i and
+ *   attends positions 0 .. p (causal inside the chunk; L_s = 1 is pa_decode):
+ *     out[row][h] = sum_{t <= p} softmax_t(scale * q[row][h] . k_t) v_t,
+ *   k_t, v_t read through block_tables[s] from kv head h / (Hq / Hkv).
+ *   max_query_len   host bound of every L_s (sizes the grid and the workspace); a
+ *                   sequence with a larger L_s, offsets outside [0, T], a negative L_s or
+ *                   L_s > context_lens[s] is skipped with PA_FLAG_QUERY_OUT_OF_RANGE.
+ *   workspace       pa_multi_token_workspace_size(...) bytes (NULL when that is 0);
+ *                   contents not preserved.
+ * bf16 caches only (PA_ERR_UNSUPPORTED otherwise); other arguments as pa_decode.
+ */
+size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                     int max_context_len, int max_query_len);
+
+pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
+                                   const void *v_cache, const float *k_scale,
+                                   const float *v_scale, int kv_dtype,
+                                   const int32_t *block_tables, int M,
+                                   const int32_t *context_lens, const int32_t *query_start,
+                                   int S, int T, int Hq, int Hkv, int D, int bs, int N,
+                                   float scale, int max_context_len, int max_query_len,
+                                   void *workspace, size_t workspace_bytes, int *err_flag,
+                                   void *stream);
 
 /*
  * Paged decode without any allocation: the same computation, arguments and

@@ -27,10 +27,12 @@ PA_FLAG_SLOT_OUT_OF_RANGE = 1
 PA_FLAG_BLOCK_OUT_OF_RANGE = 2
 PA_FLAG_CONTEXT_OUT_OF_RANGE = 4
 PA_FLAG_PREFIX_MISMATCH = 8
+PA_FLAG_QUERY_OUT_OF_RANGE = 16
 
 EXPORTED = ["pa_version", "pa_status_string", "pa_last_error_string", "pa_reshape_and_cache",
             "pa_quantize_kv", "pa_quantize_kv_fp8", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",
-            "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix"]
+            "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix",
+            "pa_multi_token_workspace_size", "pa_multi_token_attention"]
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -81,6 +83,12 @@ def load_library(path: Path | str | None = None) -> ctypes.CDLL:
                                             i32, i32, i32, f32, i32, vp, vp, i32, i32, i32, vp, sz,
                                             vp, vp]
     lib.pa_decode_shared_prefix.restype = i32
+    lib.pa_multi_token_workspace_size.argtypes = [i32] * 9
+    lib.pa_multi_token_workspace_size.restype = sz
+    lib.pa_multi_token_attention.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32,
+                                             i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, sz,
+                                             vp, vp]
+    lib.pa_multi_token_attention.restype = i32
     if path is None:
         _LIB = lib
     return lib
@@ -346,6 +354,50 @@ def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_
         int(max_context_len), _ptr(group_start), _ptr(group_prefix_len), n_groups,
         int(max_group_size), int(max_prefix_len), _ptr(workspace), ws_bytes, _flag(err_flag),
         _stream(stream, query.device)))
+
+
+def pa_multi_token_workspace_size(S: int, T: int, Hq: int, Hkv: int, D: int, bs: int,
+                                  kv_dtype: int, max_context_len: int, max_query_len: int) -> int:
+    return int(load_library().pa_multi_token_workspace_size(
+        S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len))
+
+
+def pa_multi_token_attention(out, query, k_cache, v_cache, block_tables, context_lens,
+                             query_start, scale: float, max_context_len: int,
+                             max_query_len: int, workspace=None, err_flag=None,
+                             stream=None) -> None:
+    """Several new tokens per sequence attend the paged cache, each up to its own
+    position: query/out [T][Hq][D] bf16, sequence s owning rows
+    query_start[s] .. query_start[s+1]-1.  workspace defaults to a fresh allocation."""
+    _cuda(out, "out", torch.bfloat16, 3)
+    _cuda(query, "query", torch.bfloat16, 3)
+    kv_dtype = kv_dtype_of(k_cache)
+    _cuda(k_cache, "k_cache", k_cache.dtype, 4)
+    _cuda(v_cache, "v_cache", k_cache.dtype, 4)
+    _cuda(block_tables, "block_tables", torch.int32, 2)
+    _cuda(context_lens, "context_lens", torch.int32, 1)
+    _cuda(query_start, "query_start", torch.int32, 1)
+    T, Hq, D = query.shape
+    N, Hkv, bs, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    M = block_tables.shape[1]
+    if out.shape != query.shape or v_cache.shape != k_cache.shape or D2 != D \
+            or block_tables.shape[0] != S or query_start.shape[0] != S + 1:
+        raise ValueError("pa_multi_token_attention: shape mismatch")
+    if workspace is None:
+        n = pa_multi_token_workspace_size(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len,
+                                          max_query_len)
+        workspace = torch.empty(n, dtype=torch.uint8, device=query.device) if n else None
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda(workspace, "workspace", workspace.dtype)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    lib = load_library()
+    _check(lib.pa_multi_token_attention(
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), None, None, kv_dtype,
+        _ptr(block_tables), M, _ptr(context_lens), _ptr(query_start), S, T, Hq, Hkv, D, bs, N,
+        float(scale), int(max_context_len), int(max_query_len), _ptr(workspace), ws_bytes,
+        _flag(err_flag), _stream(stream, query.device)))
 
 
 def decode_workspace(query, k_cache, max_context_len: int) -> torch.Tensor | None:

@@ -469,4 +469,131 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
     return check_launch(fn);
 }
 
+// Multi-token attention plan: CTAs of 128 (token, head) columns per kv head; the
+// context is split into partitions (multiples of 64 tokens, at most 4096) when the
+// columns alone do not fill 4 waves of 2 CTAs per SM.
+struct MultiPlan {
+    int CB, part_tokens, max_parts;
+    size_t acc_off, ml_off, bytes;
+};
+
+static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int max_context_len, int max_query_len) {
+    MultiPlan p{};
+    const int G = Hq / Hkv;
+    p.CB = std::max(1, (int)(((int64_t)max_query_len * G + multi_cols_per_cta() - 1) / multi_cols_per_cta()));
+    const int64_t units = (int64_t)S * Hkv * p.CB;
+    const double slots = (double)device_sms() * 2;
+    const int ctx = std::max(max_context_len, 1);
+    p.part_tokens = 256;
+    if ((double)units >= 4.0 * slots && ctx <= 4096) {
+        p.part_tokens = (int)align_up((size_t)ctx, 64);
+    } else {
+        double best = -1.0;
+        for (int cand : {4096, 2048, 1024, 512, 256}) {
+            const int64_t parts = (ctx + cand - 1) / cand;
+            const double waves = (double)(units * parts) / slots;
+            if (waves < 2.0 && cand != 256) continue;
+            const double fill = waves / std::ceil(waves);
+            const double len = (double)std::min(cand, ctx);
+            const double score = fill * len / (len + 64.0);
+            if (score > best + 1e-9) {
+                best = score;
+                p.part_tokens = cand;
+            }
+        }
+    }
+    p.max_parts = (ctx + p.part_tokens - 1) / p.part_tokens;
+    if (p.max_parts == 1) return p;
+    const size_t rows = (size_t)T * Hq * p.max_parts;
+    p.acc_off = 0;
+    p.ml_off = align_up(rows * D * sizeof(float), 256);
+    p.bytes = align_up(p.ml_off + rows * 2 * sizeof(float), 256);
+    return p;
+}
+
+static pa_status check_multi_args(const char *fn, int S, int T, int Hq, int Hkv, int D, int bs,
+                                  int kv_dtype, int max_context_len, int max_query_len) {
+    pa_status st = check_decode_shape(fn, S, Hq, Hkv, D, bs, kv_dtype, max_context_len);
+    if (st != PA_OK) return st;
+    if (kv_dtype != PA_KV_BF16)
+        return fail(PA_ERR_UNSUPPORTED, "%s: only bf16 caches are supported", fn);
+    if (T < 0) return fail(PA_ERR_INVALID_ARG, "%s: T = %d", fn, T);
+    if (max_query_len < 1 || max_query_len > max_context_len || max_query_len > T)
+        return fail(PA_ERR_INVALID_ARG, "%s: max_query_len = %d (1 .. min(T, max_context_len))", fn,
+                    max_query_len);
+    const int64_t cb = ((int64_t)max_query_len * (Hq / Hkv) + multi_cols_per_cta() - 1) / multi_cols_per_cta();
+    if ((int64_t)Hkv * cb > 65535 || ((int64_t)max_query_len * Hq + 3) / 4 > 0x7fffffffLL)
+        return fail(PA_ERR_UNSUPPORTED, "%s: too many new tokens per sequence", fn);
+    return PA_OK;
+}
+
+size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                     int max_context_len, int max_query_len) {
+    if (check_multi_args("pa_multi_token_workspace_size", S, T, Hq, Hkv, D, bs, kv_dtype,
+                         max_context_len, max_query_len) != PA_OK)
+        return 0;
+    return plan_multi(S, T, Hq, Hkv, D, max_context_len, max_query_len).bytes;
+}
+
+pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
+                                   const void *v_cache, const float *k_scale,
+                                   const float *v_scale, int kv_dtype,
+                                   const int32_t *block_tables, int M,
+                                   const int32_t *context_lens, const int32_t *query_start,
+                                   int S, int T, int Hq, int Hkv, int D, int bs, int N,
+                                   float scale, int max_context_len, int max_query_len,
+                                   void *workspace, size_t workspace_bytes, int *err_flag,
+                                   void *stream) {
+    const char *fn = "pa_multi_token_attention";
+    g_last_error[0] = 0;
+    (void)k_scale;
+    (void)v_scale;
+    if (S == 0 || T == 0) return PA_OK;
+    pa_status st = check_multi_args(fn, S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len);
+    if (st != PA_OK) return st;
+    if (N <= 0 || M <= 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: N = %d, M = %d must be positive", fn, N, M);
+    if ((int64_t)max_context_len > (int64_t)M * bs)
+        return fail(PA_ERR_OUT_OF_RANGE, "%s: max_context_len %d exceeds M * bs = %lld", fn,
+                    max_context_len, (long long)M * bs);
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+        return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
+    if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
+        return fail(PA_ERR_INVALID_ARG, "%s: scale must be finite", fn);
+    const MultiPlan plan = plan_multi(S, T, Hq, Hkv, D, max_context_len, max_query_len);
+    if (plan.bytes && (!workspace || workspace_bytes < plan.bytes))
+        return fail(PA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, plan.bytes,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (plan.bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(PA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
+    MultiArgs a{};
+    a.out = out;
+    a.q = query;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start = query_start;
+    a.ws_acc = plan.bytes ? (float *)((char *)workspace + plan.acc_off) : nullptr;
+    a.ws_ml = plan.bytes ? (float *)((char *)workspace + plan.ml_off) : nullptr;
+    a.err_flag = err_flag;
+    a.M = M;
+    a.S = S;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.N = N;
+    a.CB = plan.CB;
+    a.part_tokens = plan.part_tokens;
+    a.max_parts = plan.max_parts;
+    a.max_context_len = max_context_len;
+    a.max_query_len = max_query_len;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    launch_multi_token(a, D, bs, (cudaStream_t)stream);
+    return check_launch(fn);
+}
+
 }  // extern "C"

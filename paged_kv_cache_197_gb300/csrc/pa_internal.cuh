@@ -69,6 +69,25 @@ int prefix_cols_per_cta();
 cudaError_t launch_decode_shared_prefix(const DecodeArgs &a, const PrefixArgs &p, int D, int bs,
                                         cudaStream_t stream);
 
+// Multi-token attention: the newest L_s tokens of each sequence attend the cache.
+struct MultiArgs {
+    uint16_t *out;                 // [T][Hq][D] bf16
+    const uint16_t *q;             // [T][Hq][D] bf16
+    const void *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    const int32_t *query_start;    // [S + 1]: rows of sequence s
+    float *ws_acc, *ws_ml;         // [T][Hq][max_parts][D], [T][Hq][max_parts][2]
+    int *err_flag;
+    int M, S, T, Hq, Hkv, G, N;
+    int CB;                        // blocks of 128 (token, head) columns per kv head
+    int part_tokens, max_parts;    // context partitions (multiple of 64 tokens)
+    int max_context_len, max_query_len;
+    float scale_log2;
+};
+
+int multi_cols_per_cta();
+cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, cudaStream_t stream);
+
 // ------------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing was launched).
 cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *k_cache,

@@ -1,0 +1,453 @@
+// Multi-token paged attention: several new tokens of a sequence attend the paged
+// cache in one pass -- a chunk of a long prompt (chunked prefill) or the draft tokens
+// a large model verifies at once (speculative decoding); deeplearn.tn, "Les leviers
+// d'optimisation en production", and the gaiatechstar.com discussion's reply on
+// chunked prefill.  New token i of sequence s sits at position ctx - L + i and
+// attends every cached token up to and including its own position (causal inside
+// the chunk); with L = 1 this is the decode step.
+//
+// Work unit ("column"): one (new token, query head) pair.  The columns of a sequence
+// and kv head share that kv head's K and V, so a CTA takes up to 128 of them and
+// streams the sequence's K and V once for all: 64-token chunks staged in shared
+// memory by cp.async, double-buffered.  A warp multiplies 16-token tiles against 16
+// query columns on the tensor cores (S = K q^T, then O^T += V^T P^T), with an online
+// softmax in the exp2 domain and each column masked at its own position.  Warps are
+// (column group, token slice) pairs: with few columns (draft tokens) up to four
+// warps split the tiles of one group, and the slices are joined by log-sum-exp in
+// shared memory before the column is written.
+// Long contexts are split into partitions (grid x); a column whose visible tokens
+// span one partition is finished in place, the others leave (max, sum, output)
+// partials that a second kernel joins by log-sum-exp.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pa_internal.cuh"
+#include "pa_mma.cuh"
+
+namespace pa {
+namespace {
+
+using namespace tiled;
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kColsPerWarp = 16;                   // two mma n-tiles of 8 columns
+constexpr int kColsPerCta = kWarps * kColsPerWarp;  // 128
+constexpr int kChunk = 64;                         // tokens per shared-memory stage
+constexpr int kMaxPartBlocks = 4096 / 16;          // block ids of one partition
+
+__device__ __forceinline__ void raise_flag(int *err_flag, int bit) {
+    if (err_flag) atomicOr(err_flag, bit);
+}
+
+// The sequence's context, new-token count and first query row, checked: a context
+// outside [0, min(M * bs, max_context_len)] is clamped (CONTEXT flag); query offsets
+// outside [0, T], a negative count, more new tokens than context or than
+// max_query_len leave the sequence out (QUERY flag, its rows are not written).
+struct SeqView {
+    int ctx, L, row0, base;
+    bool ok;
+};
+
+template <int BS>
+__device__ __forceinline__ SeqView seq_view(const MultiArgs &a, int s, bool report) {
+    SeqView v;
+    int ctx = a.context_lens[s];
+    const int lim = min(a.M * BS, a.max_context_len);
+    if (ctx < 0 || ctx > lim) {
+        if (report) raise_flag(a.err_flag, PA_FLAG_CONTEXT_OUT_OF_RANGE);
+        ctx = ctx < 0 ? 0 : lim;
+    }
+    const int r0 = a.query_start[s], r1 = a.query_start[s + 1];
+    v.ctx = ctx;
+    v.row0 = r0;
+    v.L = r1 - r0;
+    v.ok = r0 >= 0 && r1 <= a.T && v.L >= 0 && v.L <= ctx && v.L <= a.max_query_len;
+    if (!v.ok && report) raise_flag(a.err_flag, PA_FLAG_QUERY_OUT_OF_RANGE);
+    v.base = ctx - v.L;
+    return v;
+}
+
+template <int D>
+__host__ __device__ constexpr int multi_smem_bytes() {
+    return (4 * kChunk * (2 * D + 16)) > (kWarps * kColsPerWarp * (D + 4) * 4)
+               ? (4 * kChunk * (2 * D + 16))
+               : (kWarps * kColsPerWarp * (D + 4) * 4);
+}
+
+template <int D, int BS>
+__global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_constant__ MultiArgs a) {
+    constexpr int ROW = D * 2;         // bytes of one token row (bf16)
+    constexpr int RS = ROW + 16;       // padded shared-memory row stride
+    constexpr int STAGE = kChunk * RS;  // one K (or V) stage
+    constexpr int CPR = ROW / 16;      // 16-byte pieces per row
+    constexpr int KC = D / 16;         // k-steps of the score product
+    constexpr int MT = D / 16;         // d tiles of the output product
+    constexpr int PER = D / 32;        // output values per lane in the epilogue
+    extern __shared__ __align__(128) unsigned char smem[];  // K0 K1 V0 V1, then the epilogue
+    __shared__ int s_blk[kMaxPartBlocks];
+    __shared__ float s_ml[kWarps][kColsPerWarp][2];  // each warp's (max, sum) per column
+
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
+    const int s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t = lane & 3;
+
+    const SeqView v = seq_view<BS>(a, s, part == 0 && blockIdx.y == 0 && tid == 0);
+    if (!v.ok) return;
+    const int ncols = v.L * a.G;
+    const int col0 = cb * kColsPerCta;
+    if (col0 >= ncols) return;
+    // the CTA's last column sees the most tokens
+    const int cta_lim = v.base + (min(ncols, col0 + kColsPerCta) - 1) / a.G;  // inclusive
+    const int tok_begin = part * a.part_tokens;
+    const int tok_end = min(tok_begin + a.part_tokens, cta_lim + 1);
+    if (tok_begin >= tok_end) return;
+    const int blk0 = tok_begin / BS;  // partitions start on a block boundary
+    const int nblk = (tok_end - tok_begin + BS - 1) / BS;
+    for (int i = tid; i < nblk; i += kThreads) {
+        int b = a.block_tables[(int64_t)s * a.M + blk0 + i];
+        if (b < 0 || b >= a.N) {
+            if (cb == 0) raise_flag(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
+            b = -1;  // read as zeros
+        }
+        s_blk[i] = b;
+    }
+
+    // warps = (column group of 16, token slice): with few columns (draft tokens) the
+    // idle warps take other tiles of the same columns, and the slices are joined at
+    // the end; with 5..8 groups every warp owns a group and sees every tile
+    const int ncg = (min(ncols - col0, kColsPerCta) + kColsPerWarp - 1) / kColsPerWarp;
+    const int P2 = ncg <= 1 ? 1 : ncg <= 2 ? 2 : ncg <= 4 ? 4 : 8;
+    const int slices = min(4, kWarps / P2);  // 4 tiles per chunk
+    const int cg = warp % P2, slice = warp / P2;
+    const bool active = cg < ncg && slice < slices;
+    // this warp's 16 columns: q as mma B fragments, and each column's last visible
+    // position (-1: no such column)
+    const int wcol0 = active ? col0 + cg * kColsPerWarp : ncols;
+    uint32_t qf[2][KC][2];
+    int lim[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int c = wcol0 + nt * 8 + gq;
+        if (c < ncols) {
+            const int64_t row = v.row0 + c / a.G;
+            const uint16_t *qrow = a.q + (row * a.Hq + kvh * a.G + c % a.G) * D;
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc) {
+                qf[nt][kc][0] = __ldg(reinterpret_cast<const uint32_t *>(qrow + kc * 16 + 2 * t));
+                qf[nt][kc][1] = __ldg(reinterpret_cast<const uint32_t *>(qrow + kc * 16 + 8 + 2 * t));
+            }
+        } else {
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc) qf[nt][kc][0] = qf[nt][kc][1] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int cj = wcol0 + nt * 8 + 2 * t + j;
+            // clamped to the partition: tokens past it are masked with the rest
+            lim[nt][j] = cj < ncols ? min(v.base + cj / a.G, tok_end - 1) : -1;
+        }
+    }
+    const int warp_lim = wcol0 < ncols ? min(v.base + (min(ncols, wcol0 + kColsPerWarp) - 1) / a.G, tok_end - 1) : -1;
+
+    float o[2][MT][4];
+    float m[2][2], l[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+    }
+    __syncthreads();  // s_blk
+
+    unsigned char *ks = smem, *vs = smem + 2 * STAGE;
+    // staging: thread tid always copies 16-byte piece pc of rows pr, pr + RPP, ... of a
+    // chunk, for K and for V; a (block, kv head) is BS contiguous rows in the cache
+    constexpr int RPP = kThreads / CPR;   // rows per pass: 16 (D = 128) or 32 (D = 64)
+    constexpr int PASSES = kChunk / RPP;
+    const int pc = tid % CPR, pr = tid / CPR;
+    const int64_t block_stride = (int64_t)a.Hkv * BS * ROW;
+    const char *kbase_g = static_cast<const char *>(a.k_cache) + (int64_t)kvh * BS * ROW + pc * 16;
+    const char *vbase_g = static_cast<const char *>(a.v_cache) + (int64_t)kvh * BS * ROW + pc * 16;
+    const uint32_t kdst0 = smem_u32(ks) + pr * RS + pc * 16, vdst0 = smem_u32(vs) + pr * RS + pc * 16;
+    auto stage_chunk = [&](int j, int buf) {
+        const int c0 = tok_begin + j * kChunk;
+#pragma unroll
+        for (int k = 0; k < PASSES; ++k) {
+            const int tok = c0 + pr + k * RPP;
+            const char *ksrc = kbase_g, *vsrc = vbase_g;
+            uint32_t bytes = 0;
+            if (tok < tok_end) {
+                const int b = s_blk[tok / BS - blk0];
+                if (b >= 0) {
+                    const int64_t off = b * block_stride + (tok % BS) * ROW;
+                    ksrc += off;
+                    vsrc += off;
+                    bytes = 16;
+                }
+            }
+            const uint32_t doff = buf * STAGE + k * RPP * RS;
+            cp_async16(kdst0 + doff, ksrc, bytes);
+            cp_async16(vdst0 + doff, vsrc, bytes);
+        }
+        cp_async_commit();
+    };
+
+    const int nchunks = (tok_end - tok_begin + kChunk - 1) / kChunk;
+    stage_chunk(0, 0);
+    for (int j = 0; j < nchunks; ++j) {
+        if (j + 1 < nchunks) {
+            stage_chunk(j + 1, (j + 1) & 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const int buf = j & 1;
+        const uint32_t kbase = smem_u32(ks + buf * STAGE), vbase = smem_u32(vs + buf * STAGE);
+        const int c0 = tok_begin + j * kChunk;
+#pragma unroll 1
+        for (int tt = slice; tt < kChunk / 16; tt += slices) {
+            const int tile0 = c0 + tt * 16;
+            if (tile0 > warp_lim) break;  // warp-uniform
+            float sc[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            {
+                const int row = tt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const uint32_t rb = kbase + row * RS + (lane >> 4) * 16;
+#pragma unroll
+                for (int kc = 0; kc < KC; ++kc) {
+                    uint32_t af[4];
+                    ldsm_x4(af, rb + kc * 32);
+                    mma16816(sc[0], af, qf[0][kc][0], qf[0][kc][1]);
+                    mma16816(sc[1], af, qf[1][kc][0], qf[1][kc][1]);
+                }
+            }
+            uint32_t pb[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float x[4], mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int tok = tile0 + gq + 8 * (c >> 1);
+                    x[c] = tok <= lim[nt][c & 1] ? sc[nt][c] * a.scale_log2 : -INFINITY;
+                    mx[c & 1] = fmaxf(mx[c & 1], x[c]);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    mx[jj] = fmaxf(mx[jj], __shfl_xor_sync(0xffffffffu, mx[jj], 4));
+                    mx[jj] = fmaxf(mx[jj], __shfl_xor_sync(0xffffffffu, mx[jj], 8));
+                    mx[jj] = fmaxf(mx[jj], __shfl_xor_sync(0xffffffffu, mx[jj], 16));
+                }
+                float base[2], alpha[2];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const float mnew = fmaxf(m[nt][jj], mx[jj]);
+                    base[jj] = mnew == -INFINITY ? 0.f : mnew;
+                    alpha[jj] = ex2(m[nt][jj] - base[jj]);
+                    m[nt][jj] = mnew;
+                    l[nt][jj] *= alpha[jj];
+                }
+                // the running maxima settle after a few tiles: rescale only when one moved
+                if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        o[nt][mt][0] *= alpha[0];
+                        o[nt][mt][1] *= alpha[1];
+                        o[nt][mt][2] *= alpha[0];
+                        o[nt][mt][3] *= alpha[1];
+                    }
+                }
+                float pr[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    pr[c] = ex2(x[c] - base[c & 1]);
+                    l[nt][c & 1] += pr[c];
+                }
+                pb[nt][0] = movmatrix_t(bf16x2(pr[0], pr[1]));
+                pb[nt][1] = movmatrix_t(bf16x2(pr[2], pr[3]));
+            }
+            {
+                const int row = tt * 16 + (lane & 7) + (lane >> 4) * 8;
+                const uint32_t rb = vbase + row * RS + ((lane >> 3) & 1) * 16;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    uint32_t af[4];
+                    ldsm_x4_trans(af, rb + mt * 32);
+                    mma16816(o[0][mt], af, pb[0][0], pb[0][1]);
+                    mma16816(o[1][mt], af, pb[1][0], pb[1][1]);
+                }
+            }
+        }
+        __syncthreads();  // this buffer is refilled two chunks later
+    }
+    // the merge grid may launch now (it still waits for this grid before reading)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // per-column sums over the tile rows held by the 8 lanes of each t
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            l[nt][jj] += __shfl_xor_sync(0xffffffffu, l[nt][jj], 4);
+            l[nt][jj] += __shfl_xor_sync(0xffffffffu, l[nt][jj], 8);
+            l[nt][jj] += __shfl_xor_sync(0xffffffffu, l[nt][jj], 16);
+        }
+
+    // every warp leaves its state in shared memory (the stages are free: every warp
+    // passed the loop's last barrier): O^T transposed to [column][d], (max, sum)
+    float *so = reinterpret_cast<float *>(smem) + warp * kColsPerWarp * (D + 4);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                so[(nt * 8 + 2 * t + (c & 1)) * (D + 4) + mt * 16 + gq + 8 * (c >> 1)] = o[nt][mt][c];
+    if (gq == 0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                s_ml[warp][nt * 8 + 2 * t + jj][0] = m[nt][jj];
+                s_ml[warp][nt * 8 + 2 * t + jj][1] = l[nt][jj];
+            }
+    }
+    __syncthreads();
+
+    // one warp per column (round robin): join the token slices, then finish the column
+    // (one partition) or leave a partial
+#pragma unroll 1
+    for (int cc = warp; cc < ncg * kColsPerWarp; cc += kWarps) {
+        const int c = col0 + cc;
+        if (c >= ncols) break;
+        const int i = c / a.G, h = kvh * a.G + c % a.G;
+        const int lim_c = v.base + i;
+        if (tok_begin > lim_c) continue;  // this partition holds nothing the column sees
+        const int g = cc / kColsPerWarp, cl = cc % kColsPerWarp;
+        float mv = -INFINITY;
+        for (int sl = 0; sl < slices; ++sl) mv = fmaxf(mv, s_ml[sl * P2 + g][cl][0]);
+        const float mb = mv == -INFINITY ? 0.f : mv;
+        float acc[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+        float lv = 0.f;
+        for (int sl = 0; sl < slices; ++sl) {
+            const int w = sl * P2 + g;
+            const float f = ex2(s_ml[w][cl][0] - mb);
+            lv += f * s_ml[w][cl][1];
+            const float *src = reinterpret_cast<const float *>(smem) + (w * kColsPerWarp + cl) * (D + 4) + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] += f * src[e];
+        }
+        const int64_t pair = (int64_t)(v.row0 + i) * a.Hq + h;
+        if (lim_c < a.part_tokens) {  // one partition: finish here
+            const float inv = lv > 0.f ? 1.f / lv : 0.f;
+            uint16_t *dst = a.out + pair * D + lane * PER;
+            if constexpr (PER == 4)
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(bf16x2(acc[0] * inv, acc[1] * inv), bf16x2(acc[2] * inv, acc[3] * inv));
+            else
+                *reinterpret_cast<uint32_t *>(dst) = bf16x2(acc[0] * inv, acc[1] * inv);
+        } else {
+            const int64_t prow = pair * a.max_parts + part;
+            float *dst = a.ws_acc + prow * D + lane * PER;
+            if constexpr (PER == 4)
+                *reinterpret_cast<float4 *>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            else
+                *reinterpret_cast<float2 *>(dst) = make_float2(acc[0], acc[1]);
+            if (lane == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(mv, lv);
+        }
+    }
+}
+
+// Log-sum-exp merge of a column's partitions: out = sum_p 2^(m_p - M) acc_p /
+// sum_p 2^(m_p - M) l_p, M = max_p m_p.  One warp per (new token, query head) of a
+// sequence (grid y); launched as a programmatic dependent of the attention kernel.
+template <int D, int BS>
+__global__ void __launch_bounds__(128) merge_multi_kernel(const __grid_constant__ MultiArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int PER = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.y;
+    const int jidx = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const SeqView v = seq_view<BS>(a, s, false);
+    if (!v.ok) return;
+    const int i = jidx / a.Hq, h = jidx % a.Hq;
+    if (i >= v.L) return;
+    const int nparts = (v.base + i) / a.part_tokens + 1;
+    if (nparts <= 1) return;  // finished by the attention kernel
+    const int64_t row0 = ((int64_t)(v.row0 + i) * a.Hq + h) * a.max_parts;
+    float mmax = -INFINITY;
+    for (int p = lane; p < nparts; p += 32) mmax = fmaxf(mmax, a.ws_ml[(row0 + p) * 2]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+    const float mbase = mmax == -INFINITY ? 0.f : mmax;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float lsum = 0.f;
+    for (int p0 = 0; p0 < nparts; p0 += 32) {
+        float f = 0.f;
+        if (p0 + lane < nparts) {
+            const float2 ml = *reinterpret_cast<const float2 *>(a.ws_ml + (row0 + p0 + lane) * 2);
+            f = ex2(ml.x - mbase);
+            lsum += f * ml.y;
+        }
+        const int cnt = min(32, nparts - p0);
+        for (int q = 0; q < cnt; ++q) {
+            const float fq = __shfl_sync(0xffffffffu, f, q);
+            const float *src = a.ws_acc + (row0 + p0 + q) * D + lane * PER;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] += fq * src[e];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    uint16_t *dst = a.out + ((int64_t)(v.row0 + i) * a.Hq + h) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t *>(dst + e) = bf16x2(acc[e] * inv, acc[e + 1] * inv);
+}
+
+template <int D, int BS>
+cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
+    constexpr int SMEM = multi_smem_bytes<D>();
+    static bool configured[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(paged_multi_kernel<D, BS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
+    paged_multi_kernel<D, BS><<<grid, kThreads, SMEM, stream>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || a.max_parts == 1) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.max_query_len * a.Hq + 3) / 4), a.S);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_multi_kernel<D, BS>, a);
+}
+
+}  // namespace
+
+int multi_cols_per_cta() { return kColsPerCta; }
+
+cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, cudaStream_t stream) {
+    if (D == 128)
+        return bs == 16 ? launch_multi_typed<128, 16>(a, stream) : launch_multi_typed<128, 32>(a, stream);
+    return bs == 16 ? launch_multi_typed<64, 16>(a, stream) : launch_multi_typed<64, 32>(a, stream);
+}
+
+}  // namespace pa

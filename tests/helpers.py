@@ -129,3 +129,36 @@ def compare(got: torch.Tensor, ref: np.ndarray, kv_dtype: str):
     assert err.max() <= max_abs, f"max abs error {err.max():.3e} > {max_abs}"
     assert err.mean() <= mean_abs, f"mean abs error {err.mean():.3e} > {mean_abs}"
     return float(err.max()), float(err.mean())
+
+
+def gpu_multi_step(case: workloads.PagedCase, device, max_query_len=None, max_context_len=None):
+    """Append every new token, then multi-token attention, on the GPU.  Output rows of
+    no sequence stay NaN.  Returns dict(out, k_cache, v_cache, flag)."""
+    import paged_kv_cache_197_gb300 as pa
+
+    c = case.to(device)
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+    k_cache, v_cache = c.k_pool.clone(), c.v_pool.clone()
+    pa.pa_reshape_and_cache(c.new_key, c.new_value, k_cache, v_cache, c.slot_mapping, err_flag=flag)
+    if max_context_len is None:
+        max_context_len = int(case.context_lens.max())
+    if max_query_len is None:
+        max_query_len = max(1, max(case.meta["query_lens"]))
+    out = torch.full_like(c.q, float("nan"))
+    pa.pa_multi_token_attention(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens,
+                                c.query_start, case.scale, max_context_len, max_query_len,
+                                err_flag=flag)
+    torch.cuda.synchronize(device)
+    return dict(out=out, k_cache=k_cache, v_cache=v_cache, flag=int(flag.item()))
+
+
+def oracle_multi_out(case, orc, caches) -> np.ndarray:
+    kc, vc, ks, vs = caches
+    return orc.paged_prefill(bits(case.q), kc, vc, case.block_tables.cpu().numpy(),
+                             case.context_lens.cpu().numpy(), case.query_start.cpu().numpy(),
+                             case.scale, k_scale=ks, v_scale=vs)
+
+
+def covered_rows(case) -> np.ndarray:
+    qs = case.query_start.cpu().numpy()
+    return np.concatenate([np.arange(qs[s], qs[s + 1]) for s in range(len(qs) - 1)] + [np.zeros(0, int)])

@@ -168,6 +168,64 @@ def test_shared_prefix_workspace_and_checks(lib):
     assert call(S=0) == pa.PA_OK
 
 
+def test_multi_token_workspace_and_checks(lib):
+    """Multi-token attention: 128 (token, head) columns per CTA; no partition when the
+    columns give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the
+    best of (last-wave fill) x (len / (len + 64)) over 4096..256-token partitions with
+    >= 2 waves (256 as the fallback).  The workspace holds (D + 2) fp32 per query row,
+    head and partition."""
+    import math
+
+    import paged_kv_cache_197_gb300 as pa
+
+    def plan(S, Hq, Hkv, max_ctx, max_q, slots=304):
+        cb = max(1, -(-max_q * (Hq // Hkv) // 128))
+        units = S * Hkv * cb
+        ctx = max(max_ctx, 1)
+        if units >= 4 * slots and ctx <= 4096:
+            return -(-ctx // 64) * 64
+        best, best_p = -1.0, 256
+        for cand in (4096, 2048, 1024, 512, 256):
+            parts = -(-ctx // cand)
+            waves = units * parts / slots
+            if waves < 2 and cand != 256:
+                continue
+            ln = min(cand, ctx)
+            score = waves / math.ceil(waves) * ln / (ln + 64)
+            if score > best + 1e-9:
+                best, best_p = score, cand
+        return best_p
+
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for S, T, Hq, Hkv, D, max_ctx, max_q in [(20, 80, 64, 8, 128, 8000, 4), (4, 2048, 32, 8, 128, 4096, 512),
+                                             (7, 40, 16, 2, 64, 2100, 8), (600, 600, 32, 32, 128, 1000, 1)]:
+        pt = plan(S, Hq, Hkv, max_ctx, max_q)
+        parts = -(-max_ctx // pt)
+        rows = T * Hq * parts
+        expect = 0 if parts == 1 else up(up(rows * D * 4) + rows * 2 * 4)
+        got = pa.pa_multi_token_workspace_size(S, T, Hq, Hkv, D, 16, pa.PA_KV_BF16, max_ctx, max_q)
+        assert got == expect, (S, T, got, expect)
+    ws = lambda **k: pa.pa_multi_token_workspace_size(  # noqa: E731
+        **{**dict(S=4, T=64, Hq=8, Hkv=2, D=128, bs=16, kv_dtype=0, max_context_len=8000,
+                  max_query_len=16), **k})
+    assert ws() > 0
+    assert ws(kv_dtype=pa.PA_KV_INT8) == 0
+    assert ws(max_query_len=0) == 0
+    assert ws(max_query_len=65) == 0  # more than T rows
+    fake = 1 << 20
+
+    def call(S=2, T=8, kv=pa.PA_KV_BF16, max_q=4, qs=fake, ws=fake, ws_bytes=1 << 30, max_ctx=64):
+        return lib.pa_multi_token_attention(fake, fake, fake, fake, None, None, kv, fake, 4, fake, qs,
+                                            S, T, 8, 2, 128, 16, 4, 0.1, max_ctx, max_q, ws, ws_bytes,
+                                            None, None)
+
+    assert call(kv=pa.PA_KV_FP8) == pa.PA_ERR_UNSUPPORTED
+    assert call(qs=None) == pa.PA_ERR_INVALID_ARG
+    assert call(max_q=9) == pa.PA_ERR_INVALID_ARG       # above T
+    assert call(max_ctx=65) == pa.PA_ERR_OUT_OF_RANGE   # above M * bs
+    assert call(T=0) == pa.PA_OK and call(S=0) == pa.PA_OK
+
+
 def test_cache_host_checks(lib):
     import paged_kv_cache_197_gb300 as pa
 

@@ -1,0 +1,122 @@
+"""GPU parity of multi-token paged attention (chunked prefill / draft verification)
+against the CPU oracle: every new token of a sequence attends the cache up to its
+own position."""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import paged_kv_cache_197_gb300 as pa
+
+    pa.load_library()
+
+
+def _run(case, orc, expect_flag=0, **kw):
+    got = helpers.gpu_multi_step(case, DEV, **kw)
+    caches = helpers.oracle_caches(case, orc)
+    assert np.array_equal(helpers.bits(got["k_cache"]), caches[0])
+    assert np.array_equal(helpers.bits(got["v_cache"]), caches[1])
+    assert got["flag"] == expect_flag
+    ref = helpers.oracle_multi_out(case, orc, caches)
+    rows = helpers.covered_rows(case)
+    other = np.setdiff1d(np.arange(case.q.shape[0]), rows)
+    if other.size:  # rows of no sequence are not written
+        assert torch.isnan(got["out"][torch.as_tensor(other, device=DEV)].float()).all()
+    idx = torch.as_tensor(rows, device=DEV)
+    return helpers.compare(got["out"][idx], ref[rows], "bf16")
+
+
+@pytest.mark.parametrize("D,bs,Hq,Hkv", [(128, 16, 32, 8), (64, 32, 8, 8), (128, 32, 16, 2),
+                                          (64, 16, 20, 2), (128, 16, 64, 8)])
+def test_draft_verification(oracle, D, bs, Hq, Hkv):
+    """A few new tokens per sequence on contexts from one token up, including a
+    sequence whose whole context is new and one with a single new token."""
+    lens = [1, 5, 17, 100, 513, 1300, 2100]
+    qlen = [1, 5, 4, 8, 3, 1, 7]
+    case = workloads.build_multi_case(f"verify-{D}-{bs}-{Hq}-{Hkv}", S=len(lens), Hq=Hq, Hkv=Hkv,
+                                      D=D, bs=bs, context_lens=lens, query_lens=qlen,
+                                      seed=3 * D + bs + Hq, row_offset=2, extra_rows=3)
+    _run(case, oracle)
+
+
+def test_prefill_chunks(oracle):
+    """Long chunks (several CTAs of columns per kv head): a prompt's first chunk, a
+    later chunk on top of cached tokens and a chunk of one token."""
+    lens = [300, 1000, 77]
+    qlen = [300, 260, 1]
+    case = workloads.build_multi_case("prefill", S=3, Hq=16, Hkv=4, D=128, bs=16, context_lens=lens,
+                                      query_lens=qlen, seed=31)
+    _run(case, oracle)
+
+
+def test_long_context_partitions(oracle):
+    """Few sequences with long contexts: the context is split into partitions that a
+    second kernel merges; columns of one chunk straddle partition boundaries."""
+    lens = [9000, 4097, 6000]
+    qlen = [4, 64, 2]
+    case = workloads.build_multi_case("long", S=3, Hq=8, Hkv=2, D=128, bs=16, context_lens=lens,
+                                      query_lens=qlen, seed=32)
+    _run(case, oracle)
+
+
+def test_one_token_matches_decode(oracle):
+    """With one new token per sequence the step is the decode step."""
+    import paged_kv_cache_197_gb300 as pa
+
+    lens = [1, 16, 33, 700, 5000]
+    case = workloads.build_multi_case("one", S=5, Hq=16, Hkv=4, D=128, bs=16, context_lens=lens,
+                                      query_lens=[1] * 5, seed=33)
+    got = helpers.gpu_multi_step(case, DEV)
+    c = case.to(DEV)
+    dec = torch.empty_like(c.q)
+    ws = pa.decode_workspace(c.q, got["k_cache"], max(lens))
+    pa.pa_decode(dec, c.q, got["k_cache"], got["v_cache"], c.block_tables, c.context_lens,
+                 case.scale, max(lens), workspace=ws)
+    torch.cuda.synchronize()
+    ref = helpers.oracle_multi_out(case, oracle, helpers.oracle_caches(case, oracle))
+    helpers.compare(got["out"], ref, "bf16")
+    helpers.compare(dec, ref, "bf16")
+
+
+def test_bad_offsets_are_skipped(oracle):
+    """A sequence with more new tokens than max_query_len is skipped (QUERY flag, rows
+    untouched); an empty chunk writes nothing; the others are exact."""
+    import paged_kv_cache_197_gb300 as pa
+
+    lens = [50, 400, 90]
+    qlen = [3, 9, 0]
+    case = workloads.build_multi_case("bad", S=3, Hq=8, Hkv=2, D=64, bs=16, context_lens=lens,
+                                      query_lens=qlen, seed=34)
+    got = helpers.gpu_multi_step(case, DEV, max_query_len=4)
+    assert got["flag"] == pa.PA_FLAG_QUERY_OUT_OF_RANGE
+    caches = helpers.oracle_caches(case, oracle)
+    ref = helpers.oracle_multi_out(case, oracle, caches)
+    assert torch.isnan(got["out"][3:12].float()).all()
+    helpers.compare(got["out"][0:3], ref[0:3], "bf16")
+
+
+def test_rejects_unsupported():
+    import paged_kv_cache_197_gb300 as pa
+
+    case = workloads.build_multi_case("rej", S=2, Hq=4, Hkv=4, D=64, bs=16, context_lens=[40, 40],
+                                      query_lens=[2, 2], seed=35).to(DEV)
+    out = torch.empty_like(case.q)
+    i8 = torch.zeros(case.k_pool.shape, dtype=torch.int8, device=DEV)
+    with pytest.raises(pa.PagedAttentionError):
+        pa.pa_multi_token_attention(out, case.q, i8, i8, case.block_tables, case.context_lens,
+                                    case.query_start, case.scale, 40, 2)
+    with pytest.raises(pa.PagedAttentionError):  # max_query_len above the context bound
+        pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, case.block_tables,
+                                    case.context_lens, case.query_start, case.scale, 40, 41)
+    torch.cuda.synchronize()

@@ -57,6 +57,9 @@ class PagedCase:
     cow_pairs: torch.Tensor  # [n][2] int64 (src, dst) physical blocks; n may be 0
     shared_prefix_blocks: int = 0
     meta: dict = field(default_factory=dict)
+    # multi-token steps: [S + 1] int32 row offsets of each sequence's new tokens in q,
+    # new_key, new_value and slot_mapping (then [T] rows instead of [S]); None = decode
+    query_start: torch.Tensor | None = None
 
     @property
     def G(self) -> int:
@@ -179,6 +182,48 @@ def valid_slot_mask(tables: torch.Tensor, lengths: torch.Tensor, bs: int, N: int
     return mask
 
 
+def build_multi_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, context_lens,
+                     query_lens, seed: int, pool_blocks: int | None = None, poison: bool = True,
+                     device="cpu", row_offset: int = 0, extra_rows: int = 0) -> PagedCase:
+    """A multi-token step: sequence s brings query_lens[s] new tokens at positions
+    context_lens[s] - query_lens[s] .. context_lens[s] - 1 (context_lens count them).
+    q, new_key, new_value and slot_mapping hold T rows, sequence s owning rows
+    query_start[s] .. query_start[s + 1] - 1; row_offset rows before the first
+    sequence and extra_rows after the last belong to no sequence (their slots are -1).
+    With ``poison`` every slot not holding one of the tokens before the new ones is
+    bf16 NaN."""
+    L = [int(x) for x in query_lens]
+    ctx = [int(c) for c in context_lens]
+    assert len(L) == S and all(0 <= l <= c for l, c in zip(L, ctx))
+    case = build_case(name, S=S, Hq=Hq, Hkv=Hkv, D=D, bs=bs, context_lens=ctx, seed=seed,
+                      pool_blocks=pool_blocks, poison=False, device=device)
+    qs = [row_offset]
+    for l in L:
+        qs.append(qs[-1] + l)
+    T = qs[-1] + extra_rows
+    big = _gen(seed + 2, device)
+    q = _randn_bf16((T, Hq, D), big, device)
+    new_key = _randn_bf16((T, Hkv, D), big, device)
+    new_value = _randn_bf16((T, Hkv, D), big, device)
+    tables = case.block_tables.cpu()
+    slots = torch.full((T,), -1, dtype=torch.int64)
+    for s_ in range(S):
+        for i in range(L[s_]):
+            pos = ctx[s_] - L[s_] + i
+            slots[qs[s_] + i] = int(tables[s_, pos // bs]) * bs + pos % bs
+    if poison:
+        before = torch.tensor([c - l for c, l in zip(ctx, L)], dtype=torch.int64)
+        bad = ~valid_slot_mask(case.meta["content_tables"], before, bs, case.N).to(device)
+        nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
+        for pool in (case.k_pool, case.v_pool):
+            pool.permute(0, 2, 1, 3)[bad] = nan
+    case.q, case.new_key, case.new_value = q, new_key, new_value
+    case.slot_mapping = slots.to(device)
+    case.query_start = torch.tensor(qs, dtype=torch.int32, device=device)
+    case.meta["query_lens"] = L
+    return case
+
+
 # --------------------------------------------------------------------------- configs
 def tiny(seed: int = 0, device="cpu", poison=True) -> PagedCase:
     return build_case("tiny", S=4, Hq=2, Hkv=2, D=64, bs=16, context_lens=[1, 17, 40, 100],
@@ -220,7 +265,23 @@ def fp8(seed: int = 5, device="cpu", poison=False) -> PagedCase:
                       seed=seed, kv_dtype="fp8", poison=poison, device=device)
 
 
-CONFIGS = {"tiny": tiny, "mha13b": mha13b, "gqa70b": gqa70b, "prefix": prefix, "int8": int8, "fp8": fp8}
+def verify70b(seed: int = 6, device="cpu", poison=False) -> PagedCase:
+    """Draft verification on the 70B-shaped GQA batch: 4 new tokens per sequence on
+    8000-token contexts (the 4 included)."""
+    return build_multi_case("verify70b", S=20, Hq=64, Hkv=8, D=128, bs=16, context_lens=[8000] * 20,
+                            query_lens=[4] * 20, seed=seed, pool_blocks=10000, poison=poison,
+                            device=device)
+
+
+def prefill8b(seed: int = 7, device="cpu", poison=False) -> PagedCase:
+    """Chunked prefill, Llama-3-8B shape: 4 sequences each attending a 512-token chunk
+    on top of 3584 cached tokens."""
+    return build_multi_case("prefill8b", S=4, Hq=32, Hkv=8, D=128, bs=16, context_lens=[4096] * 4,
+                            query_lens=[512] * 4, seed=seed, poison=poison, device=device)
+
+
+CONFIGS = {"tiny": tiny, "mha13b": mha13b, "gqa70b": gqa70b, "prefix": prefix, "int8": int8, "fp8": fp8,
+           "verify70b": verify70b, "prefill8b": prefill8b}
 
 
 # ------------------------------------------------------------------ byte accounting
@@ -254,18 +315,34 @@ def decode_algorithmic_bytes(case: PagedCase, unique_blocks: bool = False) -> in
         kv = sum(seen.values()) * per_token
     else:
         kv = int(ctx.sum()) * per_token
-    qo = 2 * case.S * case.Hq * case.D * 2
+    qo = 2 * case.q.shape[0] * case.Hq * case.D * 2  # query rows: S, or T new tokens
     tables = sum(blocks_needed(int(c), case.bs) for c in ctx) * 4 + case.S * 4
+    if case.query_start is not None:
+        tables += (case.S + 1) * 4
     return int(kv + qo + tables)
 
 
+def multi_token_flops(case: PagedCase) -> int:
+    """Multiply-adds x 2 of a multi-token step: each new token and query head takes a
+    D-long dot product with, and a D-long weighted sum of, every position it sees."""
+    qs = case.query_start.cpu().tolist()
+    ctx = case.context_lens.cpu().tolist()
+    seen = 0
+    for s in range(case.S):
+        L = qs[s + 1] - qs[s]
+        base = ctx[s] - L
+        seen += L * base + L * (L + 1) // 2
+    return 4 * seen * case.Hq * case.D
+
+
 def append_algorithmic_bytes(case: PagedCase) -> int:
-    """Bytes of one append of case.S new tokens: read K and V rows, write them (int8: codes
-    and one fp32 scale per row), plus the slot numbers."""
-    rows = case.S * case.Hkv
+    """Bytes of one append of the step's new tokens (one per sequence, or T): read K and
+    V rows, write them (int8: codes and one fp32 scale per row), plus the slot numbers."""
+    T = case.new_key.shape[0]
+    rows = T * case.Hkv
     if case.kv_dtype in ("int8", "fp8"):
-        return rows * 2 * (case.D * 2 + case.D + 4) + case.S * 8
-    return rows * 2 * case.D * 2 * 2 + case.S * 8
+        return rows * 2 * (case.D * 2 + case.D + 4) + T * 8
+    return rows * 2 * case.D * 2 * 2 + T * 8
 
 
 def fragmentation(case: PagedCase, max_len: int) -> dict:
