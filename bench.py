@@ -57,9 +57,15 @@ DESCRIPTIONS = {
 FLUSH_L2 = {"tiny", "prefix", "prefill8b"}
 L2_BYTES = 126 * 1024 * 1024
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode launch, from an ncu capture
-# of the kernel source with this sha256 (null once the source changes).
-NCU_TRAFFIC = {}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
+# an ncu capture of the kernel source with this sha256 prefix (null once it changes).
+NCU_TRAFFIC = {
+    ("mha13b", "626bf5ea96dcc516"): 1392730368 + 3550208,
+    ("gqa70b", "626bf5ea96dcc516"): 655776512 + 5093888,
+    ("int8", "626bf5ea96dcc516"): 3144355840 + 5534208,
+    ("fp8", "626bf5ea96dcc516"): 3144595456 + 5257216,
+    ("verify70b", "5304df044b4257f6"): 656960768 + 23457024,
+}
 
 
 def measured_peaks() -> dict:
@@ -71,8 +77,9 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def decode_source_hash() -> str:
-    src = ROOT / "paged_kv_cache_197_gb300" / "csrc" / "pa_decode.cu"
+def kernel_source_hash(name: str = "pa_decode.cu") -> str:
+    """sha256[:16] of the CUDA source of the kernel a workload times."""
+    src = ROOT / "paged_kv_cache_197_gb300" / "csrc" / name
     return hashlib.sha256(src.read_bytes()).hexdigest()[:16]
 
 
@@ -348,7 +355,8 @@ def run_ours(args, rank, world, device) -> dict | None:
     else:
         achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
         kernel_name = "pa_decode call (decode + partition merge)"
-    src_hash = decode_source_hash()
+    src_hash = kernel_source_hash("pa_multi.cu" if step.multi else
+                                  "pa_prefix.cu" if step.prefix else "pa_decode.cu")
     traffic = NCU_TRAFFIC.get((args.config, src_hash))
     value = whole_job_gbs(nbytes["total"], world, ms_per_step)
     res = {

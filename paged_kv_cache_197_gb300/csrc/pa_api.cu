@@ -477,6 +477,10 @@ struct MultiPlan {
     size_t acc_off, ml_off, bytes;
 };
 
+// Fixed cost of one multi-token CTA (q fragments, the join of token slices, the
+// writes) in tokens of streaming: larger than the decode kernel's.
+constexpr double kMultiRampTokens = 256.0;
+
 static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int max_context_len, int max_query_len) {
     MultiPlan p{};
     const int G = Hq / Hkv;
@@ -495,7 +499,7 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int max_contex
             if (waves < 2.0 && cand != 256) continue;
             const double fill = waves / std::ceil(waves);
             const double len = (double)std::min(cand, ctx);
-            const double score = fill * len / (len + 64.0);
+            const double score = fill * len / (len + kMultiRampTokens);
             if (score > best + 1e-9) {
                 best = score;
                 p.part_tokens = cand;
@@ -585,6 +589,7 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.G = Hq / Hkv;
+    a.g_shift = (a.G & (a.G - 1)) == 0 ? __builtin_ctz((unsigned)a.G) : -1;
     a.N = N;
     a.CB = plan.CB;
     a.part_tokens = plan.part_tokens;

@@ -79,6 +79,7 @@ struct MultiArgs {
     float *ws_acc, *ws_ml;         // [T][Hq][max_parts][D], [T][Hq][max_parts][2]
     int *err_flag;
     int M, S, T, Hq, Hkv, G, N;
+    int g_shift;                   // log2(G) when G is a power of two, else -1
     int CB;                        // blocks of 128 (token, head) columns per kv head
     int part_tokens, max_parts;    // context partitions (multiple of 64 tokens)
     int max_context_len, max_query_len;

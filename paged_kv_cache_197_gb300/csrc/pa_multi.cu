@@ -68,6 +68,15 @@ __device__ __forceinline__ SeqView seq_view(const MultiArgs &a, int s, bool repo
     return v;
 }
 
+// Column c of a kv head is new token c / G, query head c % G: a shift and a mask when
+// G is a power of two (g_shift >= 0), else a division.
+__device__ __forceinline__ int col_token(const MultiArgs &a, int c) {
+    return a.g_shift >= 0 ? c >> a.g_shift : c / a.G;
+}
+__device__ __forceinline__ int col_head(const MultiArgs &a, int c) {
+    return a.g_shift >= 0 ? c & (a.G - 1) : c % a.G;
+}
+
 template <int D>
 __host__ __device__ constexpr int multi_smem_bytes() {
     return (4 * kChunk * (2 * D + 16)) > (kWarps * kColsPerWarp * (D + 4) * 4)
@@ -99,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     const int col0 = cb * kColsPerCta;
     if (col0 >= ncols) return;
     // the CTA's last column sees the most tokens
-    const int cta_lim = v.base + (min(ncols, col0 + kColsPerCta) - 1) / a.G;  // inclusive
+    const int cta_lim = v.base + col_token(a, min(ncols, col0 + kColsPerCta) - 1);  // inclusive
     const int tok_begin = part * a.part_tokens;
     const int tok_end = min(tok_begin + a.part_tokens, cta_lim + 1);
     if (tok_begin >= tok_end) return;
@@ -131,8 +140,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     for (int nt = 0; nt < 2; ++nt) {
         const int c = wcol0 + nt * 8 + gq;
         if (c < ncols) {
-            const int64_t row = v.row0 + c / a.G;
-            const uint16_t *qrow = a.q + (row * a.Hq + kvh * a.G + c % a.G) * D;
+            const int64_t row = v.row0 + col_token(a, c);
+            const uint16_t *qrow = a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D;
 #pragma unroll
             for (int kc = 0; kc < KC; ++kc) {
                 qf[nt][kc][0] = __ldg(reinterpret_cast<const uint32_t *>(qrow + kc * 16 + 2 * t));
@@ -146,10 +155,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
         for (int j = 0; j < 2; ++j) {
             const int cj = wcol0 + nt * 8 + 2 * t + j;
             // clamped to the partition: tokens past it are masked with the rest
-            lim[nt][j] = cj < ncols ? min(v.base + cj / a.G, tok_end - 1) : -1;
+            lim[nt][j] = cj < ncols ? min(v.base + col_token(a, cj), tok_end - 1) : -1;
         }
     }
-    const int warp_lim = wcol0 < ncols ? min(v.base + (min(ncols, wcol0 + kColsPerWarp) - 1) / a.G, tok_end - 1) : -1;
+    const int warp_lim = wcol0 < ncols ? min(v.base + col_token(a, min(ncols, wcol0 + kColsPerWarp) - 1), tok_end - 1) : -1;
 
     float o[2][MT][4];
     float m[2][2], l[2][2];
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     for (int cc = warp; cc < ncg * kColsPerWarp; cc += kWarps) {
         const int c = col0 + cc;
         if (c >= ncols) break;
-        const int i = c / a.G, h = kvh * a.G + c % a.G;
+        const int i = col_token(a, c), h = kvh * a.G + col_head(a, c);
         const int lim_c = v.base + i;
         if (tok_begin > lim_c) continue;  // this partition holds nothing the column sees
         const int g = cc / kColsPerWarp, cl = cc % kColsPerWarp;

@@ -171,7 +171,7 @@ def test_shared_prefix_workspace_and_checks(lib):
 def test_multi_token_workspace_and_checks(lib):
     """Multi-token attention: 128 (token, head) columns per CTA; no partition when the
     columns give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the
-    best of (last-wave fill) x (len / (len + 64)) over 4096..256-token partitions with
+    best of (last-wave fill) x (len / (len + 256)) over 4096..256-token partitions with
     >= 2 waves (256 as the fallback).  The workspace holds (D + 2) fp32 per query row,
     head and partition."""
     import math
@@ -191,7 +191,7 @@ def test_multi_token_workspace_and_checks(lib):
             if waves < 2 and cand != 256:
                 continue
             ln = min(cand, ctx)
-            score = waves / math.ceil(waves) * ln / (ln + 64)
+            score = waves / math.ceil(waves) * ln / (ln + 256)
             if score > best + 1e-9:
                 best, best_p = score, cand
         return best_p
