@@ -421,20 +421,261 @@ __global__ void __launch_bounds__(128) merge_multi_kernel(const __grid_constant_
     for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t *>(dst + e) = bf16x2(acc[e] * inv, acc[e + 1] * inv);
 }
 
+// ---------------------------------------------------------------------------
+// Many columns per kv head (prefill chunks): the same computation with the query
+// columns as the rows (M) of the tensor-core products, FlashAttention-2 style.  A
+// warp owns 16 columns and takes a whole 64-token chunk per step: S = Q K^T as 8
+// n-tiles of 8 tokens (Q fragments from shared memory, K by ldmatrix), one online
+// softmax step per chunk with each row's max over the 4 lanes that hold it, then
+// O += P V with P's accumulators reused as the A operand (no transpose).  Chunks
+// that every column of the warp sees in full skip the mask.
+template <int D>
+__host__ __device__ constexpr int prefill_smem_bytes() {
+    return 4 * kChunk * (2 * D + 16) + kColsPerCta * (2 * D + 16);
+}
+
+template <int D, int BS>
+__global__ void __launch_bounds__(kThreads, 2) paged_prefill_kernel(const __grid_constant__ MultiArgs a) {
+    constexpr int ROW = D * 2;
+    constexpr int RS = ROW + 16;
+    constexpr int STAGE = kChunk * RS;
+    constexpr int CPR = ROW / 16;
+    constexpr int KC = D / 16;   // k-steps of S = Q K^T
+    constexpr int NT = kChunk / 8;  // 8-token n-tiles of a chunk
+    constexpr int DT = D / 8;    // 8-wide d-tiles of O
+    extern __shared__ __align__(128) unsigned char smem[];  // K0 K1 V0 V1 Q
+    __shared__ int s_blk[kMaxPartBlocks];
+
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
+    const int s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t = lane & 3;
+
+    const SeqView v = seq_view<BS>(a, s, part == 0 && blockIdx.y == 0 && tid == 0);
+    if (!v.ok) return;
+    const int ncols = v.L * a.G;
+    const int col0 = cb * kColsPerCta;
+    if (col0 >= ncols) return;
+    const int cta_lim = v.base + col_token(a, min(ncols, col0 + kColsPerCta) - 1);
+    const int tok_begin = part * a.part_tokens;
+    const int tok_end = min(tok_begin + a.part_tokens, cta_lim + 1);
+    if (tok_begin >= tok_end) return;
+    const int blk0 = tok_begin / BS;
+    const int nblk = (tok_end - tok_begin + BS - 1) / BS;
+    for (int i = tid; i < nblk; i += kThreads) {
+        int b = a.block_tables[(int64_t)s * a.M + blk0 + i];
+        if (b < 0 || b >= a.N) {
+            if (cb == 0) raise_flag(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
+            b = -1;
+        }
+        s_blk[i] = b;
+    }
+    unsigned char *ks = smem, *vs = smem + 2 * STAGE, *qs = smem + 4 * STAGE;
+    // the CTA's query rows (one per column; zeros past the last column)
+    for (int i = tid; i < kColsPerCta * CPR; i += kThreads) {
+        const int r = i / CPR, pc = i % CPR;
+        const int c = col0 + r;
+        const void *src = a.q;
+        uint32_t bytes = 0;
+        if (c < ncols) {
+            const int64_t row = v.row0 + col_token(a, c);
+            src = reinterpret_cast<const char *>(a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D) + pc * 16;
+            bytes = 16;
+        }
+        cp_async16(smem_u32(qs + r * RS + pc * 16), src, bytes);
+    }
+    // rows gq and gq + 8 of this warp: last visible position (-1: no such column)
+    const int wcol0 = col0 + warp * kColsPerWarp;
+    int lim[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int c = wcol0 + gq + 8 * h;
+        lim[h] = c < ncols ? min(v.base + col_token(a, c), tok_end - 1) : -1;
+    }
+    const int warp_hi = wcol0 < ncols ? min(v.base + col_token(a, min(ncols, wcol0 + kColsPerWarp) - 1), tok_end - 1) : -1;
+    const int warp_lo = wcol0 < ncols ? min(v.base + col_token(a, wcol0), tok_end - 1) : -1;
+    __syncthreads();  // s_blk
+
+    constexpr int RPP = kThreads / CPR;
+    constexpr int PASSES = kChunk / RPP;
+    const int pc = tid % CPR, pr = tid / CPR;
+    const int64_t block_stride = (int64_t)a.Hkv * BS * ROW;
+    const char *kbase_g = static_cast<const char *>(a.k_cache) + (int64_t)kvh * BS * ROW + pc * 16;
+    const char *vbase_g = static_cast<const char *>(a.v_cache) + (int64_t)kvh * BS * ROW + pc * 16;
+    const uint32_t kdst0 = smem_u32(ks) + pr * RS + pc * 16, vdst0 = smem_u32(vs) + pr * RS + pc * 16;
+    auto stage_chunk = [&](int j, int buf) {
+        const int c0 = tok_begin + j * kChunk;
+#pragma unroll
+        for (int k = 0; k < PASSES; ++k) {
+            const int tok = c0 + pr + k * RPP;
+            const char *ksrc = kbase_g, *vsrc = vbase_g;
+            uint32_t bytes = 0;
+            if (tok < tok_end) {
+                const int b = s_blk[tok / BS - blk0];
+                if (b >= 0) {
+                    const int64_t off = b * block_stride + (tok % BS) * ROW;
+                    ksrc += off;
+                    vsrc += off;
+                    bytes = 16;
+                }
+            }
+            const uint32_t doff = buf * STAGE + k * RPP * RS;
+            cp_async16(kdst0 + doff, ksrc, bytes);
+            cp_async16(vdst0 + doff, vsrc, bytes);
+        }
+        cp_async_commit();
+    };
+
+    float o[DT][4];
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    // ldmatrix lane addresses: Q as A (rows = columns), K as B (rows = tokens), V as
+    // B transposed (rows = tokens)
+    const uint32_t qaddr = smem_u32(qs) + (warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * RS + (lane >> 4) * 16;
+    const uint32_t krow = ((lane & 7) + ((lane >> 4) << 3)) * RS + ((lane >> 3) & 1) * 16;
+    const uint32_t vrow = ((lane & 7) + (((lane >> 3) & 1) << 3)) * RS + (lane >> 4) * 16;
+
+    const int nchunks = (tok_end - tok_begin + kChunk - 1) / kChunk;
+    stage_chunk(0, 0);  // first group: the query rows and chunk 0
+    for (int j = 0; j < nchunks; ++j) {
+        if (j + 1 < nchunks) {
+            stage_chunk(j + 1, (j + 1) & 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const int c0 = tok_begin + j * kChunk;
+        if (c0 <= warp_hi) {  // warp-uniform
+            const uint32_t kb = smem_u32(ks + (j & 1) * STAGE) + krow;
+            const uint32_t vb = smem_u32(vs + (j & 1) * STAGE) + vrow;
+            float sc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc) {
+                uint32_t qa[4];
+                ldsm_x4(qa, qaddr + kc * 32);
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t kb4[4];
+                    ldsm_x4(kb4, kb + np * 16 * RS + kc * 32);
+                    mma16816(sc[2 * np], qa, kb4[0], kb4[1]);
+                    mma16816(sc[2 * np + 1], qa, kb4[2], kb4[3]);
+                }
+            }
+            // every row of the warp sees the whole chunk: no mask
+            const bool full = c0 + kChunk - 1 <= warp_lo;
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float x = sc[nt][c] * a.scale_log2;
+                    if (!full) {
+                        const int tok = c0 + nt * 8 + 2 * t + (c & 1);
+                        x = tok <= lim[c >> 1] ? x : -INFINITY;
+                    }
+                    sc[nt][c] = x;
+                    mx[c >> 1] = fmaxf(mx[c >> 1], x);
+                }
+            float base[2], alpha[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+                const float mnew = fmaxf(m[h], mx[h]);
+                base[h] = mnew == -INFINITY ? 0.f : mnew;
+                alpha[h] = ex2(m[h] - base[h]);
+                m[h] = mnew;
+                l[h] *= alpha[h];
+            }
+            if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+                for (int dt = 0; dt < DT; ++dt) {
+                    o[dt][0] *= alpha[0];
+                    o[dt][1] *= alpha[0];
+                    o[dt][2] *= alpha[1];
+                    o[dt][3] *= alpha[1];
+                }
+            }
+#pragma unroll
+            for (int kk = 0; kk < NT / 2; ++kk) {
+                float p[2][4];
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        p[u][c] = ex2(sc[2 * kk + u][c] - base[c >> 1]);
+                        l[c >> 1] += p[u][c];
+                    }
+                const uint32_t pa[4] = {bf16x2(p[0][0], p[0][1]), bf16x2(p[0][2], p[0][3]),
+                                        bf16x2(p[1][0], p[1][1]), bf16x2(p[1][2], p[1][3])};
+#pragma unroll
+                for (int dp = 0; dp < DT / 2; ++dp) {
+                    uint32_t vb4[4];
+                    ldsm_x4_trans(vb4, vb + kk * 16 * RS + dp * 32);
+                    mma16816(o[2 * dp], pa, vb4[0], vb4[1]);
+                    mma16816(o[2 * dp + 1], pa, vb4[2], vb4[3]);
+                }
+            }
+        }
+        __syncthreads();  // this buffer is refilled two chunks later
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (wcol0 >= ncols) return;
+
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int c = wcol0 + gq + 8 * h;
+        if (c >= ncols) continue;
+        const int lim_c = v.base + col_token(a, c);
+        if (tok_begin > lim_c) continue;  // this partition holds nothing the column sees
+        const int64_t pair = (int64_t)(v.row0 + col_token(a, c)) * a.Hq + kvh * a.G + col_head(a, c);
+        if (lim_c < a.part_tokens) {
+            const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+            uint16_t *dst = a.out + pair * D + 2 * t;
+#pragma unroll
+            for (int dt = 0; dt < DT; ++dt)
+                *reinterpret_cast<uint32_t *>(dst + dt * 8) = bf16x2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
+        } else {
+            const int64_t prow = pair * a.max_parts + part;
+            float *dst = a.ws_acc + prow * D + 2 * t;
+#pragma unroll
+            for (int dt = 0; dt < DT; ++dt)
+                *reinterpret_cast<float2 *>(dst + dt * 8) = make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
+            if (t == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(m[h], l[h]);
+        }
+    }
+}
+
 template <int D, int BS>
 cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
     constexpr int SMEM = multi_smem_bytes<D>();
+    constexpr int PSMEM = prefill_smem_bytes<D>();
     static bool configured[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(paged_multi_kernel<D, BS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(paged_prefill_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
-    paged_multi_kernel<D, BS><<<grid, kThreads, SMEM, stream>>>(a);
+    // a full CTA of columns per kv head: the prefill layout; few columns: token slices
+    if ((int64_t)a.max_query_len * a.G >= kColsPerCta)
+        paged_prefill_kernel<D, BS><<<grid, kThreads, PSMEM, stream>>>(a);
+    else
+        paged_multi_kernel<D, BS><<<grid, kThreads, SMEM, stream>>>(a);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || a.max_parts == 1) return err;
     cudaLaunchConfig_t cfg = {};
