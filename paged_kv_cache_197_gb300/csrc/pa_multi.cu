@@ -9,12 +9,15 @@
 // Work unit ("column"): one (new token, query head) pair.  The columns of a sequence
 // and kv head share that kv head's K and V, so a CTA takes up to 128 of them and
 // streams the sequence's K and V once for all: 64-token chunks staged in shared
-// memory by cp.async, double-buffered.  A warp multiplies 16-token tiles against 16
-// query columns on the tensor cores (S = K q^T, then O^T += V^T P^T), with an online
-// softmax in the exp2 domain and each column masked at its own position.  Warps are
-// (column group, token slice) pairs: with few columns (draft tokens) up to four
-// warps split the tiles of one group, and the slices are joined by log-sum-exp in
-// shared memory before the column is written.
+// memory by cp.async, double-buffered.  The columns are the rows (M) of the
+// tensor-core products, FlashAttention-2 style: a warp owns 16 columns and, per
+// chunk, computes S = Q K^T over its share of the chunk's tokens (Q fragments from
+// shared memory, K by ldmatrix), one online-softmax step in the exp2 domain with each
+// row's max over the 4 lanes that hold it and each column masked at its own
+// position, then O += P V with P's accumulators reused as the A operand.  Warps are
+// (column group, token slice) pairs: with 5..8 groups a warp takes whole chunks;
+// with fewer columns (draft tokens) 2 or 4 warps split each chunk of a group, and
+// the slices are joined by log-sum-exp in shared memory before a column is written.
 // Long contexts are split into partitions (grid x); a column whose visible tokens
 // span one partition is finished in place, the others leave (max, sum, output)
 // partials that a second kernel joins by log-sum-exp.
@@ -79,23 +82,102 @@ __device__ __forceinline__ int col_head(const MultiArgs &a, int c) {
 
 template <int D>
 __host__ __device__ constexpr int multi_smem_bytes() {
-    return (4 * kChunk * (2 * D + 16)) > (kWarps * kColsPerWarp * (D + 4) * 4)
-               ? (4 * kChunk * (2 * D + 16))
-               : (kWarps * kColsPerWarp * (D + 4) * 4);
+    // K and V stages, then the query rows; the slice join reuses the stages
+    return 4 * kChunk * (2 * D + 16) + kColsPerCta * (2 * D + 16);
+}
+static_assert(kWarps * kColsPerWarp * (128 + 4) * 4 <= 4 * kChunk * (2 * 128 + 16), "join fits the stages");
+
+// One online-softmax step of a warp over NTW 8-token n-tiles of a staged chunk:
+// S = Q K^T (rows = the warp's 16 columns), mask, running max and sum, O += P V.
+template <int D, int NTW>
+__device__ __forceinline__ void attend_tokens(float (&o)[D / 8][4], float (&m)[2], float (&l)[2],
+                                              uint32_t qaddr, uint32_t kb, uint32_t vb, int tok0,
+                                              bool full, const int (&lim)[2], float scale_log2, int t) {
+    constexpr int RS = 2 * D + 16;
+    constexpr int KC = D / 16;
+    constexpr int DT = D / 8;
+    float sc[NTW][4];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < KC; ++kc) {
+        uint32_t qa[4];
+        ldsm_x4(qa, qaddr + kc * 32);
+#pragma unroll
+        for (int np = 0; np < NTW / 2; ++np) {
+            uint32_t kb4[4];
+            ldsm_x4(kb4, kb + np * 16 * RS + kc * 32);
+            mma16816(sc[2 * np], qa, kb4[0], kb4[1]);
+            mma16816(sc[2 * np + 1], qa, kb4[2], kb4[3]);
+        }
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float x = sc[nt][c] * scale_log2;
+            if (!full) {
+                const int tok = tok0 + nt * 8 + 2 * t + (c & 1);
+                x = tok <= lim[c >> 1] ? x : -INFINITY;
+            }
+            sc[nt][c] = x;
+            mx[c >> 1] = fmaxf(mx[c >> 1], x);
+        }
+    float base[2], alpha[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float mnew = fmaxf(m[h], mx[h]);
+        base[h] = mnew == -INFINITY ? 0.f : mnew;
+        alpha[h] = ex2(m[h] - base[h]);
+        m[h] = mnew;
+        l[h] *= alpha[h];
+    }
+    // the running maxima settle after a few steps: rescale only when one moved
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+            o[dt][0] *= alpha[0];
+            o[dt][1] *= alpha[0];
+            o[dt][2] *= alpha[1];
+            o[dt][3] *= alpha[1];
+        }
+    }
+#pragma unroll
+    for (int kk = 0; kk < NTW / 2; ++kk) {
+        float p[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                p[u][c] = ex2(sc[2 * kk + u][c] - base[c >> 1]);
+                l[c >> 1] += p[u][c];
+            }
+        const uint32_t pa[4] = {bf16x2(p[0][0], p[0][1]), bf16x2(p[0][2], p[0][3]),
+                                bf16x2(p[1][0], p[1][1]), bf16x2(p[1][2], p[1][3])};
+#pragma unroll
+        for (int dp = 0; dp < DT / 2; ++dp) {
+            uint32_t vb4[4];
+            ldsm_x4_trans(vb4, vb + kk * 16 * RS + dp * 32);
+            mma16816(o[2 * dp], pa, vb4[0], vb4[1]);
+            mma16816(o[2 * dp + 1], pa, vb4[2], vb4[3]);
+        }
+    }
 }
 
 template <int D, int BS>
 __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_constant__ MultiArgs a) {
-    constexpr int ROW = D * 2;         // bytes of one token row (bf16)
-    constexpr int RS = ROW + 16;       // padded shared-memory row stride
+    constexpr int ROW = D * 2;          // bytes of one token row (bf16)
+    constexpr int RS = ROW + 16;        // padded shared-memory row stride
     constexpr int STAGE = kChunk * RS;  // one K (or V) stage
-    constexpr int CPR = ROW / 16;      // 16-byte pieces per row
-    constexpr int KC = D / 16;         // k-steps of the score product
-    constexpr int MT = D / 16;         // d tiles of the output product
-    constexpr int PER = D / 32;        // output values per lane in the epilogue
-    extern __shared__ __align__(128) unsigned char smem[];  // K0 K1 V0 V1, then the epilogue
+    constexpr int CPR = ROW / 16;       // 16-byte pieces per row
+    constexpr int DT = D / 8;           // 8-wide d-tiles of O
+    constexpr int PER = D / 32;         // values per lane in the join
+    extern __shared__ __align__(128) unsigned char smem[];  // K0 K1 V0 V1 Q
     __shared__ int s_blk[kMaxPartBlocks];
-    __shared__ float s_ml[kWarps][kColsPerWarp][2];  // each warp's (max, sum) per column
+    __shared__ float s_ml[kWarps][kColsPerWarp][2];  // each warp's (max, sum) per row
 
     const int part = blockIdx.x;
     const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
@@ -122,59 +204,43 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
         }
         s_blk[i] = b;
     }
-
-    // warps = (column group of 16, token slice): with few columns (draft tokens) the
-    // idle warps take other tiles of the same columns, and the slices are joined at
-    // the end; with 5..8 groups every warp owns a group and sees every tile
-    const int ncg = (min(ncols - col0, kColsPerCta) + kColsPerWarp - 1) / kColsPerWarp;
-    const int P2 = ncg <= 1 ? 1 : ncg <= 2 ? 2 : ncg <= 4 ? 4 : 8;
-    const int slices = min(4, kWarps / P2);  // 4 tiles per chunk
-    const int cg = warp % P2, slice = warp / P2;
-    const bool active = cg < ncg && slice < slices;
-    // this warp's 16 columns: q as mma B fragments, and each column's last visible
-    // position (-1: no such column)
-    const int wcol0 = active ? col0 + cg * kColsPerWarp : ncols;
-    uint32_t qf[2][KC][2];
-    int lim[2][2];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int c = wcol0 + nt * 8 + gq;
+    unsigned char *ks = smem, *vs = smem + 2 * STAGE, *qs = smem + 4 * STAGE;
+    // the CTA's query rows, one per column (zeros past the last column)
+    for (int i = tid; i < kColsPerCta * CPR; i += kThreads) {
+        const int r = i / CPR, pc = i % CPR;
+        const int c = col0 + r;
+        const void *src = a.q;
+        uint32_t bytes = 0;
         if (c < ncols) {
             const int64_t row = v.row0 + col_token(a, c);
-            const uint16_t *qrow = a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D;
-#pragma unroll
-            for (int kc = 0; kc < KC; ++kc) {
-                qf[nt][kc][0] = __ldg(reinterpret_cast<const uint32_t *>(qrow + kc * 16 + 2 * t));
-                qf[nt][kc][1] = __ldg(reinterpret_cast<const uint32_t *>(qrow + kc * 16 + 8 + 2 * t));
-            }
-        } else {
-#pragma unroll
-            for (int kc = 0; kc < KC; ++kc) qf[nt][kc][0] = qf[nt][kc][1] = 0u;
+            src = reinterpret_cast<const char *>(a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D) + pc * 16;
+            bytes = 16;
         }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int cj = wcol0 + nt * 8 + 2 * t + j;
-            // clamped to the partition: tokens past it are masked with the rest
-            lim[nt][j] = cj < ncols ? min(v.base + col_token(a, cj), tok_end - 1) : -1;
-        }
+        cp_async16(smem_u32(qs + r * RS + pc * 16), src, bytes);
     }
-    const int warp_lim = wcol0 < ncols ? min(v.base + col_token(a, min(ncols, wcol0 + kColsPerWarp) - 1), tok_end - 1) : -1;
 
-    float o[2][MT][4];
-    float m[2][2], l[2][2];
+    // warps = (group of 16 columns, token slice)
+    const int ncg = (min(ncols - col0, kColsPerCta) + kColsPerWarp - 1) / kColsPerWarp;
+    const int P2 = ncg <= 1 ? 1 : ncg <= 2 ? 2 : ncg <= 4 ? 4 : 8;
+    const int slices = min(4, kWarps / P2);
+    const int grp = warp % P2, slice = warp / P2;
+    const bool active = grp < ncg && slice < slices;
+    const int width = kChunk / slices;  // tokens of a chunk per slice
+    const int wcol0 = col0 + grp * kColsPerWarp;
+    // rows gq and gq + 8: last visible position, clamped to the partition (-1: none)
+    int lim[2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
-        m[nt][0] = m[nt][1] = -INFINITY;
-        l[nt][0] = l[nt][1] = 0.f;
+    for (int h = 0; h < 2; ++h) {
+        const int c = wcol0 + gq + 8 * h;
+        lim[h] = (active && c < ncols) ? min(v.base + col_token(a, c), tok_end - 1) : -1;
     }
+    const int warp_hi = (active && wcol0 < ncols) ? min(v.base + col_token(a, min(ncols, wcol0 + kColsPerWarp) - 1), tok_end - 1) : -1;
+    const int warp_lo = (active && wcol0 < ncols) ? min(v.base + col_token(a, wcol0), tok_end - 1) : -1;
     __syncthreads();  // s_blk
 
-    unsigned char *ks = smem, *vs = smem + 2 * STAGE;
     // staging: thread tid always copies 16-byte piece pc of rows pr, pr + RPP, ... of a
     // chunk, for K and for V; a (block, kv head) is BS contiguous rows in the cache
-    constexpr int RPP = kThreads / CPR;   // rows per pass: 16 (D = 128) or 32 (D = 64)
+    constexpr int RPP = kThreads / CPR;
     constexpr int PASSES = kChunk / RPP;
     const int pc = tid % CPR, pr = tid / CPR;
     const int64_t block_stride = (int64_t)a.Hkv * BS * ROW;
@@ -204,8 +270,18 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
         cp_async_commit();
     };
 
+    float o[DT][4];
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    // ldmatrix lane addresses: Q as A (rows = columns), K as B (rows = tokens), V as
+    // B transposed (rows = tokens), the last two at the slice's first token
+    const uint32_t qaddr = smem_u32(qs) + (grp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * RS + (lane >> 4) * 16;
+    const uint32_t krow = (slice * width + (lane & 7) + ((lane >> 4) << 3)) * RS + ((lane >> 3) & 1) * 16;
+    const uint32_t vrow = (slice * width + (lane & 7) + (((lane >> 3) & 1) << 3)) * RS + (lane >> 4) * 16;
+
     const int nchunks = (tok_end - tok_begin + kChunk - 1) / kChunk;
-    stage_chunk(0, 0);
+    stage_chunk(0, 0);  // first group: the query rows and chunk 0
     for (int j = 0; j < nchunks; ++j) {
         if (j + 1 < nchunks) {
             stage_chunk(j + 1, (j + 1) & 1);
@@ -214,160 +290,112 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
             cp_async_wait<0>();
         }
         __syncthreads();
-        const int buf = j & 1;
-        const uint32_t kbase = smem_u32(ks + buf * STAGE), vbase = smem_u32(vs + buf * STAGE);
-        const int c0 = tok_begin + j * kChunk;
-#pragma unroll 1
-        for (int tt = slice; tt < kChunk / 16; tt += slices) {
-            const int tile0 = c0 + tt * 16;
-            if (tile0 > warp_lim) break;  // warp-uniform
-            float sc[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-            {
-                const int row = tt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const uint32_t rb = kbase + row * RS + (lane >> 4) * 16;
-#pragma unroll
-                for (int kc = 0; kc < KC; ++kc) {
-                    uint32_t af[4];
-                    ldsm_x4(af, rb + kc * 32);
-                    mma16816(sc[0], af, qf[0][kc][0], qf[0][kc][1]);
-                    mma16816(sc[1], af, qf[1][kc][0], qf[1][kc][1]);
-                }
-            }
-            uint32_t pb[2][2];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float x[4], mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int tok = tile0 + gq + 8 * (c >> 1);
-                    x[c] = tok <= lim[nt][c & 1] ? sc[nt][c] * a.scale_log2 : -INFINITY;
-                    mx[c & 1] = fmaxf(mx[c & 1], x[c]);
-                }
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    mx[jj] = fmaxf(mx[jj], __shfl_xor_sync(0xffffffffu, mx[jj], 4));
-                    mx[jj] = fmaxf(mx[jj], __shfl_xor_sync(0xffffffffu, mx[jj], 8));
-                    mx[jj] = fmaxf(mx[jj], __shfl_xor_sync(0xffffffffu, mx[jj], 16));
-                }
-                float base[2], alpha[2];
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const float mnew = fmaxf(m[nt][jj], mx[jj]);
-                    base[jj] = mnew == -INFINITY ? 0.f : mnew;
-                    alpha[jj] = ex2(m[nt][jj] - base[jj]);
-                    m[nt][jj] = mnew;
-                    l[nt][jj] *= alpha[jj];
-                }
-                // the running maxima settle after a few tiles: rescale only when one moved
-                if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        o[nt][mt][0] *= alpha[0];
-                        o[nt][mt][1] *= alpha[1];
-                        o[nt][mt][2] *= alpha[0];
-                        o[nt][mt][3] *= alpha[1];
-                    }
-                }
-                float pr[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    pr[c] = ex2(x[c] - base[c & 1]);
-                    l[nt][c & 1] += pr[c];
-                }
-                pb[nt][0] = movmatrix_t(bf16x2(pr[0], pr[1]));
-                pb[nt][1] = movmatrix_t(bf16x2(pr[2], pr[3]));
-            }
-            {
-                const int row = tt * 16 + (lane & 7) + (lane >> 4) * 8;
-                const uint32_t rb = vbase + row * RS + ((lane >> 3) & 1) * 16;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    uint32_t af[4];
-                    ldsm_x4_trans(af, rb + mt * 32);
-                    mma16816(o[0][mt], af, pb[0][0], pb[0][1]);
-                    mma16816(o[1][mt], af, pb[1][0], pb[1][1]);
-                }
-            }
+        const int tok0 = tok_begin + j * kChunk + slice * width;
+        if (tok0 <= warp_hi) {  // warp-uniform (inactive warps have warp_hi = -1)
+            const uint32_t kb = smem_u32(ks + (j & 1) * STAGE) + krow;
+            const uint32_t vb = smem_u32(vs + (j & 1) * STAGE) + vrow;
+            const bool full = tok0 + width - 1 <= warp_lo;  // every row sees all: no mask
+            if (slices == 1)
+                attend_tokens<D, 8>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
+            else if (slices == 2)
+                attend_tokens<D, 4>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
+            else
+                attend_tokens<D, 2>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
         }
         __syncthreads();  // this buffer is refilled two chunks later
     }
     // the merge grid may launch now (it still waits for this grid before reading)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // per-column sums over the tile rows held by the 8 lanes of each t
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-            l[nt][jj] += __shfl_xor_sync(0xffffffffu, l[nt][jj], 4);
-            l[nt][jj] += __shfl_xor_sync(0xffffffffu, l[nt][jj], 8);
-            l[nt][jj] += __shfl_xor_sync(0xffffffffu, l[nt][jj], 16);
-        }
-
-    // every warp leaves its state in shared memory (the stages are free: every warp
-    // passed the loop's last barrier): O^T transposed to [column][d], (max, sum)
-    float *so = reinterpret_cast<float *>(smem) + warp * kColsPerWarp * (D + 4);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                so[(nt * 8 + 2 * t + (c & 1)) * (D + 4) + mt * 16 + gq + 8 * (c >> 1)] = o[nt][mt][c];
-    if (gq == 0) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                s_ml[warp][nt * 8 + 2 * t + jj][0] = m[nt][jj];
-                s_ml[warp][nt * 8 + 2 * t + jj][1] = l[nt][jj];
-            }
+    for (int h = 0; h < 2; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
     }
-    __syncthreads();
-
-    // one warp per column (round robin): join the token slices, then finish the column
-    // (one partition) or leave a partial
-#pragma unroll 1
-    for (int cc = warp; cc < ncg * kColsPerWarp; cc += kWarps) {
-        const int c = col0 + cc;
-        if (c >= ncols) break;
-        const int i = col_token(a, c), h = kvh * a.G + col_head(a, c);
-        const int lim_c = v.base + i;
-        if (tok_begin > lim_c) continue;  // this partition holds nothing the column sees
-        const int g = cc / kColsPerWarp, cl = cc % kColsPerWarp;
-        float mv = -INFINITY;
-        for (int sl = 0; sl < slices; ++sl) mv = fmaxf(mv, s_ml[sl * P2 + g][cl][0]);
-        const float mb = mv == -INFINITY ? 0.f : mv;
-        float acc[PER];
+    if (slices > 1) {
+        // leave each warp's state in shared memory (the stages are free: every warp
+        // passed the loop's last barrier), rows [column][d]
+        float *so = reinterpret_cast<float *>(smem) + warp * kColsPerWarp * (D + 4);
 #pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-        float lv = 0.f;
-        for (int sl = 0; sl < slices; ++sl) {
-            const int w = sl * P2 + g;
-            const float f = ex2(s_ml[w][cl][0] - mb);
-            lv += f * s_ml[w][cl][1];
-            const float *src = reinterpret_cast<const float *>(smem) + (w * kColsPerWarp + cl) * (D + 4) + lane * PER;
+        for (int dt = 0; dt < DT; ++dt)
 #pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] += f * src[e];
+            for (int h = 0; h < 2; ++h)
+                *reinterpret_cast<float2 *>(so + (gq + 8 * h) * (D + 4) + dt * 8 + 2 * t) =
+                    make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
+        if (t == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                s_ml[warp][gq + 8 * h][0] = m[h];
+                s_ml[warp][gq + 8 * h][1] = l[h];
+            }
         }
-        const int64_t pair = (int64_t)(v.row0 + i) * a.Hq + h;
-        if (lim_c < a.part_tokens) {  // one partition: finish here
-            const float inv = lv > 0.f ? 1.f / lv : 0.f;
-            uint16_t *dst = a.out + pair * D + lane * PER;
-            if constexpr (PER == 4)
-                *reinterpret_cast<uint2 *>(dst) = make_uint2(bf16x2(acc[0] * inv, acc[1] * inv), bf16x2(acc[2] * inv, acc[3] * inv));
-            else
-                *reinterpret_cast<uint32_t *>(dst) = bf16x2(acc[0] * inv, acc[1] * inv);
+        __syncthreads();
+        // one warp per column (round robin): join the slices, then finish the column
+        // (one partition) or leave a partial
+#pragma unroll 1
+        for (int cc = warp; cc < ncg * kColsPerWarp; cc += kWarps) {
+            const int c = col0 + cc;
+            if (c >= ncols) break;
+            const int lim_c = v.base + col_token(a, c);
+            if (tok_begin > lim_c) continue;  // this partition holds nothing the column sees
+            const int g = cc / kColsPerWarp, r = cc % kColsPerWarp;
+            float mv = -INFINITY;
+            for (int sl = 0; sl < slices; ++sl) mv = fmaxf(mv, s_ml[sl * P2 + g][r][0]);
+            const float mb = mv == -INFINITY ? 0.f : mv;
+            float acc[PER];
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+            float lv = 0.f;
+            for (int sl = 0; sl < slices; ++sl) {
+                const int w = sl * P2 + g;
+                const float f = ex2(s_ml[w][r][0] - mb);
+                lv += f * s_ml[w][r][1];
+                const float *src = reinterpret_cast<const float *>(smem) + (w * kColsPerWarp + r) * (D + 4) + lane * PER;
+#pragma unroll
+                for (int e = 0; e < PER; ++e) acc[e] += f * src[e];
+            }
+            const int64_t pair = (int64_t)(v.row0 + col_token(a, c)) * a.Hq + kvh * a.G + col_head(a, c);
+            if (lim_c < a.part_tokens) {
+                const float inv = lv > 0.f ? 1.f / lv : 0.f;
+                uint16_t *dst = a.out + pair * D + lane * PER;
+                if constexpr (PER == 4)
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(bf16x2(acc[0] * inv, acc[1] * inv), bf16x2(acc[2] * inv, acc[3] * inv));
+                else
+                    *reinterpret_cast<uint32_t *>(dst) = bf16x2(acc[0] * inv, acc[1] * inv);
+            } else {
+                const int64_t prow = pair * a.max_parts + part;
+                float *dst = a.ws_acc + prow * D + lane * PER;
+                if constexpr (PER == 4)
+                    *reinterpret_cast<float4 *>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                else
+                    *reinterpret_cast<float2 *>(dst) = make_float2(acc[0], acc[1]);
+                if (lane == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(mv, lv);
+            }
+        }
+        return;
+    }
+    // one slice: each warp finishes its own rows
+    if (!active || wcol0 >= ncols) return;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int c = wcol0 + gq + 8 * h;
+        if (c >= ncols) continue;
+        const int lim_c = v.base + col_token(a, c);
+        if (tok_begin > lim_c) continue;
+        const int64_t pair = (int64_t)(v.row0 + col_token(a, c)) * a.Hq + kvh * a.G + col_head(a, c);
+        if (lim_c < a.part_tokens) {
+            const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+            uint16_t *dst = a.out + pair * D + 2 * t;
+#pragma unroll
+            for (int dt = 0; dt < DT; ++dt)
+                *reinterpret_cast<uint32_t *>(dst + dt * 8) = bf16x2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
         } else {
             const int64_t prow = pair * a.max_parts + part;
-            float *dst = a.ws_acc + prow * D + lane * PER;
-            if constexpr (PER == 4)
-                *reinterpret_cast<float4 *>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            else
-                *reinterpret_cast<float2 *>(dst) = make_float2(acc[0], acc[1]);
-            if (lane == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(mv, lv);
+            float *dst = a.ws_acc + prow * D + 2 * t;
+#pragma unroll
+            for (int dt = 0; dt < DT; ++dt)
+                *reinterpret_cast<float2 *>(dst + dt * 8) = make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
+            if (t == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(m[h], l[h]);
         }
     }
 }
@@ -421,261 +449,20 @@ __global__ void __launch_bounds__(128) merge_multi_kernel(const __grid_constant_
     for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t *>(dst + e) = bf16x2(acc[e] * inv, acc[e + 1] * inv);
 }
 
-// ---------------------------------------------------------------------------
-// Many columns per kv head (prefill chunks): the same computation with the query
-// columns as the rows (M) of the tensor-core products, FlashAttention-2 style.  A
-// warp owns 16 columns and takes a whole 64-token chunk per step: S = Q K^T as 8
-// n-tiles of 8 tokens (Q fragments from shared memory, K by ldmatrix), one online
-// softmax step per chunk with each row's max over the 4 lanes that hold it, then
-// O += P V with P's accumulators reused as the A operand (no transpose).  Chunks
-// that every column of the warp sees in full skip the mask.
-template <int D>
-__host__ __device__ constexpr int prefill_smem_bytes() {
-    return 4 * kChunk * (2 * D + 16) + kColsPerCta * (2 * D + 16);
-}
-
-template <int D, int BS>
-__global__ void __launch_bounds__(kThreads, 2) paged_prefill_kernel(const __grid_constant__ MultiArgs a) {
-    constexpr int ROW = D * 2;
-    constexpr int RS = ROW + 16;
-    constexpr int STAGE = kChunk * RS;
-    constexpr int CPR = ROW / 16;
-    constexpr int KC = D / 16;   // k-steps of S = Q K^T
-    constexpr int NT = kChunk / 8;  // 8-token n-tiles of a chunk
-    constexpr int DT = D / 8;    // 8-wide d-tiles of O
-    extern __shared__ __align__(128) unsigned char smem[];  // K0 K1 V0 V1 Q
-    __shared__ int s_blk[kMaxPartBlocks];
-
-    const int part = blockIdx.x;
-    const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
-    const int s = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t = lane & 3;
-
-    const SeqView v = seq_view<BS>(a, s, part == 0 && blockIdx.y == 0 && tid == 0);
-    if (!v.ok) return;
-    const int ncols = v.L * a.G;
-    const int col0 = cb * kColsPerCta;
-    if (col0 >= ncols) return;
-    const int cta_lim = v.base + col_token(a, min(ncols, col0 + kColsPerCta) - 1);
-    const int tok_begin = part * a.part_tokens;
-    const int tok_end = min(tok_begin + a.part_tokens, cta_lim + 1);
-    if (tok_begin >= tok_end) return;
-    const int blk0 = tok_begin / BS;
-    const int nblk = (tok_end - tok_begin + BS - 1) / BS;
-    for (int i = tid; i < nblk; i += kThreads) {
-        int b = a.block_tables[(int64_t)s * a.M + blk0 + i];
-        if (b < 0 || b >= a.N) {
-            if (cb == 0) raise_flag(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
-            b = -1;
-        }
-        s_blk[i] = b;
-    }
-    unsigned char *ks = smem, *vs = smem + 2 * STAGE, *qs = smem + 4 * STAGE;
-    // the CTA's query rows (one per column; zeros past the last column)
-    for (int i = tid; i < kColsPerCta * CPR; i += kThreads) {
-        const int r = i / CPR, pc = i % CPR;
-        const int c = col0 + r;
-        const void *src = a.q;
-        uint32_t bytes = 0;
-        if (c < ncols) {
-            const int64_t row = v.row0 + col_token(a, c);
-            src = reinterpret_cast<const char *>(a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D) + pc * 16;
-            bytes = 16;
-        }
-        cp_async16(smem_u32(qs + r * RS + pc * 16), src, bytes);
-    }
-    // rows gq and gq + 8 of this warp: last visible position (-1: no such column)
-    const int wcol0 = col0 + warp * kColsPerWarp;
-    int lim[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int c = wcol0 + gq + 8 * h;
-        lim[h] = c < ncols ? min(v.base + col_token(a, c), tok_end - 1) : -1;
-    }
-    const int warp_hi = wcol0 < ncols ? min(v.base + col_token(a, min(ncols, wcol0 + kColsPerWarp) - 1), tok_end - 1) : -1;
-    const int warp_lo = wcol0 < ncols ? min(v.base + col_token(a, wcol0), tok_end - 1) : -1;
-    __syncthreads();  // s_blk
-
-    constexpr int RPP = kThreads / CPR;
-    constexpr int PASSES = kChunk / RPP;
-    const int pc = tid % CPR, pr = tid / CPR;
-    const int64_t block_stride = (int64_t)a.Hkv * BS * ROW;
-    const char *kbase_g = static_cast<const char *>(a.k_cache) + (int64_t)kvh * BS * ROW + pc * 16;
-    const char *vbase_g = static_cast<const char *>(a.v_cache) + (int64_t)kvh * BS * ROW + pc * 16;
-    const uint32_t kdst0 = smem_u32(ks) + pr * RS + pc * 16, vdst0 = smem_u32(vs) + pr * RS + pc * 16;
-    auto stage_chunk = [&](int j, int buf) {
-        const int c0 = tok_begin + j * kChunk;
-#pragma unroll
-        for (int k = 0; k < PASSES; ++k) {
-            const int tok = c0 + pr + k * RPP;
-            const char *ksrc = kbase_g, *vsrc = vbase_g;
-            uint32_t bytes = 0;
-            if (tok < tok_end) {
-                const int b = s_blk[tok / BS - blk0];
-                if (b >= 0) {
-                    const int64_t off = b * block_stride + (tok % BS) * ROW;
-                    ksrc += off;
-                    vsrc += off;
-                    bytes = 16;
-                }
-            }
-            const uint32_t doff = buf * STAGE + k * RPP * RS;
-            cp_async16(kdst0 + doff, ksrc, bytes);
-            cp_async16(vdst0 + doff, vsrc, bytes);
-        }
-        cp_async_commit();
-    };
-
-    float o[DT][4];
-#pragma unroll
-    for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    // ldmatrix lane addresses: Q as A (rows = columns), K as B (rows = tokens), V as
-    // B transposed (rows = tokens)
-    const uint32_t qaddr = smem_u32(qs) + (warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * RS + (lane >> 4) * 16;
-    const uint32_t krow = ((lane & 7) + ((lane >> 4) << 3)) * RS + ((lane >> 3) & 1) * 16;
-    const uint32_t vrow = ((lane & 7) + (((lane >> 3) & 1) << 3)) * RS + (lane >> 4) * 16;
-
-    const int nchunks = (tok_end - tok_begin + kChunk - 1) / kChunk;
-    stage_chunk(0, 0);  // first group: the query rows and chunk 0
-    for (int j = 0; j < nchunks; ++j) {
-        if (j + 1 < nchunks) {
-            stage_chunk(j + 1, (j + 1) & 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const int c0 = tok_begin + j * kChunk;
-        if (c0 <= warp_hi) {  // warp-uniform
-            const uint32_t kb = smem_u32(ks + (j & 1) * STAGE) + krow;
-            const uint32_t vb = smem_u32(vs + (j & 1) * STAGE) + vrow;
-            float sc[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-            for (int kc = 0; kc < KC; ++kc) {
-                uint32_t qa[4];
-                ldsm_x4(qa, qaddr + kc * 32);
-#pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                    uint32_t kb4[4];
-                    ldsm_x4(kb4, kb + np * 16 * RS + kc * 32);
-                    mma16816(sc[2 * np], qa, kb4[0], kb4[1]);
-                    mma16816(sc[2 * np + 1], qa, kb4[2], kb4[3]);
-                }
-            }
-            // every row of the warp sees the whole chunk: no mask
-            const bool full = c0 + kChunk - 1 <= warp_lo;
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float x = sc[nt][c] * a.scale_log2;
-                    if (!full) {
-                        const int tok = c0 + nt * 8 + 2 * t + (c & 1);
-                        x = tok <= lim[c >> 1] ? x : -INFINITY;
-                    }
-                    sc[nt][c] = x;
-                    mx[c >> 1] = fmaxf(mx[c >> 1], x);
-                }
-            float base[2], alpha[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-                mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-                const float mnew = fmaxf(m[h], mx[h]);
-                base[h] = mnew == -INFINITY ? 0.f : mnew;
-                alpha[h] = ex2(m[h] - base[h]);
-                m[h] = mnew;
-                l[h] *= alpha[h];
-            }
-            if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-                for (int dt = 0; dt < DT; ++dt) {
-                    o[dt][0] *= alpha[0];
-                    o[dt][1] *= alpha[0];
-                    o[dt][2] *= alpha[1];
-                    o[dt][3] *= alpha[1];
-                }
-            }
-#pragma unroll
-            for (int kk = 0; kk < NT / 2; ++kk) {
-                float p[2][4];
-#pragma unroll
-                for (int u = 0; u < 2; ++u)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        p[u][c] = ex2(sc[2 * kk + u][c] - base[c >> 1]);
-                        l[c >> 1] += p[u][c];
-                    }
-                const uint32_t pa[4] = {bf16x2(p[0][0], p[0][1]), bf16x2(p[0][2], p[0][3]),
-                                        bf16x2(p[1][0], p[1][1]), bf16x2(p[1][2], p[1][3])};
-#pragma unroll
-                for (int dp = 0; dp < DT / 2; ++dp) {
-                    uint32_t vb4[4];
-                    ldsm_x4_trans(vb4, vb + kk * 16 * RS + dp * 32);
-                    mma16816(o[2 * dp], pa, vb4[0], vb4[1]);
-                    mma16816(o[2 * dp + 1], pa, vb4[2], vb4[3]);
-                }
-            }
-        }
-        __syncthreads();  // this buffer is refilled two chunks later
-    }
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (wcol0 >= ncols) return;
-
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int c = wcol0 + gq + 8 * h;
-        if (c >= ncols) continue;
-        const int lim_c = v.base + col_token(a, c);
-        if (tok_begin > lim_c) continue;  // this partition holds nothing the column sees
-        const int64_t pair = (int64_t)(v.row0 + col_token(a, c)) * a.Hq + kvh * a.G + col_head(a, c);
-        if (lim_c < a.part_tokens) {
-            const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
-            uint16_t *dst = a.out + pair * D + 2 * t;
-#pragma unroll
-            for (int dt = 0; dt < DT; ++dt)
-                *reinterpret_cast<uint32_t *>(dst + dt * 8) = bf16x2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
-        } else {
-            const int64_t prow = pair * a.max_parts + part;
-            float *dst = a.ws_acc + prow * D + 2 * t;
-#pragma unroll
-            for (int dt = 0; dt < DT; ++dt)
-                *reinterpret_cast<float2 *>(dst + dt * 8) = make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
-            if (t == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(m[h], l[h]);
-        }
-    }
-}
-
 template <int D, int BS>
 cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
     constexpr int SMEM = multi_smem_bytes<D>();
-    constexpr int PSMEM = prefill_smem_bytes<D>();
     static bool configured[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(paged_multi_kernel<D, BS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(paged_prefill_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
-    // a full CTA of columns per kv head: the prefill layout; few columns: token slices
-    if ((int64_t)a.max_query_len * a.G >= kColsPerCta)
-        paged_prefill_kernel<D, BS><<<grid, kThreads, PSMEM, stream>>>(a);
-    else
-        paged_multi_kernel<D, BS><<<grid, kThreads, SMEM, stream>>>(a);
+    paged_multi_kernel<D, BS><<<grid, kThreads, SMEM, stream>>>(a);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || a.max_parts == 1) return err;
     cudaLaunchConfig_t cfg = {};
