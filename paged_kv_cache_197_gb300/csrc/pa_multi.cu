@@ -16,8 +16,10 @@
 // row's max over the 4 lanes that hold it and each column masked at its own
 // position, then O += P V with P's accumulators reused as the A operand.  Warps are
 // (column group, token slice) pairs: with 5..8 groups a warp takes whole chunks;
-// with fewer columns (draft tokens) 2 or 4 warps split each chunk of a group, and
-// the slices are joined by log-sum-exp in shared memory before a column is written.
+// with up to four groups (draft tokens) two warps split each chunk of a group (32
+// tokens each: narrower slices cost more per token than the idle warps they would
+// employ), and the slices are joined by log-sum-exp in shared memory before a column
+// is written.
 // Long contexts are split into partitions (grid x); a column whose visible tokens
 // span one partition is finished in place, the others leave (max, sum, output)
 // partials that a second kernel joins by log-sum-exp.
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     // warps = (group of 16 columns, token slice)
     const int ncg = (min(ncols - col0, kColsPerCta) + kColsPerWarp - 1) / kColsPerWarp;
     const int P2 = ncg <= 1 ? 1 : ncg <= 2 ? 2 : ncg <= 4 ? 4 : 8;
-    const int slices = min(4, kWarps / P2);
+    const int slices = min(2, kWarps / P2);  // a slice keeps >= 32 tokens per step
     const int grp = warp % P2, slice = warp / P2;
     const bool active = grp < ncg && slice < slices;
     const int width = kChunk / slices;  // tokens of a chunk per slice
@@ -297,10 +299,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
             const bool full = tok0 + width - 1 <= warp_lo;  // every row sees all: no mask
             if (slices == 1)
                 attend_tokens<D, 8>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
-            else if (slices == 2)
-                attend_tokens<D, 4>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
             else
-                attend_tokens<D, 2>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
+                attend_tokens<D, 4>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
         }
         __syncthreads();  // this buffer is refilled two chunks later
     }
