@@ -64,7 +64,8 @@ NCU_TRAFFIC = {
     ("gqa70b", "626bf5ea96dcc516"): 655776512 + 5093888,
     ("int8", "626bf5ea96dcc516"): 3144355840 + 5534208,
     ("fp8", "626bf5ea96dcc516"): 3144595456 + 5257216,
-    ("verify70b", "5304df044b4257f6"): 656960768 + 23457024,
+    ("verify70b", "a049483ec87ff4c6"): 656778496 + 18600448,
+    ("prefill8b", "a049483ec87ff4c6"): 84009472 + 88355072,
 }
 
 
@@ -371,7 +372,9 @@ def run_ours(args, rank, world, device) -> dict | None:
                    "l2": "flushed before each step" if flush is not None else
                          "K/V pools far larger than L2 (no flush needed)",
                    "bytes_per_step": nbytes},
-        "tokens_per_s_per_layer": round(case.S * world / (ms_per_step * 1e-3), 1),
+        # tokens attended per second: one per sequence in decode, every new token in a
+        # multi-token step
+        "tokens_per_s_per_layer": round(case.q.shape[0] * world / (ms_per_step * 1e-3), 1),
         "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
