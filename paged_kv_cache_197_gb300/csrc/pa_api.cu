@@ -332,6 +332,8 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
     return check_launch(fn);
 }
 
+constexpr int kShortOwnTokens = 1024;
+
 // Workspace of the shared-prefix decode: per-sequence start and group, prefix
 // partials per 128-token chunk, own-token partials per partition.
 struct PrefixPlan {
@@ -348,6 +350,11 @@ static PrefixPlan plan_prefix(int S, int Hq, int Hkv, int D, int bs, int kv_dtyp
     // own ranges (shorter prefixes, sequences in no group) just take more partitions
     const int own_len = std::max(1, max_context_len - max_prefix_len);
     p.own = plan_decode(S, Hq, Hkv, D, bs, kv_dtype, own_len);
+    // short own ranges run next to the grouped prefix kernel, which fills the GPU as
+    // well: one partition each (one partial per head for the merge) beats splitting
+    // them further (measured: 512-token ranges 48.8 us in one, 52.9 us in 256-token
+    // partitions, 59.0 us in 128-token ones)
+    if (own_len <= kShortOwnTokens) p.own.part_tokens = own_len;
     p.own.part_tokens = (int)align_up((size_t)p.own.part_tokens, 64);  // whole tiles and blocks
     p.MP = std::max(1, (max_context_len + p.own.part_tokens - 1) / p.own.part_tokens);
     const int chunk = prefix_chunk_tokens();

@@ -120,8 +120,8 @@ def test_shared_prefix_workspace_and_checks(lib):
     """Workspace of the prefix-aware decode: S int32 group ids and S start offsets, then
     (D + 2) fp32 per query head and 128-token prefix chunk, then (D + 2) fp32 per query
     head and own-token partition; partitions sized for max_context_len - max_prefix_len
-    (rounded up to 64 tokens), counted over max_context_len; each region 256-byte
-    aligned.  Host checks refuse what the kernels do not take."""
+    (one partition when that is at most 1024 tokens; rounded up to 64 tokens), counted
+    over max_context_len; each region 256-byte aligned.  Host checks refuse what the kernels do not take."""
     import paged_kv_cache_197_gb300 as pa
 
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
@@ -129,7 +129,9 @@ def test_shared_prefix_workspace_and_checks(lib):
             (50, 32, 8, 128, 16, 2512, 50, 2000), (8, 4, 4, 64, 32, 1372, 8, 672),
             (5, 8, 2, 128, 16, 9000, 1, 0), (56, 64, 16, 64, 32, 1005, 40, 640)]:
         units = S * Hkv * ((Hq // Hkv + 7) // 8)
-        pt = -(-part_tokens(units, max(1, max_ctx - max_prefix)) // 64) * 64
+        own = max(1, max_ctx - max_prefix)
+        pt = own if own <= 1024 else part_tokens(units, own)
+        pt = -(-pt // 64) * 64
         MP = max(1, -(-max_ctx // pt))
         PP = -(-max_prefix // 128)
         pre, own = S * Hq * PP, S * Hq * MP
