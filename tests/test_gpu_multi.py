@@ -120,3 +120,105 @@ def test_rejects_unsupported():
         pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, case.block_tables,
                                     case.context_lens, case.query_start, case.scale, 40, 41)
     torch.cuda.synchronize()
+
+
+def test_block_permutation_bit_identical():
+    """The result depends on logical order only: moving blocks changes no bit."""
+    case = workloads.build_multi_case("perm", S=4, Hq=16, Hkv=4, D=128, bs=16,
+                                      context_lens=[40, 700, 1300, 90], query_lens=[3, 8, 140, 1],
+                                      seed=36, poison=False)
+    a = helpers.gpu_multi_step(case, DEV)["out"]
+    pi = torch.randperm(case.N, generator=torch.Generator().manual_seed(5))
+    moved = workloads.PagedCase(**{**case.__dict__})
+    moved.k_pool = torch.empty_like(case.k_pool)
+    moved.v_pool = torch.empty_like(case.v_pool)
+    moved.k_pool[pi] = case.k_pool
+    moved.v_pool[pi] = case.v_pool
+    moved.block_tables = pi[case.block_tables.long()].to(torch.int32)
+    slots = case.slot_mapping.clone()
+    ok = slots >= 0
+    moved.slot_mapping = torch.where(ok, pi[(slots // case.bs).clamp(min=0)] * case.bs + slots % case.bs, slots)
+    b = helpers.gpu_multi_step(moved, DEV)["out"]
+    assert torch.equal(a, b)
+
+
+def test_error_flags():
+    """A block id beyond the pool is skipped (read as zeros) and flagged; a context past
+    max_context_len is clamped and flagged."""
+    import paged_kv_cache_197_gb300 as pa
+
+    case = workloads.build_multi_case("flags", S=2, Hq=8, Hkv=2, D=64, bs=16, context_lens=[90, 300],
+                                      query_lens=[4, 5], seed=37, poison=False).to(DEV)
+    out = torch.empty_like(case.q)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tables = case.block_tables.clone()
+    tables[1, 2] = case.N + 7
+    pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, tables, case.context_lens,
+                                case.query_start, case.scale, 300, 5, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == pa.PA_FLAG_BLOCK_OUT_OF_RANGE
+    assert torch.isfinite(out.float()).all()
+    flag.zero_()
+    pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, case.block_tables,
+                                case.context_lens, case.query_start, case.scale, 200, 5, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == pa.PA_FLAG_CONTEXT_OUT_OF_RANGE
+
+
+def test_graph_capture_replays():
+    """The call captured in a CUDA graph (with its merge launched as a programmatic
+    dependent) replays to the same bits as the eager call."""
+    import paged_kv_cache_197_gb300 as pa
+
+    case = workloads.build_multi_case("graph", S=3, Hq=16, Hkv=2, D=128, bs=16,
+                                      context_lens=[5000, 9000, 300], query_lens=[4, 2, 150],
+                                      seed=38, poison=False).to(DEV)
+    max_ctx, max_q = 9000, 150
+    n = pa.pa_multi_token_workspace_size(case.S, case.q.shape[0], case.Hq, case.Hkv, case.D, case.bs,
+                                         pa.PA_KV_BF16, max_ctx, max_q)
+    assert n > 0  # the contexts are split: the merge kernel is part of the call
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    eager = torch.empty_like(case.q)
+    call = lambda out: pa.pa_multi_token_attention(  # noqa: E731
+        out, case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens,
+        case.query_start, case.scale, max_ctx, max_q, workspace=ws)
+    call(eager)
+    torch.cuda.synchronize()
+    replay = torch.full_like(case.q, float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(replay)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager, replay)
+
+
+def _sequences(case, seqs):
+    """The case cut to the listed sequences (their query rows, tables and lengths)."""
+    qs = case.query_start.cpu().tolist()
+    rows = torch.cat([torch.arange(qs[s], qs[s + 1]) for s in seqs])
+    sub = workloads.PagedCase(**{**case.__dict__})
+    sub.q = case.q.cpu()[rows]
+    sub.block_tables = case.block_tables.cpu()[seqs]
+    sub.context_lens = case.context_lens.cpu()[seqs]
+    starts = [0]
+    for s in seqs:
+        starts.append(starts[-1] + qs[s + 1] - qs[s])
+    sub.query_start = torch.tensor(starts, dtype=torch.int32)
+    sub.S = len(seqs)
+    return sub, rows
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["verify70b", "prefill8b"])
+def test_full_size_sampled(oracle, name):
+    """The full-size multi-token workloads in the launch configuration bench.py times,
+    checked on a sample of sequences."""
+    case = workloads.CONFIGS[name](device="cpu", poison=True)
+    got = helpers.gpu_multi_step(case, DEV)
+    assert got["flag"] == 0
+    caches = helpers.oracle_caches(case, oracle)
+    seqs = [0, case.S - 1]
+    sub, rows = _sequences(case, seqs)
+    ref = helpers.oracle_multi_out(sub, oracle, caches)
+    helpers.compare(got["out"][rows.to(DEV)], ref, "bf16")

@@ -144,3 +144,32 @@ def test_full_prefix_workload_sampled(oracle):
     seqs = [0, 7, 23, 49]
     ref = helpers.oracle_out(case, oracle, caches, seqs)
     helpers.compare(got["out"][torch.as_tensor(seqs, device=DEV)], ref, "bf16")
+
+
+def test_graph_capture_replays():
+    """The shared-prefix call captured in a CUDA graph -- its side-stream fork and join
+    become graph edges -- replays to the same bits as the eager call."""
+    import paged_kv_cache_197_gb300 as pa
+
+    prefix = 21 * 32
+    lens = [prefix + o for o in (3, 40, 300, 900)]
+    case = workloads.build_case("pfx-graph", S=4, Hq=32, Hkv=8, D=128, bs=16, context_lens=lens,
+                                seed=16, prefix_tokens=prefix, poison=False).to(DEV)
+    gs = torch.tensor([0, 4], dtype=torch.int32, device=DEV)
+    gp = torch.tensor([prefix], dtype=torch.int32, device=DEV)
+    max_ctx = max(lens)
+    n = pa.pa_decode_shared_prefix_workspace_size(4, 32, 8, 128, 16, pa.PA_KV_BF16, max_ctx, 4, prefix)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    call = lambda out: pa.pa_decode_shared_prefix(  # noqa: E731
+        out, case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens, case.scale,
+        max_ctx, gs, gp, 4, prefix, workspace=ws)
+    eager = torch.empty_like(case.q)
+    call(eager)  # the first call on a device creates the side stream, outside the capture
+    torch.cuda.synchronize()
+    replay = torch.full_like(case.q, float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(replay)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager, replay)
