@@ -112,26 +112,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// int8 -> fp16, exactly.  The fp16 bit pattern 0x64XX is 1024 + XX for XX in
+// int8 -> fp16, biased.  The fp16 bit pattern 0x64XX is 1024 + XX for XX in
 // [0, 255]; with XX = x + 128 (the int8 byte with its top bit flipped) the value is
-// 1152 + x, and subtracting 1152 leaves x.
-__device__ __forceinline__ uint32_t biased_to_f16x2(uint32_t t) {
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&t), __half2half2(__ushort_as_half(0x6480)));
-    return *reinterpret_cast<const uint32_t *>(&r);
-}
+// 1152 + x, exactly.  The tensor-core products take these biased values and the bias
+// is taken out of their fp32 results instead: a score loses kInt8Bias * sum_d q_d
+// (fixed per head), an output element kInt8Bias * sum_t p_t over the fp16 weights
+// fed to the product -- one subtraction per result rather than one per converted
+// pair.
+constexpr float kInt8Bias = 1152.0f;
 
-// The four int8 values of word w (one K row) as the fp16 pairs (w0, w1), (w2, w3).
+// The four int8 values of word w (one K row) as the biased fp16 pairs (w0, w1), (w2, w3).
 __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
     const uint32_t u = w ^ 0x80808080u;
-    lo = biased_to_f16x2(__byte_perm(u, 0x64646464u, 0x4140));
-    hi = biased_to_f16x2(__byte_perm(u, 0x64646464u, 0x4342));
+    lo = __byte_perm(u, 0x64646464u, 0x4140);
+    hi = __byte_perm(u, 0x64646464u, 0x4342);
 }
 
-// Byte 0 and byte 2 of t hold int8 values a and b (bytes 1 and 3 are ignored):
-// the fp16 pair (a, b).  One logic op flips the top bits and writes the 0x64 bytes.
+// Byte 0 and byte 2 of t hold int8 values a and b (bytes 1 and 3 are ignored): the
+// biased fp16 pair (a, b).  One logic op flips the top bits and writes the 0x64 bytes.
 __device__ __forceinline__ uint32_t i8pair_to_f16x2(uint32_t t) {
     const uint32_t m = 0x00ff00ffu, c = 0x64806480u;
-    return biased_to_f16x2((m & (t ^ c)) | (~m & c));
+    return (m & (t ^ c)) | (~m & c);
 }
 
 // fp8 (e4m3) cache entries: every e4m3 value is exactly an fp16 value, and the
@@ -205,6 +206,8 @@ struct Geo {
     static constexpr int MT = D / 16;              // d tiles of the output product
     static constexpr int SUB = TILE / 16;          // 16-token sub-tiles
     static constexpr int QW = D / 8;               // q words per lane
+    // int8 entries enter the products biased by kInt8Bias (fp8 ones are exact)
+    static constexpr bool BIASED = std::is_same<KV, int8_t>::value;
     static_assert(K_CHUNKS >= 1 && V_BYTES >= 8, "unsupported head_dim / dtype");
 };
 
@@ -286,12 +289,13 @@ struct WarpState {
     float m[2];          // running max of heads 2t, 2t+1 (log2 units)
     float l[2];          // running sum, partial over this lane's tokens
     int ve;              // int8: O is kept in units of 2^ve (ve >= exponent of every value scale so far)
+    float ps[2];         // int8: sum of the fp16 weights fed to the value product, heads 2t, 2t+1
 };
 
 template <typename KV, int D, int TILE>
 __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
                                              Tile<Geo<KV, D, TILE>> &R, const uint32_t *qw,
-                                             float scale_log2, int g, int t) {
+                                             const float (&qb)[2], float scale_log2, int g, int t) {
     using G_ = Geo<KV, D, TILE>;
     // ---- scores S[token][head] for the tile's 16-token sub-tiles
     float sc[G_::SUB][4];
@@ -322,7 +326,7 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int tok = 16 * s + g + 8 * (c >> 1);
-            float v = sc[s][c] * scale_log2;
+            float v = (G_::BIASED ? sc[s][c] - qb[c & 1] : sc[s][c]) * scale_log2;
             if constexpr (G_::ELEM == 1) v *= __shfl_sync(0xffffffffu, R.ks, tok);
             v = tok < R.nvalid ? v : -INFINITY;
             x[s][c] = v;
@@ -352,6 +356,10 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
         }
         st.l[0] *= alpha[0];
         st.l[1] *= alpha[1];
+        if constexpr (G_::BIASED) {
+            st.ps[0] *= alpha[0];
+            st.ps[1] *= alpha[1];
+        }
     }
     // int8: keep the weights p * v_scale below 1 in fp16 by working in units of 2^ve,
     // ve the exponent of the largest value scale seen so far (O rescaled when it grows)
@@ -370,6 +378,10 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
                     st.o[mt][1] *= f;
                     st.o[mt][2] *= f;
                     st.o[mt][3] *= f;
+                }
+                if constexpr (G_::BIASED) {
+                    st.ps[0] *= f;
+                    st.ps[1] *= f;
                 }
                 st.ve = e;
             }
@@ -403,8 +415,15 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
             b0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
             b1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
         } else {
-            b0 = movmatrix_trans(pack_f16x2(p[0], p[1]));
-            b1 = movmatrix_trans(pack_f16x2(p[2], p[3]));
+            const uint32_t w0 = pack_f16x2(p[0], p[1]), w1 = pack_f16x2(p[2], p[3]);
+            if constexpr (G_::BIASED) {  // the weights exactly as the product sees them
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w0));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w1));
+                st.ps[0] += f0.x + f1.x;
+                st.ps[1] += f0.y + f1.y;
+            }
+            b0 = movmatrix_trans(w0);
+            b1 = movmatrix_trans(w1);
         }
         const int j0 = 4 * s;  // V rows 2t, 2t+1, 2t+8, 2t+9 of this sub-tile
 #pragma unroll
@@ -486,6 +505,7 @@ paged_decode_kernel(const DecodeArgs a) {
         for (int i = 0; i < G_::QW; ++i) qw[i] = 0u;
     }
     float scale_log2 = a.scale_log2;
+    float qb[2] = {0.0f, 0.0f};  // int8: score bias per score column
     if constexpr (G_::ELEM == 1) {
         // fp16 q for the int8 products: scaled by 2^sig so the largest |q| of the CTA's
         // heads lands in [2^13, 2^14); the scores are scaled back by 2^-sig
@@ -501,6 +521,20 @@ paged_decode_kernel(const DecodeArgs a) {
         for (int i = 0; i < G_::QW; ++i)
             qw[i] = pack_f16x2(__uint_as_float(qw[i] << 16) * up, __uint_as_float(qw[i] & 0xffff0000u) * up);
         scale_log2 *= ldexpf(1.0f, -sig);
+        if constexpr (G_::BIASED) {
+            // kInt8Bias * sum_d q_d of the fp16 q fed to the score product, for the
+            // heads of this lane's score columns (2t, 2t+1; head g sits in lanes 4g..)
+            float part = 0.0f;
+#pragma unroll
+            for (int i = 0; i < G_::QW; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qw[i]));
+                part += f.x + f.y;
+            }
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            qb[0] = kInt8Bias * __shfl_sync(0xffffffffu, part, 8 * t);
+            qb[1] = kInt8Bias * __shfl_sync(0xffffffffu, part, 8 * t + 4);
+        }
     }
     __syncthreads();
 
@@ -509,6 +543,7 @@ paged_decode_kernel(const DecodeArgs a) {
     for (int mt = 0; mt < G_::MT; ++mt) st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.0f;
+    st.ps[0] = st.ps[1] = 0.0f;
     st.ve = -1000;  // no value scale seen yet
 
     const int ntiles = (tok_end - tok_begin + TILE - 1) / TILE;
@@ -518,12 +553,12 @@ paged_decode_kernel(const DecodeArgs a) {
     while (i < ntiles) {
         if (i + kWarps < ntiles)
             load_tile<KV, D, BS, TILE>(B, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE>(st, A, qw, scale_log2, g, t);
+        consume_tile<KV, D, TILE>(st, A, qw, qb, scale_log2, g, t);
         i += kWarps;
         if (i >= ntiles) break;
         if (i + kWarps < ntiles)
             load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE>(st, B, qw, scale_log2, g, t);
+        consume_tile<KV, D, TILE>(st, B, qw, qb, scale_log2, g, t);
         i += kWarps;
     }
 
@@ -545,11 +580,22 @@ paged_decode_kernel(const DecodeArgs a) {
         s_l[warp][2 * t + 1] = st.l[1];
     }
     const float oscale = (G_::ELEM == 1 && st.ve > -200) ? ldexpf(1.0f, st.ve) : 1.0f;
+    float obias[2] = {0.0f, 0.0f};  // int8: kInt8Bias * the weights summed over all tokens
+    if constexpr (G_::BIASED) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float v = st.ps[j];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            obias[j] = kInt8Bias * v;
+        }
+    }
 #pragma unroll
     for (int mt = 0; mt < G_::MT; ++mt)
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-            s_o[warp][2 * t + (c & 1)][out_dim<G_::ELEM, D>(mt, g, c >> 1)] = st.o[mt][c] * oscale;
+            s_o[warp][2 * t + (c & 1)][out_dim<G_::ELEM, D>(mt, g, c >> 1)] = (st.o[mt][c] - obias[c & 1]) * oscale;
     __syncthreads();
 
     constexpr int DPT = D / 16;  // output values per thread: 16 threads per head
