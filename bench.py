@@ -53,8 +53,10 @@ DESCRIPTIONS = {
                  "(causal among them), 64/8 heads, head_dim 128, block 16",
     "prefill8b": "chunked prefill, Llama-3-8B shape: 4 seqs x 512-token chunk on 3584 cached tokens, "
                  "32/8 heads, head_dim 128, block 16",
+    "verify70b_fp8": "the draft-verification workload with an fp8 (e4m3) cache and per-token scales",
+    "prefill8b_fp8": "the chunked-prefill workload with an fp8 (e4m3) cache and per-token scales",
 }
-FLUSH_L2 = {"tiny", "prefix", "prefill8b"}
+FLUSH_L2 = {"tiny", "prefix", "prefill8b", "prefill8b_fp8"}
 L2_BYTES = 126 * 1024 * 1024
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
@@ -241,7 +243,8 @@ class Step:
             self.pa.pa_multi_token_attention(
                 out, q, self.k_cache, self.v_cache, tables, lens,
                 self.case.query_start if query_start is None else query_start, self.case.scale,
-                self.max_ctx, self.max_q, workspace=self.ws, err_flag=self.flag, stream=self.stream)
+                self.max_ctx, self.max_q, workspace=self.ws, k_scale=self.k_scale,
+                v_scale=self.v_scale, err_flag=self.flag, stream=self.stream)
             return
         if self.prefix:
             self.pa.pa_decode_shared_prefix(out, q, self.k_cache, self.v_cache, tables, lens,

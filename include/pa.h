@@ -254,7 +254,12 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
  *                   L_s > context_lens[s] is skipped with PA_FLAG_QUERY_OUT_OF_RANGE.
  *   workspace       pa_multi_token_workspace_size(...) bytes (NULL when that is 0);
  *                   contents not preserved.
- * bf16 caches only (PA_ERR_UNSUPPORTED otherwise); other arguments as pa_decode.
+ * bf16, int8 and fp8 caches (k_scale, v_scale required for the last two); other
+ * arguments as pa_decode.  8-bit entries are dequantised on their way through shared
+ * memory as fp16 code x scale (the scale rounded to fp16, the product rounded once),
+ * the query rows as fp16 scaled by a power of two per row; the products are fp16 with
+ * fp32 accumulation.  The dequantised values must lie within fp16's range (|x| <=
+ * 65504, the scale above fp16's smallest normal 2^-14 for full precision).
  */
 size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
                                      int max_context_len, int max_query_len);

@@ -364,8 +364,8 @@ def pa_multi_token_workspace_size(S: int, T: int, Hq: int, Hkv: int, D: int, bs:
 
 def pa_multi_token_attention(out, query, k_cache, v_cache, block_tables, context_lens,
                              query_start, scale: float, max_context_len: int,
-                             max_query_len: int, workspace=None, err_flag=None,
-                             stream=None) -> None:
+                             max_query_len: int, workspace=None, k_scale=None, v_scale=None,
+                             err_flag=None, stream=None) -> None:
     """Several new tokens per sequence attend the paged cache, each up to its own
     position: query/out [T][Hq][D] bf16, sequence s owning rows
     query_start[s] .. query_start[s+1]-1.  workspace defaults to a fresh allocation."""
@@ -377,6 +377,11 @@ def pa_multi_token_attention(out, query, k_cache, v_cache, block_tables, context
     _cuda(block_tables, "block_tables", torch.int32, 2)
     _cuda(context_lens, "context_lens", torch.int32, 1)
     _cuda(query_start, "query_start", torch.int32, 1)
+    if kv_dtype != PA_KV_BF16:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an int8 or fp8 cache needs k_scale and v_scale")
+        _cuda(k_scale, "k_scale", torch.float32, 3)
+        _cuda(v_scale, "v_scale", torch.float32, 3)
     T, Hq, D = query.shape
     N, Hkv, bs, D2 = k_cache.shape
     S = context_lens.shape[0]
@@ -394,8 +399,8 @@ def pa_multi_token_attention(out, query, k_cache, v_cache, block_tables, context
         ws_bytes = workspace.numel() * workspace.element_size()
     lib = load_library()
     _check(lib.pa_multi_token_attention(
-        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), None, None, kv_dtype,
-        _ptr(block_tables), M, _ptr(context_lens), _ptr(query_start), S, T, Hq, Hkv, D, bs, N,
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        kv_dtype, _ptr(block_tables), M, _ptr(context_lens), _ptr(query_start), S, T, Hq, Hkv, D, bs, N,
         float(scale), int(max_context_len), int(max_query_len), _ptr(workspace), ws_bytes,
         _flag(err_flag), _stream(stream, query.device)))
 

@@ -526,8 +526,6 @@ static pa_status check_multi_args(const char *fn, int S, int T, int Hq, int Hkv,
                                   int kv_dtype, int max_context_len, int max_query_len) {
     pa_status st = check_decode_shape(fn, S, Hq, Hkv, D, bs, kv_dtype, max_context_len);
     if (st != PA_OK) return st;
-    if (kv_dtype != PA_KV_BF16)
-        return fail(PA_ERR_UNSUPPORTED, "%s: only bf16 caches are supported", fn);
     if (T < 0) return fail(PA_ERR_INVALID_ARG, "%s: T = %d", fn, T);
     if (max_query_len < 1 || max_query_len > max_context_len || max_query_len > T)
         return fail(PA_ERR_INVALID_ARG, "%s: max_query_len = %d (1 .. min(T, max_context_len))", fn,
@@ -557,8 +555,6 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
                                    void *stream) {
     const char *fn = "pa_multi_token_attention";
     g_last_error[0] = 0;
-    (void)k_scale;
-    (void)v_scale;
     if (S == 0 || T == 0) return PA_OK;
     pa_status st = check_multi_args(fn, S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len);
     if (st != PA_OK) return st;
@@ -569,6 +565,8 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
                     max_context_len, (long long)M * bs);
     if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
         return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (kv_dtype != PA_KV_BF16 && (!k_scale || !v_scale))
+        return fail(PA_ERR_INVALID_ARG, "%s: an int8 or fp8 cache needs k_scale and v_scale", fn);
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
     if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
@@ -584,6 +582,8 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
     a.q = query;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.query_start = query_start;
@@ -604,7 +604,7 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
     a.max_context_len = max_context_len;
     a.max_query_len = max_query_len;
     a.scale_log2 = scale * 1.4426950408889634f;
-    launch_multi_token(a, D, bs, (cudaStream_t)stream);
+    launch_multi_token(a, D, bs, kv_dtype, (cudaStream_t)stream);
     return check_launch(fn);
 }
 

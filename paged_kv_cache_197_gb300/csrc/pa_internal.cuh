@@ -74,6 +74,7 @@ struct MultiArgs {
     uint16_t *out;                 // [T][Hq][D] bf16
     const uint16_t *q;             // [T][Hq][D] bf16
     const void *k_cache, *v_cache;
+    const float *k_scale, *v_scale;  // int8 / fp8 caches: [N][Hkv][bs]
     const int32_t *block_tables, *context_lens;
     const int32_t *query_start;    // [S + 1]: rows of sequence s
     float *ws_acc, *ws_ml;         // [T][Hq][max_parts][D], [T][Hq][max_parts][2]
@@ -87,7 +88,7 @@ struct MultiArgs {
 };
 
 int multi_cols_per_cta();
-cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, cudaStream_t stream);
+cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream);
 
 // ------------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing was launched).

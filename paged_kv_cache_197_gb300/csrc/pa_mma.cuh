@@ -3,6 +3,7 @@
 // tensor-core product, movmatrix and exp2.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace pa {
@@ -15,6 +16,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 // 16-byte global -> shared copy; src_bytes 0 fills the destination with zeros.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// 4-byte global -> shared copy (L1-allocating); src_bytes 0 writes a zero.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
 }
 
@@ -65,6 +72,15 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Two e4m3 codes (low byte first) as an fp16 pair; every e4m3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(out)
+        : "r"(pair16));
+    return out;
 }
 
 }  // namespace tiled

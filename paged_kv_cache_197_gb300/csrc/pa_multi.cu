@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "pa_internal.cuh"
 #include "pa_mma.cuh"
 
@@ -33,6 +35,10 @@ namespace pa {
 namespace {
 
 using namespace tiled;
+
+struct e4m3_tag {  // an fp8 (e4m3) cache entry
+    uint8_t bits;
+};
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
@@ -87,6 +93,20 @@ __host__ __device__ constexpr int multi_smem_bytes() {
     // K and V stages, then the query rows; the slice join reuses the stages
     return 4 * kChunk * (2 * D + 16) + kColsPerCta * (2 * D + 16);
 }
+
+// 8-bit caches: raw codes of a chunk (K then V) as copied from the cache
+template <int D>
+__host__ __device__ constexpr int raw_chunk_bytes() {
+    return 2 * kChunk * D;
+}
+
+// 8-bit caches: one fp16 K and V stage, the query rows, two raw chunks
+template <int D>
+__host__ __device__ constexpr int multi_smem_bytes_q() {
+    return 2 * kChunk * (2 * D + 16) + kColsPerCta * (2 * D + 16) + 2 * raw_chunk_bytes<D>();
+}
+static_assert(kWarps * kColsPerWarp * (128 + 4) * 4 <= 2 * kChunk * (2 * 128 + 16) + kColsPerCta * (2 * 128 + 16),
+              "the join fits the stage and query rows");
 static_assert(kWarps * kColsPerWarp * (128 + 4) * 4 <= 4 * kChunk * (2 * 128 + 16), "join fits the stages");
 
 // One online-softmax step of a warp over NTW 8-token n-tiles of a staged chunk:
@@ -169,17 +189,151 @@ __device__ __forceinline__ void attend_tokens(float (&o)[D / 8][4], float (&m)[2
     }
 }
 
-template <int D, int BS>
+// 8-bit caches: sixteen codes of one row times the row's scale, as sixteen fp16 (two
+// 16-byte words).  The codes become exact fp16 first -- int8 through the fp16 pattern
+// 0x64XX = 1024 + XX with XX = x + 128, less 1152; fp8 (e4m3) by the hardware
+// conversion (every e4m3 value is an fp16 value) -- then one fp16 multiply by the
+// scale (rounded to fp16) per pair.
+template <typename KV>
+__device__ __forceinline__ void codes_to_f16(const uint4 &c, float scale, uint4 &lo, uint4 &hi) {
+    const __half2 sc2 = __float2half2_rn(scale);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<KV, int8_t>::value) {
+            const uint32_t u = w[i] ^ 0x80808080u;
+            const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+            const uint32_t b0 = __byte_perm(u, 0x64646464u, 0x4140), b1 = __byte_perm(u, 0x64646464u, 0x4342);
+            const __half2 h0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b0), bias), sc2);
+            const __half2 h1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b1), bias), sc2);
+            out[2 * i] = *reinterpret_cast<const uint32_t *>(&h0);
+            out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+        } else {
+            const uint32_t e0 = e4m3x2_to_f16x2(w[i] & 0xffffu), e1 = e4m3x2_to_f16x2(w[i] >> 16);
+            const __half2 h0 = __hmul2(*reinterpret_cast<const __half2 *>(&e0), sc2);
+            const __half2 h1 = __hmul2(*reinterpret_cast<const __half2 *>(&e1), sc2);
+            out[2 * i] = *reinterpret_cast<const uint32_t *>(&h0);
+            out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+        }
+    }
+    lo = make_uint4(out[0], out[1], out[2], out[3]);
+    hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+__device__ __forceinline__ void mma16816_f16(float *c, const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Exponent e with |x| < 2^e for a finite, positive, normal x.
+__device__ __forceinline__ int exponent_above(float x) {
+    return (int)((__float_as_uint(x) >> 23) & 0xffu) - 126;
+}
+
+// The step of attend_tokens for 8-bit caches: K and V rows are fp16 (code x scale),
+// the query rows fp16 scaled by a power of two per row (rs[h] = softmax scale x 2^-sig
+// of row gq + 8h), the weights fp16; products f16 with fp32 accumulation.
+template <int D, int NTW>
+__device__ __forceinline__ void attend_tokens_q(float (&o)[D / 8][4], float (&m)[2], float (&l)[2],
+                                                uint32_t qaddr, uint32_t kb, uint32_t vb, int tok0,
+                                                bool full, const int (&lim)[2], const float (&rs)[2], int t) {
+    constexpr int RS = 2 * D + 16;
+    constexpr int KC = D / 16;
+    constexpr int DT = D / 8;
+    float sc[NTW][4];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int kc = 0; kc < KC; ++kc) {
+        uint32_t qa[4];
+        ldsm_x4(qa, qaddr + kc * 32);
+#pragma unroll
+        for (int np = 0; np < NTW / 2; ++np) {
+            uint32_t kb4[4];
+            ldsm_x4(kb4, kb + np * 16 * RS + kc * 32);
+            mma16816_f16(sc[2 * np], qa, kb4[0], kb4[1]);
+            mma16816_f16(sc[2 * np + 1], qa, kb4[2], kb4[3]);
+        }
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float x = sc[nt][c] * rs[c >> 1];
+            if (!full) {
+                const int tok = tok0 + nt * 8 + 2 * t + (c & 1);
+                x = tok <= lim[c >> 1] ? x : -INFINITY;
+            }
+            sc[nt][c] = x;
+            mx[c >> 1] = fmaxf(mx[c >> 1], x);
+        }
+    float base[2], alpha[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float mnew = fmaxf(m[h], mx[h]);
+        base[h] = mnew == -INFINITY ? 0.f : mnew;
+        alpha[h] = ex2(m[h] - base[h]);
+        m[h] = mnew;
+        l[h] *= alpha[h];
+    }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+            o[dt][0] *= alpha[0];
+            o[dt][1] *= alpha[0];
+            o[dt][2] *= alpha[1];
+            o[dt][3] *= alpha[1];
+        }
+    }
+#pragma unroll
+    for (int kk = 0; kk < NTW / 2; ++kk) {
+        float p[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                p[u][c] = ex2(sc[2 * kk + u][c] - base[c >> 1]);
+                l[c >> 1] += p[u][c];
+            }
+        const uint32_t pa[4] = {f16x2(p[0][0], p[0][1]), f16x2(p[0][2], p[0][3]),
+                                f16x2(p[1][0], p[1][1]), f16x2(p[1][2], p[1][3])};
+#pragma unroll
+        for (int dp = 0; dp < DT / 2; ++dp) {
+            uint32_t vb4[4];
+            ldsm_x4_trans(vb4, vb + kk * 16 * RS + dp * 32);
+            mma16816_f16(o[2 * dp], pa, vb4[0], vb4[1]);
+            mma16816_f16(o[2 * dp + 1], pa, vb4[2], vb4[3]);
+        }
+    }
+}
+
+template <typename KV, int D, int BS>
 __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_constant__ MultiArgs a) {
+    constexpr bool QUANT = sizeof(KV) == 1;  // int8 / fp8 cache: fp16 code x scale, fp16 products
     constexpr int ROW = D * 2;          // bytes of one token row (bf16)
     constexpr int RS = ROW + 16;        // padded shared-memory row stride
     constexpr int STAGE = kChunk * RS;  // one K (or V) stage
     constexpr int CPR = ROW / 16;       // 16-byte pieces per row
     constexpr int DT = D / 8;           // 8-wide d-tiles of O
     constexpr int PER = D / 32;         // values per lane in the join
-    extern __shared__ __align__(128) unsigned char smem[];  // K0 K1 V0 V1 Q
+    extern __shared__ __align__(128) unsigned char smem[];  // K0 K1 V0 V1 Q (8-bit: K V Q raw0 raw1)
     __shared__ int s_blk[kMaxPartBlocks];
     __shared__ float s_ml[kWarps][kColsPerWarp][2];  // each warp's (max, sum) per row
+    // 8-bit caches: each query row's softmax scale x 2^-sig (its fp16 copy is scaled
+    // by 2^sig)
+    __shared__ float s_qs[QUANT ? kColsPerCta : 1];
 
     const int part = blockIdx.x;
     const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
@@ -206,19 +360,53 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
         }
         s_blk[i] = b;
     }
-    unsigned char *ks = smem, *vs = smem + 2 * STAGE, *qs = smem + 4 * STAGE;
+    unsigned char *ks = smem, *vs = smem + (QUANT ? 1 : 2) * STAGE, *qs = smem + (QUANT ? 2 : 4) * STAGE;
+    unsigned char *raw = qs + kColsPerCta * RS;  // 8-bit caches only
     // the CTA's query rows, one per column (zeros past the last column)
-    for (int i = tid; i < kColsPerCta * CPR; i += kThreads) {
-        const int r = i / CPR, pc = i % CPR;
-        const int c = col0 + r;
-        const void *src = a.q;
-        uint32_t bytes = 0;
-        if (c < ncols) {
-            const int64_t row = v.row0 + col_token(a, c);
-            src = reinterpret_cast<const char *>(a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D) + pc * 16;
-            bytes = 16;
+    if constexpr (!QUANT) {
+        for (int i = tid; i < kColsPerCta * CPR; i += kThreads) {
+            const int r = i / CPR, pc = i % CPR;
+            const int c = col0 + r;
+            const void *src = a.q;
+            uint32_t bytes = 0;
+            if (c < ncols) {
+                const int64_t row = v.row0 + col_token(a, c);
+                src = reinterpret_cast<const char *>(a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D) + pc * 16;
+                bytes = 16;
+            }
+            cp_async16(smem_u32(qs + r * RS + pc * 16), src, bytes);
         }
-        cp_async16(smem_u32(qs + r * RS + pc * 16), src, bytes);
+    } else {
+        // as fp16 scaled by 2^sig per row, sig putting the row's largest |q| in
+        // [2^13, 2^14); the CPR threads of a row are consecutive lanes of one warp
+        for (int i = tid; i < kColsPerCta * CPR; i += kThreads) {
+            const int r = i / CPR, pc = i % CPR;
+            const int c = col0 + r;
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (c < ncols) {
+                const int64_t row = v.row0 + col_token(a, c);
+                raw = __ldg(reinterpret_cast<const uint4 *>(a.q + (row * a.Hq + kvh * a.G + col_head(a, c)) * D) + pc);
+            }
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            float f[8], amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = __uint_as_float(w[e] << 16);
+                f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(f[2 * e]), fabsf(f[2 * e + 1])));
+            }
+#pragma unroll
+            for (int off = CPR / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+            const int sig = amax > 0.f ? min(100, max(-100, 14 - exponent_above(amax))) : 0;
+            const float up = ldexpf(1.f, sig);
+            uint4 h;
+            h.x = f16x2(f[0] * up, f[1] * up);
+            h.y = f16x2(f[2] * up, f[3] * up);
+            h.z = f16x2(f[4] * up, f[5] * up);
+            h.w = f16x2(f[6] * up, f[7] * up);
+            *reinterpret_cast<uint4 *>(qs + r * RS + pc * 16) = h;
+            if (pc == 0) s_qs[r] = a.scale_log2 * ldexpf(1.f, -sig);
+        }
     }
 
     // warps = (group of 16 columns, token slice)
@@ -240,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     const int warp_lo = (active && wcol0 < ncols) ? min(v.base + col_token(a, wcol0), tok_end - 1) : -1;
     __syncthreads();  // s_blk
 
-    // staging: thread tid always copies 16-byte piece pc of rows pr, pr + RPP, ... of a
-    // chunk, for K and for V; a (block, kv head) is BS contiguous rows in the cache
+    // staging (bf16): thread tid always copies 16-byte piece pc of rows pr, pr + RPP, ...
+    // of a chunk, for K and for V; a (block, kv head) is BS contiguous rows in the cache
     constexpr int RPP = kThreads / CPR;
     constexpr int PASSES = kChunk / RPP;
     const int pc = tid % CPR, pr = tid / CPR;
@@ -283,26 +471,108 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     const uint32_t vrow = (slice * width + (lane & 7) + (((lane >> 3) & 1) << 3)) * RS + (lane >> 4) * 16;
 
     const int nchunks = (tok_end - tok_begin + kChunk - 1) / kChunk;
-    stage_chunk(0, 0);  // first group: the query rows and chunk 0
-    for (int j = 0; j < nchunks; ++j) {
-        if (j + 1 < nchunks) {
-            stage_chunk(j + 1, (j + 1) & 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
+    float rs[2] = {0.f, 0.f};  // 8-bit caches: the rows' softmax scale x 2^-sig
+    auto attend_chunk = [&](int j) {
         const int tok0 = tok_begin + j * kChunk + slice * width;
         if (tok0 <= warp_hi) {  // warp-uniform (inactive warps have warp_hi = -1)
-            const uint32_t kb = smem_u32(ks + (j & 1) * STAGE) + krow;
-            const uint32_t vb = smem_u32(vs + (j & 1) * STAGE) + vrow;
+            const int buf = QUANT ? 0 : (j & 1);
+            const uint32_t kb = smem_u32(ks + buf * STAGE) + krow;
+            const uint32_t vb = smem_u32(vs + buf * STAGE) + vrow;
             const bool full = tok0 + width - 1 <= warp_lo;  // every row sees all: no mask
-            if (slices == 1)
-                attend_tokens<D, 8>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
-            else
-                attend_tokens<D, 4>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
+            if constexpr (QUANT) {
+                if (slices == 1)
+                    attend_tokens_q<D, 8>(o, m, l, qaddr, kb, vb, tok0, full, lim, rs, t);
+                else
+                    attend_tokens_q<D, 4>(o, m, l, qaddr, kb, vb, tok0, full, lim, rs, t);
+            } else {
+                if (slices == 1)
+                    attend_tokens<D, 8>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
+                else
+                    attend_tokens<D, 4>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
+            }
         }
-        __syncthreads();  // this buffer is refilled two chunks later
+    };
+    if constexpr (!QUANT) {
+        stage_chunk(0, 0);  // first group: the query rows and chunk 0
+        for (int j = 0; j < nchunks; ++j) {
+            if (j + 1 < nchunks) {
+                stage_chunk(j + 1, (j + 1) & 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            __syncthreads();
+            attend_chunk(j);
+            __syncthreads();  // this buffer is refilled two chunks later
+        }
+    } else {
+        // 8-bit caches: the next chunk's codes are copied raw (cp.async) into the other
+        // of two raw buffers, and its rows' scales loaded into registers, while the
+        // current chunk is computed; each thread then converts the pieces it copied
+        // itself (its own completed copies need no barrier) to fp16, code x scale, in the
+        // single K and V stage.
+        constexpr int QPR = D / 16;                  // 16-code pieces per row
+        constexpr int NPT = kChunk * QPR / kThreads;  // pieces per thread and chunk
+        const char *kc8 = static_cast<const char *>(a.k_cache), *vc8 = static_cast<const char *>(a.v_cache);
+        float ksr[NPT], vsr[NPT];
+        auto issue_raw = [&](int j, int b) {
+            const int c0 = tok_begin + j * kChunk;
+            unsigned char *rb = raw + b * raw_chunk_bytes<D>();
+#pragma unroll
+            for (int k = 0; k < NPT; ++k) {
+                const int i = tid + k * kThreads, r = i / QPR, qc = i % QPR;
+                const int tok = c0 + r;
+                const char *ksrc = kc8, *vsrc = vc8;
+                uint32_t bytes = 0;
+                ksr[k] = vsr[k] = 0.f;
+                if (tok < tok_end) {
+                    const int blk = s_blk[tok / BS - blk0];
+                    if (blk >= 0) {
+                        const int64_t row = ((int64_t)blk * a.Hkv + kvh) * BS + tok % BS;
+                        ksrc += row * D + qc * 16;
+                        vsrc += row * D + qc * 16;
+                        ksr[k] = __ldg(a.k_scale + row);
+                        vsr[k] = __ldg(a.v_scale + row);
+                        bytes = 16;
+                    }
+                }
+                cp_async16(smem_u32(rb + r * D + qc * 16), ksrc, bytes);
+                cp_async16(smem_u32(rb + kChunk * D + r * D + qc * 16), vsrc, bytes);
+            }
+            cp_async_commit();
+        };
+        auto convert_raw = [&](int b) {
+            const unsigned char *rb = raw + b * raw_chunk_bytes<D>();
+#pragma unroll
+            for (int k = 0; k < NPT; ++k) {
+                const int i = tid + k * kThreads, r = i / QPR, qc = i % QPR;
+                uint4 lo, hi;
+                codes_to_f16<KV>(*reinterpret_cast<const uint4 *>(rb + r * D + qc * 16), ksr[k], lo, hi);
+                uint4 *kd = reinterpret_cast<uint4 *>(ks + r * RS + qc * 32);
+                kd[0] = lo;
+                kd[1] = hi;
+                codes_to_f16<KV>(*reinterpret_cast<const uint4 *>(rb + kChunk * D + r * D + qc * 16), vsr[k], lo, hi);
+                uint4 *vd = reinterpret_cast<uint4 *>(vs + r * RS + qc * 32);
+                vd[0] = lo;
+                vd[1] = hi;
+            }
+        };
+        issue_raw(0, 0);
+        cp_async_wait<0>();
+        convert_raw(0);
+        __syncthreads();  // query rows, row scales, chunk 0
+        rs[0] = s_qs[grp * 16 + gq];
+        rs[1] = s_qs[grp * 16 + gq + 8];
+        for (int j = 0; j < nchunks; ++j) {
+            if (j + 1 < nchunks) issue_raw(j + 1, (j + 1) & 1);
+            attend_chunk(j);
+            __syncthreads();  // the stage is free
+            if (j + 1 < nchunks) {
+                cp_async_wait<0>();
+                convert_raw((j + 1) & 1);
+            }
+            __syncthreads();  // chunk j + 1 staged
+        }
     }
     // the merge grid may launch now (it still waits for this grid before reading)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -449,20 +719,20 @@ __global__ void __launch_bounds__(128) merge_multi_kernel(const __grid_constant_
     for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t *>(dst + e) = bf16x2(acc[e] * inv, acc[e + 1] * inv);
 }
 
-template <int D, int BS>
+template <typename KV, int D, int BS>
 cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
-    constexpr int SMEM = multi_smem_bytes<D>();
+    constexpr int SMEM = sizeof(KV) == 1 ? multi_smem_bytes_q<D>() : multi_smem_bytes<D>();
     static bool configured[64] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(paged_multi_kernel<D, BS>,
+        cudaError_t e = cudaFuncSetAttribute(paged_multi_kernel<KV, D, BS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
-    paged_multi_kernel<D, BS><<<grid, kThreads, SMEM, stream>>>(a);
+    paged_multi_kernel<KV, D, BS><<<grid, kThreads, SMEM, stream>>>(a);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || a.max_parts == 1) return err;
     cudaLaunchConfig_t cfg = {};
@@ -481,10 +751,17 @@ cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
 
 int multi_cols_per_cta() { return kColsPerCta; }
 
-cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, cudaStream_t stream) {
+template <typename KV>
+cudaError_t launch_multi_kv(const MultiArgs &a, int D, int bs, cudaStream_t stream) {
     if (D == 128)
-        return bs == 16 ? launch_multi_typed<128, 16>(a, stream) : launch_multi_typed<128, 32>(a, stream);
-    return bs == 16 ? launch_multi_typed<64, 16>(a, stream) : launch_multi_typed<64, 32>(a, stream);
+        return bs == 16 ? launch_multi_typed<KV, 128, 16>(a, stream) : launch_multi_typed<KV, 128, 32>(a, stream);
+    return bs == 16 ? launch_multi_typed<KV, 64, 16>(a, stream) : launch_multi_typed<KV, 64, 32>(a, stream);
+}
+
+cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
+    if (kv_dtype == PA_KV_INT8) return launch_multi_kv<int8_t>(a, D, bs, stream);
+    if (kv_dtype == PA_KV_FP8) return launch_multi_kv<e4m3_tag>(a, D, bs, stream);
+    return launch_multi_kv<uint16_t>(a, D, bs, stream);
 }
 
 }  // namespace pa

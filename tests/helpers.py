@@ -138,8 +138,26 @@ def gpu_multi_step(case: workloads.PagedCase, device, max_query_len=None, max_co
 
     c = case.to(device)
     flag = torch.zeros(1, dtype=torch.int32, device=device)
-    k_cache, v_cache = c.k_pool.clone(), c.v_pool.clone()
-    pa.pa_reshape_and_cache(c.new_key, c.new_value, k_cache, v_cache, c.slot_mapping, err_flag=flag)
+    k_scale = v_scale = None
+    if case.kv_dtype == "bf16":
+        k_cache, v_cache = c.k_pool.clone(), c.v_pool.clone()
+        pa.pa_reshape_and_cache(c.new_key, c.new_value, k_cache, v_cache, c.slot_mapping,
+                                err_flag=flag)
+    else:  # quantise the pool, poison the scales of empty slots as the oracle does, append
+        N, Hkv, bs, D = case.k_pool.shape
+        fp8 = case.kv_dtype == "fp8"
+        quant = pa.pa_quantize_kv_fp8 if fp8 else pa.pa_quantize_kv
+        k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.uint8 if fp8 else torch.int8, device=device)
+        v_cache = torch.empty_like(k_cache)
+        k_scale = torch.empty((N, Hkv, bs), dtype=torch.float32, device=device)
+        v_scale = torch.empty_like(k_scale)
+        quant(int8_pool_rows(c.k_pool), int8_pool_rows(c.v_pool), k_cache, v_cache, k_scale, v_scale,
+              torch.arange(N * bs, dtype=torch.int64, device=device), err_flag=flag)
+        bad = ~workloads.valid_slot_mask(case.meta["content_tables"], case.context_lens - 1,
+                                         case.bs, case.N).to(device)
+        k_scale.permute(0, 2, 1)[bad] = float("nan")
+        v_scale.permute(0, 2, 1)[bad] = float("nan")
+        quant(c.new_key, c.new_value, k_cache, v_cache, k_scale, v_scale, c.slot_mapping, err_flag=flag)
     if max_context_len is None:
         max_context_len = int(case.context_lens.max())
     if max_query_len is None:
@@ -147,9 +165,10 @@ def gpu_multi_step(case: workloads.PagedCase, device, max_query_len=None, max_co
     out = torch.full_like(c.q, float("nan"))
     pa.pa_multi_token_attention(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens,
                                 c.query_start, case.scale, max_context_len, max_query_len,
-                                err_flag=flag)
+                                k_scale=k_scale, v_scale=v_scale, err_flag=flag)
     torch.cuda.synchronize(device)
-    return dict(out=out, k_cache=k_cache, v_cache=v_cache, flag=int(flag.item()))
+    return dict(out=out, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
+                flag=int(flag.item()))
 
 
 def oracle_multi_out(case, orc, caches) -> np.ndarray:

@@ -211,7 +211,8 @@ def test_multi_token_workspace_and_checks(lib):
         **{**dict(S=4, T=64, Hq=8, Hkv=2, D=128, bs=16, kv_dtype=0, max_context_len=8000,
                   max_query_len=16), **k})
     assert ws() > 0
-    assert ws(kv_dtype=pa.PA_KV_INT8) == 0
+    assert ws(kv_dtype=pa.PA_KV_INT8) == ws() and ws(kv_dtype=pa.PA_KV_FP8) == ws()
+    assert ws(kv_dtype=7) == 0
     assert ws(max_query_len=0) == 0
     assert ws(max_query_len=65) == 0  # more than T rows
     fake = 1 << 20
@@ -221,7 +222,8 @@ def test_multi_token_workspace_and_checks(lib):
                                             S, T, 8, 2, 128, 16, 4, 0.1, max_ctx, max_q, ws, ws_bytes,
                                             None, None)
 
-    assert call(kv=pa.PA_KV_FP8) == pa.PA_ERR_UNSUPPORTED
+    assert call(kv=pa.PA_KV_FP8) == pa.PA_ERR_INVALID_ARG  # scales missing
+    assert call(kv=5) == pa.PA_ERR_UNSUPPORTED
     assert call(qs=None) == pa.PA_ERR_INVALID_ARG
     assert call(max_q=9) == pa.PA_ERR_INVALID_ARG       # above T
     assert call(max_ctx=65) == pa.PA_ERR_OUT_OF_RANGE   # above M * bs

@@ -25,8 +25,13 @@ def _library():
 def _run(case, orc, expect_flag=0, **kw):
     got = helpers.gpu_multi_step(case, DEV, **kw)
     caches = helpers.oracle_caches(case, orc)
-    assert np.array_equal(helpers.bits(got["k_cache"]), caches[0])
-    assert np.array_equal(helpers.bits(got["v_cache"]), caches[1])
+    if case.kv_dtype == "bf16":
+        assert np.array_equal(helpers.bits(got["k_cache"]), caches[0])
+        assert np.array_equal(helpers.bits(got["v_cache"]), caches[1])
+    else:
+        assert np.array_equal(got["k_cache"].cpu().numpy(), caches[0])
+        assert np.array_equal(got["v_cache"].cpu().numpy(), caches[1])
+        assert np.array_equal(got["k_scale"].cpu().numpy().view(np.uint32), caches[2].view(np.uint32))
     assert got["flag"] == expect_flag
     ref = helpers.oracle_multi_out(case, orc, caches)
     rows = helpers.covered_rows(case)
@@ -34,39 +39,43 @@ def _run(case, orc, expect_flag=0, **kw):
     if other.size:  # rows of no sequence are not written
         assert torch.isnan(got["out"][torch.as_tensor(other, device=DEV)].float()).all()
     idx = torch.as_tensor(rows, device=DEV)
-    return helpers.compare(got["out"][idx], ref[rows], "bf16")
+    return helpers.compare(got["out"][idx], ref[rows], case.kv_dtype)
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("D,bs,Hq,Hkv", [(128, 16, 32, 8), (64, 32, 8, 8), (128, 32, 16, 2),
                                           (64, 16, 20, 2), (128, 16, 64, 8)])
-def test_draft_verification(oracle, D, bs, Hq, Hkv):
+def test_draft_verification(oracle, D, bs, Hq, Hkv, kv_dtype):
     """A few new tokens per sequence on contexts from one token up, including a
     sequence whose whole context is new and one with a single new token."""
     lens = [1, 5, 17, 100, 513, 1300, 2100]
     qlen = [1, 5, 4, 8, 3, 1, 7]
     case = workloads.build_multi_case(f"verify-{D}-{bs}-{Hq}-{Hkv}", S=len(lens), Hq=Hq, Hkv=Hkv,
                                       D=D, bs=bs, context_lens=lens, query_lens=qlen,
-                                      seed=3 * D + bs + Hq, row_offset=2, extra_rows=3)
+                                      seed=3 * D + bs + Hq, row_offset=2, extra_rows=3,
+                                      kv_dtype=kv_dtype)
     _run(case, oracle)
 
 
-def test_prefill_chunks(oracle):
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
+def test_prefill_chunks(oracle, kv_dtype):
     """Long chunks (several CTAs of columns per kv head): a prompt's first chunk, a
     later chunk on top of cached tokens and a chunk of one token."""
     lens = [300, 1000, 77]
     qlen = [300, 260, 1]
     case = workloads.build_multi_case("prefill", S=3, Hq=16, Hkv=4, D=128, bs=16, context_lens=lens,
-                                      query_lens=qlen, seed=31)
+                                      query_lens=qlen, seed=31, kv_dtype=kv_dtype)
     _run(case, oracle)
 
 
-def test_long_context_partitions(oracle):
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
+def test_long_context_partitions(oracle, kv_dtype):
     """Few sequences with long contexts: the context is split into partitions that a
     second kernel merges; columns of one chunk straddle partition boundaries."""
     lens = [9000, 4097, 6000]
     qlen = [4, 64, 2]
     case = workloads.build_multi_case("long", S=3, Hq=8, Hkv=2, D=128, bs=16, context_lens=lens,
-                                      query_lens=qlen, seed=32)
+                                      query_lens=qlen, seed=32, kv_dtype=kv_dtype)
     _run(case, oracle)
 
 
@@ -113,7 +122,7 @@ def test_rejects_unsupported():
                                       query_lens=[2, 2], seed=35).to(DEV)
     out = torch.empty_like(case.q)
     i8 = torch.zeros(case.k_pool.shape, dtype=torch.int8, device=DEV)
-    with pytest.raises(pa.PagedAttentionError):
+    with pytest.raises(ValueError):  # an int8 cache without its scales
         pa.pa_multi_token_attention(out, case.q, i8, i8, case.block_tables, case.context_lens,
                                     case.query_start, case.scale, 40, 2)
     with pytest.raises(pa.PagedAttentionError):  # max_query_len above the context bound

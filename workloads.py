@@ -184,7 +184,8 @@ def valid_slot_mask(tables: torch.Tensor, lengths: torch.Tensor, bs: int, N: int
 
 def build_multi_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, context_lens,
                      query_lens, seed: int, pool_blocks: int | None = None, poison: bool = True,
-                     device="cpu", row_offset: int = 0, extra_rows: int = 0) -> PagedCase:
+                     device="cpu", row_offset: int = 0, extra_rows: int = 0,
+                     kv_dtype: str = "bf16") -> PagedCase:
     """A multi-token step: sequence s brings query_lens[s] new tokens at positions
     context_lens[s] - query_lens[s] .. context_lens[s] - 1 (context_lens count them).
     q, new_key, new_value and slot_mapping hold T rows, sequence s owning rows
@@ -196,7 +197,7 @@ def build_multi_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, cont
     ctx = [int(c) for c in context_lens]
     assert len(L) == S and all(0 <= l <= c for l, c in zip(L, ctx))
     case = build_case(name, S=S, Hq=Hq, Hkv=Hkv, D=D, bs=bs, context_lens=ctx, seed=seed,
-                      pool_blocks=pool_blocks, poison=False, device=device)
+                      pool_blocks=pool_blocks, poison=False, device=device, kv_dtype=kv_dtype)
     qs = [row_offset]
     for l in L:
         qs.append(qs[-1] + l)
@@ -211,7 +212,7 @@ def build_multi_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, cont
         for i in range(L[s_]):
             pos = ctx[s_] - L[s_] + i
             slots[qs[s_] + i] = int(tables[s_, pos // bs]) * bs + pos % bs
-    if poison:
+    if poison and kv_dtype == "bf16":  # quantised sources stay finite: tests poison their scales
         before = torch.tensor([c - l for c, l in zip(ctx, L)], dtype=torch.int64)
         bad = ~valid_slot_mask(case.meta["content_tables"], before, bs, case.N).to(device)
         nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16).view(torch.bfloat16).item()
@@ -265,23 +266,35 @@ def fp8(seed: int = 5, device="cpu", poison=False) -> PagedCase:
                       seed=seed, kv_dtype="fp8", poison=poison, device=device)
 
 
-def verify70b(seed: int = 6, device="cpu", poison=False) -> PagedCase:
+def verify70b(seed: int = 6, device="cpu", poison=False, kv_dtype="bf16") -> PagedCase:
     """Draft verification on the 70B-shaped GQA batch: 4 new tokens per sequence on
     8000-token contexts (the 4 included)."""
     return build_multi_case("verify70b", S=20, Hq=64, Hkv=8, D=128, bs=16, context_lens=[8000] * 20,
                             query_lens=[4] * 20, seed=seed, pool_blocks=10000, poison=poison,
-                            device=device)
+                            device=device, kv_dtype=kv_dtype)
 
 
-def prefill8b(seed: int = 7, device="cpu", poison=False) -> PagedCase:
+def prefill8b(seed: int = 7, device="cpu", poison=False, kv_dtype="bf16") -> PagedCase:
     """Chunked prefill, Llama-3-8B shape: 4 sequences each attending a 512-token chunk
     on top of 3584 cached tokens."""
     return build_multi_case("prefill8b", S=4, Hq=32, Hkv=8, D=128, bs=16, context_lens=[4096] * 4,
-                            query_lens=[512] * 4, seed=seed, poison=poison, device=device)
+                            query_lens=[512] * 4, seed=seed, poison=poison, device=device,
+                            kv_dtype=kv_dtype)
+
+
+def verify70b_fp8(seed: int = 6, device="cpu", poison=False) -> PagedCase:
+    """The draft-verification workload with an fp8 (e4m3) cache."""
+    return verify70b(seed, device, poison, kv_dtype="fp8")
+
+
+def prefill8b_fp8(seed: int = 7, device="cpu", poison=False) -> PagedCase:
+    """The chunked-prefill workload with an fp8 (e4m3) cache."""
+    return prefill8b(seed, device, poison, kv_dtype="fp8")
 
 
 CONFIGS = {"tiny": tiny, "mha13b": mha13b, "gqa70b": gqa70b, "prefix": prefix, "int8": int8, "fp8": fp8,
-           "verify70b": verify70b, "prefill8b": prefill8b}
+           "verify70b": verify70b, "prefill8b": prefill8b, "verify70b_fp8": verify70b_fp8,
+           "prefill8b_fp8": prefill8b_fp8}
 
 
 # ------------------------------------------------------------------ byte accounting
