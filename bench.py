@@ -66,8 +66,10 @@ NCU_TRAFFIC = {
     ("gqa70b", "0a92d8beb0508d47"): 655764224 + 5198848,
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
     ("fp8", "0a92d8beb0508d47"): 3144265472 + 5437952,
-    ("verify70b", "a049483ec87ff4c6"): 656778496 + 18600448,
-    ("prefill8b", "a049483ec87ff4c6"): 84009472 + 88355072,
+    ("verify70b", "c25396a67b4994d3"): 656778752 + 18288896,
+    ("prefill8b", "c25396a67b4994d3"): 84117504 + 88478976,
+    ("verify70b_fp8", "c25396a67b4994d3"): 339649792 + 19931392,
+    ("prefill8b_fp8", "c25396a67b4994d3"): 51451904 + 84611072,
 }
 
 
