@@ -89,14 +89,14 @@ __device__ __forceinline__ int find_group_warp(const int (&off)[4], int n_groups
 // the group's first member lands in the same group and holds the prefix, and its
 // table repeats the first member's prefix blocks, all of them inside the pool; a
 // member joined to g thus implies that the first member is joined to g too.  With up
-// to 127 groups and 128 prefix blocks the warp needs two rounds of loads.
+// to 127 groups and 128 prefix blocks the warp needs two batches of dependent loads.
 __global__ void __launch_bounds__(256) prefix_setup_kernel(const __grid_constant__ DecodeArgs a,
                                                            const __grid_constant__ PrefixArgs p, int bs) {
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (s >= a.S) return;
     const int32_t *row = a.block_tables + (int64_t)s * a.M;
-    // round 1: the group offsets, this sequence's length and first table entries
+    // first batch of loads: the group offsets, this sequence's length and first table entries
     int off[4], mine[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) prefix_setup_kernel(const __grid_constant
             hi = p.group_start[g + 1];
         }
         const bool lo_ok = lo >= 0 && lo < hi && hi <= a.S;
-        // round 2: the prefix length, the first member's length and table entries
+        // second batch of loads: the prefix length, the first member's length and table entries
         const int plen = p.group_prefix[g];
         const int32_t *lead = a.block_tables + (int64_t)(lo_ok ? lo : s) * a.M;
         int theirs[4];
