@@ -216,7 +216,10 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
  *                     prefixes (multiple of bs, <= max_context_len).
  *   workspace         pa_decode_shared_prefix_workspace_size(...) bytes; contents
  *                     not preserved.
- * bf16 caches only (PA_ERR_UNSUPPORTED otherwise).
+ * bf16, int8 and fp8 caches (k_scale, v_scale as for pa_decode).  With an 8-bit cache
+ * the shared prefix is staged as fp16 code x scale and attended with fp16 products
+ * (values within fp16's range); the members' own tokens go through pa_decode's exact
+ * path.
  */
 size_t pa_decode_shared_prefix_workspace_size(int S, int Hq, int Hkv, int D, int bs, int kv_dtype,
                                               int max_context_len, int max_group_size,

@@ -320,7 +320,7 @@ def pa_decode_shared_prefix_workspace_size(S: int, Hq: int, Hkv: int, D: int, bs
 def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_lens,
                             scale: float, max_context_len: int, group_start, group_prefix_len,
                             max_group_size: int, max_prefix_len: int, workspace=None,
-                            err_flag=None, stream=None) -> None:
+                            k_scale=None, v_scale=None, err_flag=None, stream=None) -> None:
     """Paged decode of a batch whose groups of consecutive sequences share prefix blocks;
     the same result as pa_decode.  group_start [n_groups + 1] and group_prefix_len
     [n_groups] are int32 device tensors; workspace defaults to a fresh allocation."""
@@ -333,6 +333,11 @@ def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_
     _cuda(context_lens, "context_lens", torch.int32, 1)
     _cuda(group_start, "group_start", torch.int32, 1)
     _cuda(group_prefix_len, "group_prefix_len", torch.int32, 1)
+    if kv_dtype != PA_KV_BF16:
+        if k_scale is None or v_scale is None:
+            raise ValueError("an int8 or fp8 cache needs k_scale and v_scale")
+        _cuda(k_scale, "k_scale", torch.float32, 3)
+        _cuda(v_scale, "v_scale", torch.float32, 3)
     S, Hq, D = query.shape
     N, Hkv, bs, D2 = k_cache.shape
     M = block_tables.shape[1]
@@ -349,8 +354,8 @@ def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_
     ws_bytes = workspace.numel() * workspace.element_size()
     lib = load_library()
     _check(lib.pa_decode_shared_prefix(
-        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), None, None, kv_dtype,
-        _ptr(block_tables), M, _ptr(context_lens), S, Hq, Hkv, D, bs, N, float(scale),
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        kv_dtype, _ptr(block_tables), M, _ptr(context_lens), S, Hq, Hkv, D, bs, N, float(scale),
         int(max_context_len), _ptr(group_start), _ptr(group_prefix_len), n_groups,
         int(max_group_size), int(max_prefix_len), _ptr(workspace), ws_bytes, _flag(err_flag),
         _stream(stream, query.device)))

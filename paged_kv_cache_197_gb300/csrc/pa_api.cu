@@ -376,8 +376,6 @@ static pa_status check_prefix_args(const char *fn, int S, int Hq, int Hkv, int D
                                    int max_prefix_len) {
     pa_status st = check_decode_shape(fn, S, Hq, Hkv, D, bs, kv_dtype, max_context_len);
     if (st != PA_OK) return st;
-    if (kv_dtype != PA_KV_BF16)
-        return fail(PA_ERR_UNSUPPORTED, "%s: only bf16 caches are supported", fn);
     if (n_groups < 0 || n_groups > 65535)
         return fail(PA_ERR_INVALID_ARG, "%s: n_groups = %d", fn, n_groups);
     if (max_prefix_len < 0 || max_prefix_len % bs != 0 || max_prefix_len > max_context_len)
@@ -410,8 +408,6 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
                                   void *stream) {
     const char *fn = "pa_decode_shared_prefix";
     g_last_error[0] = 0;
-    (void)k_scale;
-    (void)v_scale;
     if (S == 0) return PA_OK;
     pa_status st = check_prefix_args(fn, S, Hq, Hkv, D, bs, kv_dtype, max_context_len, n_groups,
                                       max_group_size, max_prefix_len);
@@ -425,6 +421,8 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
         return fail(PA_ERR_INVALID_ARG, "%s: null pointer", fn);
     if (n_groups > 0 && (!group_start || !group_prefix_len))
         return fail(PA_ERR_INVALID_ARG, "%s: group arrays missing", fn);
+    if (kv_dtype != PA_KV_BF16 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale)))
+        return fail(PA_ERR_INVALID_ARG, "%s: an int8 or fp8 cache needs 16-byte aligned k_scale and v_scale", fn);
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
     if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
@@ -442,6 +440,8 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
     a.q = query;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.ws_acc = (float *)(ws + plan.acc_off);
@@ -472,7 +472,7 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
     p.pml = (float *)(ws + plan.pml_off);
     p.PP = plan.PP;
     p.CB = plan.CB;
-    launch_decode_shared_prefix(a, p, D, bs, (cudaStream_t)stream);
+    launch_decode_shared_prefix(a, p, D, bs, kv_dtype, (cudaStream_t)stream);
     return check_launch(fn);
 }
 

@@ -66,7 +66,7 @@ struct PrefixArgs {
 
 int prefix_chunk_tokens();
 int prefix_cols_per_cta();
-cudaError_t launch_decode_shared_prefix(const DecodeArgs &a, const PrefixArgs &p, int D, int bs,
+cudaError_t launch_decode_shared_prefix(const DecodeArgs &a, const PrefixArgs &p, int D, int bs, int kv_dtype,
                                         cudaStream_t stream);
 
 // Multi-token attention: the newest L_s tokens of each sequence attend the cache.

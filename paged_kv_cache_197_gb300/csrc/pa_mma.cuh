@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace pa {
 namespace tiled {
 
@@ -81,6 +83,60 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
         : "=r"(out)
         : "r"(pair16));
     return out;
+}
+
+struct e4m3_tag {  // an fp8 (e4m3) cache entry
+    uint8_t bits;
+};
+
+// 8-bit caches: sixteen codes of one row times the row's scale, as sixteen fp16 (two
+// 16-byte words).  The codes become exact fp16 first -- int8 through the fp16 pattern
+// 0x64XX = 1024 + XX with XX = x + 128, less 1152; fp8 (e4m3) by the hardware
+// conversion (every e4m3 value is an fp16 value) -- then one fp16 multiply by the
+// scale (rounded to fp16) per pair.
+template <typename KV>
+__device__ __forceinline__ void codes_to_f16(const uint4 &c, float scale, uint4 &lo, uint4 &hi) {
+    const __half2 sc2 = __float2half2_rn(scale);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<KV, int8_t>::value) {
+            const uint32_t u = w[i] ^ 0x80808080u;
+            const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+            const uint32_t b0 = __byte_perm(u, 0x64646464u, 0x4140), b1 = __byte_perm(u, 0x64646464u, 0x4342);
+            const __half2 h0 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b0), bias), sc2);
+            const __half2 h1 = __hmul2(__hsub2(*reinterpret_cast<const __half2 *>(&b1), bias), sc2);
+            out[2 * i] = *reinterpret_cast<const uint32_t *>(&h0);
+            out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+        } else {
+            const uint32_t e0 = e4m3x2_to_f16x2(w[i] & 0xffffu), e1 = e4m3x2_to_f16x2(w[i] >> 16);
+            const __half2 h0 = __hmul2(*reinterpret_cast<const __half2 *>(&e0), sc2);
+            const __half2 h1 = __hmul2(*reinterpret_cast<const __half2 *>(&e1), sc2);
+            out[2 * i] = *reinterpret_cast<const uint32_t *>(&h0);
+            out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+        }
+    }
+    lo = make_uint4(out[0], out[1], out[2], out[3]);
+    hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+__device__ __forceinline__ void mma16816_f16(float *c, const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Exponent e with |x| < 2^e for a finite, positive, normal x.
+__device__ __forceinline__ int exponent_above(float x) {
+    return (int)((__float_as_uint(x) >> 23) & 0xffu) - 126;
 }
 
 }  // namespace tiled

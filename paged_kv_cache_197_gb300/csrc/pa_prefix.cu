@@ -155,10 +155,13 @@ __global__ void __launch_bounds__(256) prefix_setup_kernel(const __grid_constant
 }
 
 // ---------------------------------------------------- 2. grouped prefix kernel
-template <int D, int BS>
+template <typename KV, int D, int BS>
 __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_constant__ DecodeArgs a,
                                                                   const __grid_constant__ PrefixArgs p) {
-    constexpr int ROW = D * 2;        // bytes of one token row (bf16)
+    // 8-bit caches: rows staged as fp16 code x scale, q as fp16 scaled by a power of two
+    // per column, fp16 products
+    constexpr bool QUANT = sizeof(KV) == 1;
+    constexpr int ROW = D * 2;        // bytes of one staged token row (bf16 or fp16)
     constexpr int RS = ROW + 16;      // padded shared-memory row stride
     constexpr int KC = D / 16;        // k-steps of the score product
     constexpr int MT = D / 16;        // d tiles of the output product
@@ -186,26 +189,61 @@ __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_c
     if (tid < (ntok + BS - 1) / BS) s_blk[tid] = a.block_tables[(int64_t)lo * a.M + tok0 / BS + tid];
     __syncthreads();
     // stage the chunk's K and V rows; rows past the prefix are zero-filled
-    constexpr int CPR = ROW / 16;  // 16-byte chunks per row
-    for (int i = tid; i < 2 * kPrefixChunk * CPR; i += kThreads) {
-        const int isv = i >= kPrefixChunk * CPR;
-        const int rem = isv ? i - kPrefixChunk * CPR : i;
-        const int r = rem / CPR, c = rem % CPR;
-        const void *src = a.k_cache;
-        uint32_t bytes = 0;
-        if (r < ntok) {
-            const int blk = s_blk[r / BS];
-            const int64_t row = ((int64_t)blk * a.Hkv + kvh) * BS + (tok0 + r) % BS;
-            src = static_cast<const char *>(isv ? a.v_cache : a.k_cache) + row * ROW + c * 16;
-            bytes = 16;
+    if constexpr (!QUANT) {
+        constexpr int CPR = ROW / 16;  // 16-byte chunks per row
+        for (int i = tid; i < 2 * kPrefixChunk * CPR; i += kThreads) {
+            const int isv = i >= kPrefixChunk * CPR;
+            const int rem = isv ? i - kPrefixChunk * CPR : i;
+            const int r = rem / CPR, c = rem % CPR;
+            const void *src = a.k_cache;
+            uint32_t bytes = 0;
+            if (r < ntok) {
+                const int blk = s_blk[r / BS];
+                const int64_t row = ((int64_t)blk * a.Hkv + kvh) * BS + (tok0 + r) % BS;
+                src = static_cast<const char *>(isv ? a.v_cache : a.k_cache) + row * ROW + c * 16;
+                bytes = 16;
+            }
+            cp_async16(smem_u32((isv ? vs : ks) + r * RS + c * 16), src, bytes);
         }
-        cp_async16(smem_u32((isv ? vs : ks) + r * RS + c * 16), src, bytes);
+        cp_async_wait_all();
+    } else {
+        // sixteen codes and the row's scale per piece, all loads issued before the
+        // conversions
+        constexpr int QPR = D / 16;                        // 16-code pieces per row
+        constexpr int NPT = kPrefixChunk * QPR / kThreads;  // pieces per thread
+        uint4 kr[NPT], vr[NPT];
+        float ksr[NPT], vsr[NPT];
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) {
+            const int i = tid + k * kThreads, r = i / QPR, qc = i % QPR;
+            kr[k] = vr[k] = make_uint4(0u, 0u, 0u, 0u);
+            ksr[k] = vsr[k] = 0.f;
+            if (r < ntok) {
+                const int blk = s_blk[r / BS];
+                const int64_t row = ((int64_t)blk * a.Hkv + kvh) * BS + (tok0 + r) % BS;
+                kr[k] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(a.k_cache) + row * D) + qc);
+                vr[k] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const char *>(a.v_cache) + row * D) + qc);
+                ksr[k] = __ldg(a.k_scale + row);
+                vsr[k] = __ldg(a.v_scale + row);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) {
+            const int i = tid + k * kThreads, r = i / QPR, qc = i % QPR;
+            uint4 lo, hi;
+            codes_to_f16<KV>(kr[k], ksr[k], lo, hi);
+            reinterpret_cast<uint4 *>(ks + r * RS + qc * 32)[0] = lo;
+            reinterpret_cast<uint4 *>(ks + r * RS + qc * 32)[1] = hi;
+            codes_to_f16<KV>(vr[k], vsr[k], lo, hi);
+            reinterpret_cast<uint4 *>(vs + r * RS + qc * 32)[0] = lo;
+            reinterpret_cast<uint4 *>(vs + r * RS + qc * 32)[1] = hi;
+        }
     }
-    cp_async_wait_all();
     __syncthreads();
 
     // this warp's 16 query columns (member, head) -> B fragments of q
     uint32_t qf[2][KC][2];
+    float csc[2][2];  // score scale of this lane's score columns 2t, 2t + 1 per n-tile
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int c = col0 + warp * kColsPerWarp + nt * 8 + gq;
@@ -221,6 +259,33 @@ __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_c
 #pragma unroll
             for (int kc = 0; kc < KC; ++kc) qf[nt][kc][0] = qf[nt][kc][1] = 0u;
         }
+        float colscale = a.scale_log2;  // of column nt * 8 + gq
+        if constexpr (QUANT) {
+            // fp16 q scaled by 2^sig, sig putting the column's largest |q| (spread over
+            // the 4 lanes of the quad) in [2^13, 2^14)
+            float amax = 0.f;
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc)
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    amax = fmaxf(amax, fabsf(__uint_as_float(qf[nt][kc][w] << 16)));
+                    amax = fmaxf(amax, fabsf(__uint_as_float(qf[nt][kc][w] & 0xffff0000u)));
+                }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int sig = amax > 0.f ? min(100, max(-100, 14 - exponent_above(amax))) : 0;
+            const float up = ldexpf(1.f, sig);
+#pragma unroll
+            for (int kc = 0; kc < KC; ++kc)
+#pragma unroll
+                for (int w = 0; w < 2; ++w)
+                    qf[nt][kc][w] = f16x2(__uint_as_float(qf[nt][kc][w] << 16) * up,
+                                          __uint_as_float(qf[nt][kc][w] & 0xffff0000u) * up);
+            colscale = a.scale_log2 * ldexpf(1.f, -sig);
+        }
+        // score column 2t + j is held (as column gq) by lanes 4 (2t + j) .. + 3
+        csc[nt][0] = __shfl_sync(0xffffffffu, colscale, 8 * t);
+        csc[nt][1] = __shfl_sync(0xffffffffu, colscale, 8 * t + 4);
     }
     if (col0 + warp * kColsPerWarp >= ncols) return;  // nothing for this warp (no more barriers)
 
@@ -247,8 +312,13 @@ __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_c
             for (int kc = 0; kc < KC; ++kc) {
                 uint32_t af[4];
                 ldsm_x4(af, rb + kc * 32);
-                mma16816(sc[0], af, qf[0][kc][0], qf[0][kc][1]);
-                mma16816(sc[1], af, qf[1][kc][0], qf[1][kc][1]);
+                if constexpr (QUANT) {
+                    mma16816_f16(sc[0], af, qf[0][kc][0], qf[0][kc][1]);
+                    mma16816_f16(sc[1], af, qf[1][kc][0], qf[1][kc][1]);
+                } else {
+                    mma16816(sc[0], af, qf[0][kc][0], qf[0][kc][1]);
+                    mma16816(sc[1], af, qf[1][kc][0], qf[1][kc][1]);
+                }
             }
         }
         uint32_t pb[2][2];
@@ -258,7 +328,7 @@ __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_c
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int tok = gq + 8 * (c >> 1);
-                x[c] = tok < nvalid ? sc[nt][c] * a.scale_log2 : -INFINITY;
+                x[c] = tok < nvalid ? sc[nt][c] * csc[nt][c & 1] : -INFINITY;
                 mx[c & 1] = fmaxf(mx[c & 1], x[c]);
             }
 #pragma unroll
@@ -289,8 +359,13 @@ __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_c
                 pr[c] = ex2(x[c] - base[c & 1]);
                 l[nt][c & 1] += pr[c];
             }
-            pb[nt][0] = movmatrix_t(bf16x2(pr[0], pr[1]));
-            pb[nt][1] = movmatrix_t(bf16x2(pr[2], pr[3]));
+            if constexpr (QUANT) {
+                pb[nt][0] = movmatrix_t(f16x2(pr[0], pr[1]));
+                pb[nt][1] = movmatrix_t(f16x2(pr[2], pr[3]));
+            } else {
+                pb[nt][0] = movmatrix_t(bf16x2(pr[0], pr[1]));
+                pb[nt][1] = movmatrix_t(bf16x2(pr[2], pr[3]));
+            }
         }
         // O^T += V^T P^T; the V fragments serve both n-tiles (rows past the prefix are 0)
         {
@@ -300,8 +375,13 @@ __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_c
             for (int mt = 0; mt < MT; ++mt) {
                 uint32_t af[4];
                 ldsm_x4_trans(af, rb + mt * 32);
-                mma16816(o[0][mt], af, pb[0][0], pb[0][1]);
-                mma16816(o[1][mt], af, pb[1][0], pb[1][1]);
+                if constexpr (QUANT) {
+                    mma16816_f16(o[0][mt], af, pb[0][0], pb[0][1]);
+                    mma16816_f16(o[1][mt], af, pb[1][0], pb[1][1]);
+                } else {
+                    mma16816(o[0][mt], af, pb[0][0], pb[0][1]);
+                    mma16816(o[1][mt], af, pb[1][0], pb[1][1]);
+                }
             }
         }
     }
@@ -458,8 +538,8 @@ cudaError_t side_stream(int dev, SideStream *&out) {
     return cudaSuccess;
 }
 
-template <int D, int BS>
-cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, cudaStream_t stream) {
+template <typename KV, int D, int BS>
+cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, int kv_dtype, cudaStream_t stream) {
     constexpr int SMEM = 2 * kPrefixChunk * (D * 2 + 16);
     static bool configured[64] = {false};
     static std::mutex mu;  // one enqueue sequence at a time: the events are shared
@@ -467,7 +547,7 @@ cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, cudaSt
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_prefix_kernel<D, BS>,
+        cudaError_t e = cudaFuncSetAttribute(grouped_prefix_kernel<KV, D, BS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -481,10 +561,10 @@ cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, cudaSt
         if ((err = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return err;
         if ((err = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return err;
         dim3 grid(p.PP, a.Hkv * p.CB, p.n_groups);
-        grouped_prefix_kernel<D, BS><<<grid, kThreads, SMEM, ss->stream>>>(a, p);
+        grouped_prefix_kernel<KV, D, BS><<<grid, kThreads, SMEM, ss->stream>>>(a, p);
         if ((err = cudaEventRecord(ss->join, ss->stream)) != cudaSuccess) return err;
     }
-    err = launch_decode(a, D, BS, PA_KV_BF16, stream);  // own tokens, partials only
+    err = launch_decode(a, D, BS, kv_dtype, stream);  // own tokens, partials only
     if (grouped) {
         const cudaError_t e = cudaStreamWaitEvent(stream, ss->join, 0);  // join even on error
         if (err == cudaSuccess) err = e;
@@ -499,11 +579,21 @@ cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, cudaSt
 int prefix_chunk_tokens() { return kPrefixChunk; }
 int prefix_cols_per_cta() { return kColsPerCta; }
 
-cudaError_t launch_decode_shared_prefix(const DecodeArgs &a, const PrefixArgs &p, int D, int bs,
-                                        cudaStream_t stream) {
+template <typename KV>
+cudaError_t launch_prefix_kv(const DecodeArgs &a, const PrefixArgs &p, int D, int bs, int kv_dtype,
+                             cudaStream_t stream) {
     if (D == 128)
-        return bs == 16 ? launch_prefix_typed<128, 16>(a, p, stream) : launch_prefix_typed<128, 32>(a, p, stream);
-    return bs == 16 ? launch_prefix_typed<64, 16>(a, p, stream) : launch_prefix_typed<64, 32>(a, p, stream);
+        return bs == 16 ? launch_prefix_typed<KV, 128, 16>(a, p, kv_dtype, stream)
+                        : launch_prefix_typed<KV, 128, 32>(a, p, kv_dtype, stream);
+    return bs == 16 ? launch_prefix_typed<KV, 64, 16>(a, p, kv_dtype, stream)
+                    : launch_prefix_typed<KV, 64, 32>(a, p, kv_dtype, stream);
+}
+
+cudaError_t launch_decode_shared_prefix(const DecodeArgs &a, const PrefixArgs &p, int D, int bs, int kv_dtype,
+                                        cudaStream_t stream) {
+    if (kv_dtype == PA_KV_INT8) return launch_prefix_kv<int8_t>(a, p, D, bs, kv_dtype, stream);
+    if (kv_dtype == PA_KV_FP8) return launch_prefix_kv<e4m3_tag>(a, p, D, bs, kv_dtype, stream);
+    return launch_prefix_kv<uint16_t>(a, p, D, bs, kv_dtype, stream);
 }
 
 }  // namespace pa

@@ -71,7 +71,7 @@ def gpu_step(case: workloads.PagedCase, device, max_context_len=None, poison_int
         gp = torch.as_tensor(plens, dtype=torch.int32).to(device)
         pa.pa_decode_shared_prefix(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens,
                                    case.scale, max_context_len, gs, gp, max_group, max_prefix,
-                                   err_flag=flag)
+                                   k_scale=k_scale, v_scale=v_scale, err_flag=flag)
     else:
         ws = pa.decode_workspace(c.q, k_cache, max_context_len)
         pa.pa_decode(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens, case.scale,

@@ -147,7 +147,8 @@ def test_shared_prefix_workspace_and_checks(lib):
         **{**dict(S=4, Hq=8, Hkv=2, D=128, bs=16, kv_dtype=0, max_context_len=512,
                   max_group_size=4, max_prefix_len=256), **k})
     assert ws() > 0
-    assert ws(kv_dtype=pa.PA_KV_INT8) == 0      # bf16 caches only
+    assert ws(kv_dtype=pa.PA_KV_INT8) == ws()
+    assert ws(kv_dtype=9) == 0                  # no such cache type
     assert ws(max_prefix_len=200) == 0          # not whole blocks
     assert ws(max_prefix_len=1024) == 0         # longer than any context
     assert ws(max_group_size=0) == 0
@@ -161,7 +162,8 @@ def test_shared_prefix_workspace_and_checks(lib):
                                            8, 2, 128, 16, 4, 0.1, 64, gs, fake, n_groups,
                                            max_group, max_prefix, ws, ws_bytes, None, None)
 
-    assert call(kv=pa.PA_KV_FP8) == pa.PA_ERR_UNSUPPORTED
+    assert call(kv=pa.PA_KV_FP8) == pa.PA_ERR_INVALID_ARG  # scales missing
+    assert call(kv=6) == pa.PA_ERR_UNSUPPORTED
     assert call(gs=None) == pa.PA_ERR_INVALID_ARG
     assert call(n_groups=-1) == pa.PA_ERR_INVALID_ARG
     assert call(max_prefix=48 + 8) == pa.PA_ERR_INVALID_ARG

@@ -43,9 +43,10 @@ def _run(case, orc, groups, expect_flag=0):
     return helpers.compare(got["out"], ref, case.kv_dtype)
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("D,bs,Hq,Hkv", [(128, 16, 32, 8), (64, 32, 4, 4), (128, 32, 16, 2),
                                           (64, 16, 20, 2), (128, 16, 64, 8)])
-def test_one_group_with_cow(oracle, D, bs, Hq, Hkv):
+def test_one_group_with_cow(oracle, D, bs, Hq, Hkv, kv_dtype):
     """Every sequence shares one prefix (several 128-token chunks and a ragged last
     chunk); each sequence's last block is a copy-on-write target."""
     prefix = 21 * 32  # 672 tokens: five chunks of 128 and one of 32
@@ -53,17 +54,18 @@ def test_one_group_with_cow(oracle, D, bs, Hq, Hkv):
     lens = [prefix + o for o in own]
     case = workloads.build_case(f"pfx-{D}-{bs}-{Hq}-{Hkv}", S=len(lens), Hq=Hq, Hkv=Hkv, D=D,
                                 bs=bs, context_lens=lens, seed=7 * D + bs + Hq,
-                                prefix_tokens=prefix, cow=True)
+                                prefix_tokens=prefix, cow=True, kv_dtype=kv_dtype)
     _run(case, oracle, ([0, case.S], [prefix], case.S, prefix))
 
 
-def test_mixed_groups(oracle):
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
+def test_mixed_groups(oracle, kv_dtype):
     """Several groups with different prefixes, a one-member group, an empty group,
     sequences in no group, a member whose whole context is the prefix, and a prefix
     whose last chunk is ragged (208 = 128 + 80 tokens)."""
     lens = [300, 290, 1000, 129, 50, 208, 400, 209, 3000, 77, 1, 2500]
     case = workloads.build_case("pfx-mixed", S=len(lens), Hq=32, Hkv=8, D=128, bs=16,
-                                context_lens=lens, seed=11)
+                                context_lens=lens, seed=11, kv_dtype=kv_dtype)
     _share(case, [0, 1, 2, 3], 128)
     _share(case, [5, 6, 7, 8], 208)
     # groups: [0,4) 128 tokens, [4,5) 48 tokens, [5,5) empty, [5,9) 208 tokens; 9.. alone
@@ -108,8 +110,8 @@ def test_no_groups_matches_decode(oracle):
 
 
 def test_rejects_unsupported():
-    """Host-side checks: quantised caches, prefix bounds that are not whole blocks,
-    and a short workspace are refused before anything is queued."""
+    """Host-side checks: an 8-bit cache without scales, prefix bounds that are not whole
+    blocks, and a short workspace are refused before anything is queued."""
     import paged_kv_cache_197_gb300 as pa
 
     case = workloads.build_case("pfx-rej", S=2, Hq=4, Hkv=4, D=64, bs=16, context_lens=[40, 40],
@@ -118,7 +120,7 @@ def test_rejects_unsupported():
     gs = torch.tensor([0, 2], dtype=torch.int32, device=DEV)
     gp = torch.tensor([32], dtype=torch.int32, device=DEV)
     i8 = torch.zeros(case.k_pool.shape, dtype=torch.int8, device=DEV)
-    with pytest.raises(pa.PagedAttentionError):
+    with pytest.raises(ValueError):  # an int8 cache without its scales
         pa.pa_decode_shared_prefix(out, case.q, i8, i8, case.block_tables, case.context_lens,
                                    case.scale, 40, gs, gp, 2, 32)
     with pytest.raises(pa.PagedAttentionError):
