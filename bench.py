@@ -54,9 +54,10 @@ DESCRIPTIONS = {
     "prefill8b": "chunked prefill, Llama-3-8B shape: 4 seqs x 512-token chunk on 3584 cached tokens, "
                  "32/8 heads, head_dim 128, block 16",
     "verify70b_fp8": "the draft-verification workload with an fp8 (e4m3) cache and per-token scales",
+    "prefix_fp8": "the prefix-shared workload with an fp8 (e4m3) cache and per-token scales",
     "prefill8b_fp8": "the chunked-prefill workload with an fp8 (e4m3) cache and per-token scales",
 }
-FLUSH_L2 = {"tiny", "prefix", "prefill8b", "prefill8b_fp8"}
+FLUSH_L2 = {"tiny", "prefix", "prefix_fp8", "prefill8b", "prefill8b_fp8"}
 L2_BYTES = 126 * 1024 * 1024
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
@@ -66,10 +67,11 @@ NCU_TRAFFIC = {
     ("gqa70b", "0a92d8beb0508d47"): 655764224 + 5198848,
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
     ("fp8", "0a92d8beb0508d47"): 3144265472 + 5437952,
-    ("verify70b", "c25396a67b4994d3"): 656778752 + 18288896,
-    ("prefill8b", "c25396a67b4994d3"): 84117504 + 88478976,
-    ("verify70b_fp8", "c25396a67b4994d3"): 339649792 + 19931392,
-    ("prefill8b_fp8", "c25396a67b4994d3"): 51451904 + 84611072,
+    ("prefix", "0a92d8beb0508d47"): 72100608 + 1082624,
+    ("verify70b", "0a4d444bf63ed80d"): 656779008 + 18277376,
+    ("prefill8b", "0a4d444bf63ed80d"): 83963392 + 88199936,
+    ("verify70b_fp8", "0a4d444bf63ed80d"): 339652352 + 19790592,
+    ("prefill8b_fp8", "0a4d444bf63ed80d"): 51504128 + 84613632,
 }
 
 
@@ -252,7 +254,8 @@ class Step:
             self.pa.pa_decode_shared_prefix(out, q, self.k_cache, self.v_cache, tables, lens,
                                             self.case.scale, self.max_ctx, self.group_start,
                                             self.group_prefix, self.case.S, self.prefix,
-                                            workspace=self.ws, err_flag=self.flag,
+                                            workspace=self.ws, k_scale=self.k_scale,
+                                            v_scale=self.v_scale, err_flag=self.flag,
                                             stream=self.stream)
             return
         self.pa.pa_decode(out, q, self.k_cache, self.v_cache, tables, lens, self.case.scale,
@@ -409,7 +412,7 @@ def run_ours(args, rank, world, device) -> dict | None:
         res["config"]["decode_path"] = "shared-prefix (one group of all sequences)"
         res["roofline"]["achieved_per_sequence_bytes"] = round(
             nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9, 1)
-    elif args.config == "prefix":
+    elif case.shared_prefix_blocks:
         res["roofline"]["achieved_unique_bytes"] = round(
             nbytes["decode_unique"] / (dec_mean_ms * 1e-3) / 1e9, 1)
     if not args.no_cpu_baseline and not args.quick and world == 1:

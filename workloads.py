@@ -242,11 +242,16 @@ def gqa70b(seed: int = 2, device="cpu", poison=False) -> PagedCase:
                       seed=seed, pool_blocks=10000, poison=poison, device=device)
 
 
-def prefix(seed: int = 3, device="cpu", poison=False) -> PagedCase:
+def prefix(seed: int = 3, device="cpu", poison=False, kv_dtype="bf16") -> PagedCase:
     own = torch.randint(64, 513, (50,), generator=_gen(seed + 100))
     lens = (2000 + own).tolist()
     return build_case("prefix", S=50, Hq=32, Hkv=8, D=128, bs=16, context_lens=lens, seed=seed,
-                      prefix_tokens=2000, cow=True, poison=poison, device=device)
+                      prefix_tokens=2000, cow=True, poison=poison, device=device, kv_dtype=kv_dtype)
+
+
+def prefix_fp8(seed: int = 3, device="cpu", poison=False) -> PagedCase:
+    """The shared-prompt workload with an fp8 (e4m3) cache."""
+    return prefix(seed, device, poison, kv_dtype="fp8")
 
 
 def int8_lengths(S: int, seed: int, lo: int = 128, hi: int = 32768) -> list[int]:
@@ -294,7 +299,7 @@ def prefill8b_fp8(seed: int = 7, device="cpu", poison=False) -> PagedCase:
 
 CONFIGS = {"tiny": tiny, "mha13b": mha13b, "gqa70b": gqa70b, "prefix": prefix, "int8": int8, "fp8": fp8,
            "verify70b": verify70b, "prefill8b": prefill8b, "verify70b_fp8": verify70b_fp8,
-           "prefill8b_fp8": prefill8b_fp8}
+           "prefill8b_fp8": prefill8b_fp8, "prefix_fp8": prefix_fp8}
 
 
 # ------------------------------------------------------------------ byte accounting
