@@ -69,10 +69,14 @@ enum {
     PA_FLAG_PREFIX_MISMATCH = 8,      /* pa_decode_shared_prefix: a group or member did not
                                          meet the prefix preconditions and was decoded on
                                          its own (the result is still correct)            */
-    PA_FLAG_QUERY_OUT_OF_RANGE = 16   /* pa_multi_token_attention: query offsets of a
+    PA_FLAG_QUERY_OUT_OF_RANGE = 16,  /* pa_multi_token_attention: query offsets of a
                                          sequence outside [0, T], decreasing, longer than
                                          its context or than max_query_len: its rows are
                                          not written                                      */
+    PA_FLAG_TIMEOUT = 32              /* a kernel's bounded wait for its own copies or
+                                         tensor-core products gave up (the affected
+                                         outputs are not written); not expected in normal
+                                         operation                                        */
 };
 
 /* Version of this ABI (bumped on any signature change). */

@@ -19,7 +19,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = ROOT / "_build"
 LIBRARY = PKG / "libpa.so"
-SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefix.cu", "pa_multi.cu", "pa_noalloc.cu", "pa_blocks.cpp"]
+SOURCES = ["pa_api.cu", "pa_cache.cu", "pa_decode.cu", "pa_prefix.cu", "pa_multi.cu", "pa_multi_tc.cu", "pa_noalloc.cu", "pa_blocks.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -488,15 +488,25 @@ struct MultiPlan {
 // writes) in tokens of streaming: larger than the decode kernel's.
 constexpr double kMultiRampTokens = 256.0;
 
-static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int max_context_len, int max_query_len) {
+static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int kv_dtype, int max_context_len,
+                            int max_query_len) {
     MultiPlan p{};
     const int G = Hq / Hkv;
     p.CB = std::max(1, (int)(((int64_t)max_query_len * G + multi_cols_per_cta() - 1) / multi_cols_per_cta()));
     const int64_t units = (int64_t)S * Hkv * p.CB;
-    const double slots = (double)device_sms() * 2;
+    const bool tc = multi_tc_eligible(D, kv_dtype, G, max_query_len);
+    const double slots = (double)device_sms() * (tc ? 1 : 2);
     const int ctx = std::max(max_context_len, 1);
     p.part_tokens = 256;
-    if ((double)units >= 4.0 * slots && ctx <= 4096) {
+    if (tc) {
+        // whole contexts (partials and their merge cost more than a ragged last wave),
+        // unless the CTAs would fill less than half the SMs: then about one wave
+        p.part_tokens = (int)align_up((size_t)ctx, 64);
+        if ((double)units < slots / 2) {
+            const int64_t want = (int64_t)std::ceil(slots / (double)units);
+            p.part_tokens = std::max(512, (int)align_up((size_t)((ctx + want - 1) / want), 128));
+        }
+    } else if ((double)units >= 4.0 * slots && ctx <= 4096) {
         p.part_tokens = (int)align_up((size_t)ctx, 64);
     } else {
         double best = -1.0;
@@ -541,7 +551,7 @@ size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int b
     if (check_multi_args("pa_multi_token_workspace_size", S, T, Hq, Hkv, D, bs, kv_dtype,
                          max_context_len, max_query_len) != PA_OK)
         return 0;
-    return plan_multi(S, T, Hq, Hkv, D, max_context_len, max_query_len).bytes;
+    return plan_multi(S, T, Hq, Hkv, D, kv_dtype, max_context_len, max_query_len).bytes;
 }
 
 pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
@@ -571,7 +581,7 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
         return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
     if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
         return fail(PA_ERR_INVALID_ARG, "%s: scale must be finite", fn);
-    const MultiPlan plan = plan_multi(S, T, Hq, Hkv, D, max_context_len, max_query_len);
+    const MultiPlan plan = plan_multi(S, T, Hq, Hkv, D, kv_dtype, max_context_len, max_query_len);
     if (plan.bytes && (!workspace || workspace_bytes < plan.bytes))
         return fail(PA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, plan.bytes,
                     workspace ? workspace_bytes : (size_t)0);

@@ -682,6 +682,11 @@ cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
     paged_multi_kernel<KV, D, BS><<<grid, kThreads, SMEM, stream>>>(a);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || a.max_parts == 1) return err;
+    return launch_multi_merge(a, D, BS, stream);
+}
+
+template <int D, int BS>
+cudaError_t launch_merge_typed(const MultiArgs &a, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((a.max_query_len * a.Hq + 3) / 4), a.S);
     cfg.blockDim = dim3(128);
@@ -698,6 +703,11 @@ cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
 
 int multi_cols_per_cta() { return kColsPerCta; }
 
+cudaError_t launch_multi_merge(const MultiArgs &a, int D, int bs, cudaStream_t stream) {
+    if (D == 128) return bs == 16 ? launch_merge_typed<128, 16>(a, stream) : launch_merge_typed<128, 32>(a, stream);
+    return bs == 16 ? launch_merge_typed<64, 16>(a, stream) : launch_merge_typed<64, 32>(a, stream);
+}
+
 template <typename KV>
 cudaError_t launch_multi_kv(const MultiArgs &a, int D, int bs, cudaStream_t stream) {
     if (D == 128)
@@ -706,6 +716,7 @@ cudaError_t launch_multi_kv(const MultiArgs &a, int D, int bs, cudaStream_t stre
 }
 
 cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
+    if (multi_tc_eligible(D, kv_dtype, a.G, a.max_query_len)) return launch_multi_tc(a, bs, stream);
     if (kv_dtype == PA_KV_INT8) return launch_multi_kv<int8_t>(a, D, bs, stream);
     if (kv_dtype == PA_KV_FP8) return launch_multi_kv<e4m3_tag>(a, D, bs, stream);
     return launch_multi_kv<uint16_t>(a, D, bs, stream);

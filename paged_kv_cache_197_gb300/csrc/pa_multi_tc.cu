@@ -1,0 +1,572 @@
+// Multi-token paged attention on the fifth-generation tensor cores (tcgen05), for
+// bf16 caches with head_dim 128: the prefill-shaped case, where a kv head of a
+// sequence has at least half a tile (64) of (new token, query head) columns.
+//
+// What is computed is the same as the mma.sync kernel in pa_multi.cu (deeplearn.tn,
+// "Les leviers d'optimisation en production": a chunk of new tokens attends the
+// paged cache, each token up to its own position).  One CTA takes 128 columns of one
+// (sequence, kv head, context partition) and streams the partition in 128-token
+// tiles.  Its seven warps have fixed roles, coupled only through mbarriers:
+//   * warp 4 copies K tiles, warp 5 V tiles, into two stages each by TMA: per cache
+//     block, two boxes of 64 dims x block-size rows with the 128-byte swizzle, so a
+//     staged tile is the K-major layout the tensor core reads (the block ids come
+//     from the table, one lane per block; entries outside the pool and blocks past
+//     the partition are copied from past the end of the pool, i.e. as zeros);
+//   * warp 6 issues, from one lane, S_t = Q K_t^T (M 128 columns x N 128 tokens,
+//     K 128 dims; two tensor-memory buffers, so S of the next tile is computed while
+//     this one is turned into P) and O += P_t V_t (N 128 dims, K 128 tokens; V read
+//     as an MN-major operand from the same staged tile), and commits each to the
+//     barriers that free the stages and wake the row warps;
+//   * warps 0-3 own one row each (tensor-memory lane = thread): they read the row's
+//     scores, mask tokens past its position, keep a running max (raised only when a
+//     tile's max exceeds it by more than 2^8 in the exp2 domain; O is then rescaled in
+//     tensor memory) and sum, write P in bf16 to shared memory in the swizzled
+//     K-major layout, and finally write the output row or its (max, sum, output)
+//     partial for the merge kernel shared with the mma.sync path.
+// Every wait is bounded (PA_FLAG_TIMEOUT when one gives up; the outputs are then not
+// written).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTcThreads = 128;
+constexpr int kTcRows = 128;  // columns per CTA: the M of both products
+constexpr int kTcTile = 128;  // cached tokens per tile: N of S, K of P V
+constexpr int kTcD = 128;
+constexpr int kTcTileBytes = kTcTile * kTcD * 2;
+constexpr int kTcAtom = kTcTile * 128;  // one 64-dim half of a tile: 128 rows of 128 B
+constexpr int kTcSmem = 6 * kTcTileBytes + 1024;  // Q, K x2, V x2, P; 1024-byte alignment
+constexpr float kTcRescaleLog2 = 8.0f;
+constexpr unsigned long long kTcWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t tc_smem(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long tc_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void tc_raise(int *err_flag, int bit) {
+    if (err_flag) atomicOr(err_flag, bit);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Wait for the phase with the given parity to complete; false after kTcWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    unsigned long long t0 = 0;
+    for (int it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (it == 0)
+            t0 = tc_now();
+        else if (tc_now() - t0 > kTcWaitNs)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start, leading and stride byte
+// offsets (16-byte units), descriptor version 1, layout type 2.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (1), N and M.
+__host__ __device__ constexpr uint32_t bf16_idesc(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of the calling thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float tc_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t tc_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Byte offset of the 16-byte chunk ch (8 bf16 values, ch in [0, 16)) of row r in a
+// 128-row, 128-element K-major tile with 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) {
+    return (ch >> 3) * kTcAtom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ void mbar_init_n(uint32_t bar, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Roles: warps 0-3 own the 128 rows (scores, softmax, P, epilogue); warp 4 copies K
+// tiles, warp 5 V tiles, warp 6 issues the tensor-core products (one lane each).
+constexpr int kTcSoftmaxWarps = 4;
+constexpr int kTcWarps = 7;
+constexpr int kTcAllThreads = kTcWarps * 32;
+
+struct TcShared {
+    uint64_t kfull[2], vfull[2];  // tile landed (TMA transaction count)
+    uint64_t kfree[2], vfree[2];  // stage consumed by S_t / by P V_t (tcgen05.commit)
+    uint64_t sfull[2], sfree[2];  // S_t in tensor memory / read by all 128 rows
+    uint64_t pfull, odone;        // P_t written by all rows / P V_t done
+    uint32_t taddr;
+    int abort;
+};
+
+template <int BS>
+__global__ void __launch_bounds__(kTcAllThreads, 1)
+multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ unsigned char dsm[];
+    __shared__ TcShared sh;
+    unsigned char *base = dsm + ((1024 - (tc_smem(dsm) & 1023)) & 1023);
+    unsigned char *Qs = base, *Ps = base + 5 * kTcTileBytes;
+    const uint32_t q_s = tc_smem(Qs), p_s = tc_smem(Ps);
+
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
+    const int s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- the sequence, the CTA's columns and its token range (as in pa_multi.cu)
+    int ctx = a.context_lens[s];
+    const int lim_ctx = min(a.M * BS, a.max_context_len);
+    const bool report = part == 0 && blockIdx.y == 0 && tid == 0;
+    if (ctx < 0 || ctx > lim_ctx) {
+        if (report) tc_raise(a.err_flag, PA_FLAG_CONTEXT_OUT_OF_RANGE);
+        ctx = ctx < 0 ? 0 : lim_ctx;
+    }
+    const int r0 = a.query_start[s], r1 = a.query_start[s + 1];
+    const int L = r1 - r0;
+    if (!(r0 >= 0 && r1 <= a.T && L >= 0 && L <= ctx && L <= a.max_query_len)) {
+        if (report) tc_raise(a.err_flag, PA_FLAG_QUERY_OUT_OF_RANGE);
+        return;
+    }
+    const int qbase = ctx - L;
+    const int ncols = L * a.G;
+    const int col0 = cb * kTcRows;
+    if (col0 >= ncols) return;
+    auto ctok = [&](int c) { return a.g_shift >= 0 ? c >> a.g_shift : c / a.G; };
+    auto chead = [&](int c) { return a.g_shift >= 0 ? c & (a.G - 1) : c % a.G; };
+    const int cta_lim = qbase + ctok(min(ncols, col0 + kTcRows) - 1);
+    const int tok_begin = part * a.part_tokens;
+    const int tok_end = min(tok_begin + a.part_tokens, cta_lim + 1);
+    if (tok_begin >= tok_end) return;
+    const int blk0 = tok_begin / BS;
+    const int nblk = (tok_end - tok_begin + BS - 1) / BS;
+    const int ntile = (tok_end - tok_begin + kTcTile - 1) / kTcTile;
+
+    // ---- rows: thread tid < 128 owns column col0 + tid
+    const bool row_thread = warp < kTcSoftmaxWarps;
+    const int c = col0 + tid;
+    const bool has = row_thread && c < ncols;
+    const int lim = has ? qbase + ctok(c) : -1;  // last visible token
+    const int lim_p = min(lim, tok_end - 1);     // ... inside this partition
+    int64_t pair = 0;
+    if (has) pair = (int64_t)(r0 + ctok(c)) * a.Hq + kvh * a.G + chead(c);
+    if (row_thread) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + pair * kTcD);
+#pragma unroll 4
+        for (int ch = 0; ch < 16; ++ch) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (has) x = __ldg(src + ch);
+            *reinterpret_cast<uint4 *>(Qs + sw128_chunk(tid, ch)) = x;
+        }
+    }
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tc_smem(&sh.kfull[i]));
+            mbar_init(tc_smem(&sh.vfull[i]));
+            mbar_init(tc_smem(&sh.kfree[i]));
+            mbar_init(tc_smem(&sh.vfree[i]));
+            mbar_init(tc_smem(&sh.sfull[i]));
+            mbar_init_n(tc_smem(&sh.sfree[i]), kTcRows);
+        }
+        mbar_init_n(tc_smem(&sh.pfull), kTcRows);
+        mbar_init(tc_smem(&sh.odone));
+        sh.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the tensor core
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(tc_smem(&sh.taddr))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.taddr;
+    const uint32_t t_o = tmem + 256;  // O: columns 256..383; S buffers at 0 and 128
+
+    if (warp == 4 || warp == 5) {
+        // ---- copies: K (warp 4) or V (warp 5) tiles into their two stages; the whole
+        // warp follows the loop (waits), lane 0 issues
+        const bool is_k = warp == 4;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        const int oob_row = a.N * a.Hkv * BS;  // a row past the pool: the copy fills zeros
+#pragma unroll 1
+        for (int t = 0; t < ntile; ++t) {
+            const int st = t & 1;
+            // lane i < 128 / BS reads the table entry of the tile's block i; entries
+            // outside [0, N) are flagged (once, by the K copies of the first column
+            // block) and read as zeros, like blocks past the partition
+            int y = oob_row;
+            const int idx = t * (kTcTile / BS) + lane;
+            if (lane < kTcTile / BS && idx < nblk) {
+                const int b = __ldg(a.block_tables + (int64_t)s * a.M + blk0 + idx);
+                if (b >= 0 && b < a.N)
+                    y = (b * a.Hkv + kvh) * BS;
+                else if (is_k && cb == 0)
+                    tc_raise(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
+            }
+            bool ok = true;
+            if (t >= 2) ok = mbar_wait(tc_smem(is_k ? &sh.kfree[st] : &sh.vfree[st]), ((t >> 1) - 1) & 1);
+            if (__any_sync(0xffffffffu, !ok || sh.abort != 0)) {
+                if (lane == 0 && !ok) atomicOr(&sh.abort, 1);
+                break;
+            }
+            if (lane == 0) mbar_expect(tc_smem(is_k ? &sh.kfull[st] : &sh.vfull[st]), kTcTileBytes);
+            __syncwarp();
+            const uint32_t bar = tc_smem(is_k ? &sh.kfull[st] : &sh.vfull[st]);
+            const uint32_t dst = tc_smem(base + ((is_k ? 1 : 3) + st) * kTcTileBytes);
+#pragma unroll
+            for (int i = 0; i < kTcTile / BS; ++i) {
+                const int yi = __shfl_sync(0xffffffffu, y, i);
+                if (lane == 0) {
+                    tma_load(dst + (i * BS / 8) * 1024, map, 0, yi, bar);
+                    tma_load(dst + kTcAtom + (i * BS / 8) * 1024, map, 64, yi, bar);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == 6) {
+        // ---- tensor-core products in the order S_0, S_1, PV_0, S_2, PV_1, ...: the
+        // whole warp waits, lane 0 issues
+        auto issue_s = [&](int t) -> bool {
+            const int st = t & 1;
+            bool ok = mbar_wait(tc_smem(&sh.kfull[st]), (t >> 1) & 1);
+            if (ok && t >= 2) ok = mbar_wait(tc_smem(&sh.sfree[st]), ((t >> 1) - 1) & 1);
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t kb = tc_smem(base + (1 + st) * kTcTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTcD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kTcAtom + (kk & 3) * 32;
+                    umma(tmem + st * 128, sw128_desc(q_s + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
+                         bf16_idesc(128, 128, 0), kk > 0);
+                }
+                umma_commit(tc_smem(&sh.sfull[st]));
+                umma_commit(tc_smem(&sh.kfree[st]));
+            }
+            __syncwarp();
+            return true;
+        };
+        bool ok = issue_s(0);
+#pragma unroll 1
+        for (int j = 0; ok && j < ntile; ++j) {
+            const int st = j & 1;
+            if (j + 1 < ntile) ok = issue_s(j + 1);
+            if (ok) ok = mbar_wait(tc_smem(&sh.pfull), j & 1) && mbar_wait(tc_smem(&sh.vfull[st]), (j >> 1) & 1);
+            if (!__all_sync(0xffffffffu, ok && sh.abort == 0)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t vb = tc_smem(base + (3 + st) * kTcTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTcTile / 16; ++kk)
+                    umma(t_o, sw128_desc(p_s + (kk >> 2) * kTcAtom + (kk & 3) * 32, 16, 1024),
+                         sw128_desc(vb + kk * 2048, kTcAtom, 1024), bf16_idesc(128, 128, 1), (j > 0 || kk > 0));
+                umma_commit(tc_smem(&sh.odone));
+                umma_commit(tc_smem(&sh.vfree[st]));
+            }
+            __syncwarp();
+        }
+        if (!ok && lane == 0) atomicOr(&sh.abort, 1);
+    } else {
+        // ---- rows: scores, online softmax, P, output
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+#pragma unroll 1
+        for (int j = 0; j < ntile; ++j) {
+            const int st = j & 1;
+            ok = mbar_wait(tc_smem(&sh.sfull[st]), (j >> 1) & 1);
+            if (__any_sync(0xffffffffu, !ok || sh.abort != 0)) { ok = false; break; }
+            tc_fence_after();
+            float sv[kTcTile];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + st * 128 + 32 * q, sv + 32 * q);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(tc_smem(&sh.sfree[st]));
+
+            // masked row max, eight independent chains
+            const int k0 = tok_begin + j * kTcTile;
+            if (k0 + kTcTile - 1 > lim_p) {
+#pragma unroll
+                for (int k = 0; k < kTcTile; ++k)
+                    if (k0 + k > lim_p) sv[k] = -INFINITY;
+            }
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = sv[i];
+#pragma unroll
+            for (int k = 8; k < kTcTile; ++k) mx[k & 7] = fmaxf(mx[k & 7], sv[k]);
+            const float mt_s =
+                fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                a.scale_log2;
+
+            // the previous product is done: O is stable and P may be rewritten
+            if (j > 0) {
+                ok = mbar_wait(tc_smem(&sh.odone), (j - 1) & 1);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                tc_fence_after();
+            }
+            // the running max moves only when the tile's max exceeds it by more than
+            // 2^8 in the exp2 domain; then the row's sum and output are rescaled
+            // (tensor-memory accesses are warp-wide: the warp's other rows take 1)
+            float f = 1.f;
+            bool resc = false;
+            if (mt_s > m_run + kTcRescaleLog2) {
+                if (m_run != -INFINITY) {
+                    f = tc_exp2(m_run - mt_s);
+                    l_run *= f;
+                    resc = true;
+                }
+                m_run = mt_s;
+            }
+            if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float ov[32];
+                    tmem_ld32(t_o + lane_off + 32 * q, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] *= f;
+                    tmem_st32(t_o + lane_off + 32 * q, ov);
+                }
+                tmem_wait_st();
+            }
+            const float mb = m_run == -INFINITY ? 0.f : m_run;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = tc_exp2(fmaf(sv[8 * ch + 2 * e], a.scale_log2, -mb));
+                    const float p1 = tc_exp2(fmaf(sv[8 * ch + 2 * e + 1], a.scale_log2, -mb));
+                    ls[e] += p0 + p1;
+                    w[e] = tc_bf16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(Ps + sw128_chunk(tid, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // the last tile's rows past the partition in a partly used block may hold
+            // anything (a zero weight times a NaN is a NaN): zero them in the V stage
+            const int r_lo = tok_end - k0;
+            if (j == ntile - 1 && r_lo < kTcTile && tok_end % BS != 0) {
+                ok = mbar_wait(tc_smem(&sh.vfull[st]), (j >> 1) & 1);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                const int r_hi = min(kTcTile, (tok_end + BS - 1) / BS * BS - k0);
+                unsigned char *vst = base + (3 + st) * kTcTileBytes;
+                for (int i = tid; i < (r_hi - r_lo) * 16; i += kTcRows)
+                    *reinterpret_cast<uint4 *>(vst + sw128_chunk(r_lo + i / 16, i % 16)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor core
+            tc_fence_before();
+            mbar_arrive(tc_smem(&sh.pfull));
+        }
+        if (ok) ok = mbar_wait(tc_smem(&sh.odone), (ntile - 1) & 1);
+        if (!ok) atomicOr(&sh.abort, 1);
+        tc_fence_after();
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        if (__all_sync(0xffffffffu, ok)) {
+            // ---- epilogue: this thread's output row (the tensor-memory loads are
+            // warp-wide; rows with nothing to write discard them)
+            const bool write = has && tok_begin <= lim;
+            const bool finished = lim < a.part_tokens;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const int64_t prow = pair * a.max_parts + part;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float ov[32];
+                tmem_ld32(t_o + lane_off + 32 * q, ov);
+                tmem_wait_ld();
+                if (!write) continue;
+                if (finished) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.out + pair * kTcD) + 4 * q;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(tc_bf16x2(ov[8 * i] * inv, ov[8 * i + 1] * inv),
+                                            tc_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv),
+                                            tc_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv),
+                                            tc_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv));
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + prow * kTcD) + 8 * q;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+                }
+            }
+            if (write && !finished) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(m_run, l_run);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && sh.abort) tc_raise(a.err_flag, PA_FLAG_TIMEOUT);
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+}
+
+}  // namespace
+
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+    static const EncodeTiled fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiled) nullptr;
+        return reinterpret_cast<EncodeTiled>(p);
+    }();
+    return fn;
+}
+
+// A cache pool [N][Hkv][bs][128] bf16 seen as rows of 128 values, copied in boxes of
+// 64 values x bs rows with the 128-byte swizzle.
+bool pool_map(CUtensorMap *map, const void *pool, int rows, int bs) {
+    const EncodeTiled fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kTcD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kTcD * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)bs};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BS>
+cudaError_t launch_tc_typed(const MultiArgs &a, cudaStream_t stream) {
+    CUtensorMap kmap, vmap;
+    if ((int64_t)a.N * a.Hkv * BS >= (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // TMA row coordinates
+    const int rows = a.N * a.Hkv * BS;
+    if (!pool_map(&kmap, a.k_cache, rows, BS) || !pool_map(&vmap, a.v_cache, rows, BS)) return cudaErrorInvalidValue;
+    static bool configured[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(multi_tc_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
+    multi_tc_kernel<BS><<<grid, kTcAllThreads, kTcSmem, stream>>>(a, kmap, vmap);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || a.max_parts == 1) return err;
+    return launch_multi_merge(a, kTcD, BS, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream) {
+    return bs == 16 ? launch_tc_typed<16>(a, stream) : launch_tc_typed<32>(a, stream);
+}
+
+bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len) {
+    return kv_dtype == PA_KV_BF16 && D == kTcD && (int64_t)max_query_len * G >= kTcRows / 2;
+}
+
+}  // namespace pa

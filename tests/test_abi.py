@@ -173,19 +173,29 @@ def test_shared_prefix_workspace_and_checks(lib):
 
 
 def test_multi_token_workspace_and_checks(lib):
-    """Multi-token attention: 128 (token, head) columns per CTA; no partition when the
-    columns give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the
-    best of (last-wave fill) x (len / (len + 256)) over 4096..256-token partitions with
-    >= 2 waves (256 as the fallback).  The workspace holds (D + 2) fp32 per query row,
-    head and partition."""
+    """Multi-token attention: 128 (token, head) columns per CTA.  On the tcgen05 path
+    (bf16 cache, head_dim 128, max_query_len * G >= 64; one CTA per SM) no partition
+    unless the CTAs fill less than half the SMs, then about one wave of partitions
+    (multiples of 128 tokens, at least 512).  Otherwise no partition when the columns
+    give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the best of
+    (last-wave fill) x (len / (len + 256)) over 4096..256-token partitions with >= 2
+    waves (256 as the fallback).  The workspace holds (D + 2) fp32 per query row, head
+    and partition."""
     import math
 
     import paged_kv_cache_197_gb300 as pa
 
-    def plan(S, Hq, Hkv, max_ctx, max_q, slots=304):
-        cb = max(1, -(-max_q * (Hq // Hkv) // 128))
+    def plan(S, Hq, Hkv, D, max_ctx, max_q, sms=152):
+        G = Hq // Hkv
+        cb = max(1, -(-max_q * G // 128))
         units = S * Hkv * cb
         ctx = max(max_ctx, 1)
+        if D == 128 and max_q * G >= 64:
+            if units < sms / 2:
+                want = math.ceil(sms / units)
+                return max(512, -(-(-(-ctx // want)) // 128) * 128)
+            return -(-ctx // 64) * 64
+        slots = 2 * sms
         if units >= 4 * slots and ctx <= 4096:
             return -(-ctx // 64) * 64
         best, best_p = -1.0, 256
@@ -202,8 +212,9 @@ def test_multi_token_workspace_and_checks(lib):
 
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     for S, T, Hq, Hkv, D, max_ctx, max_q in [(20, 80, 64, 8, 128, 8000, 4), (4, 2048, 32, 8, 128, 4096, 512),
-                                             (7, 40, 16, 2, 64, 2100, 8), (600, 600, 32, 32, 128, 1000, 1)]:
-        pt = plan(S, Hq, Hkv, max_ctx, max_q)
+                                             (7, 40, 16, 2, 64, 2100, 8), (600, 600, 32, 32, 128, 1000, 1),
+                                             (1, 128, 32, 8, 128, 32768, 128), (2, 300, 16, 2, 128, 9000, 150)]:
+        pt = plan(S, Hq, Hkv, D, max_ctx, max_q)
         parts = -(-max_ctx // pt)
         rows = T * Hq * parts
         expect = 0 if parts == 1 else up(up(rows * D * 4) + rows * 2 * 4)
@@ -211,9 +222,12 @@ def test_multi_token_workspace_and_checks(lib):
         assert got == expect, (S, T, got, expect)
     ws = lambda **k: pa.pa_multi_token_workspace_size(  # noqa: E731
         **{**dict(S=4, T=64, Hq=8, Hkv=2, D=128, bs=16, kv_dtype=0, max_context_len=8000,
-                  max_query_len=16), **k})
+                  max_query_len=8), **k})
     assert ws() > 0
     assert ws(kv_dtype=pa.PA_KV_INT8) == ws() and ws(kv_dtype=pa.PA_KV_FP8) == ws()
+    # 16 tokens x 4 heads reach the tcgen05 path for bf16 only: 16 CTAs of columns fill
+    # less than half the SMs, so the contexts are split for one wave
+    assert ws(max_query_len=16) > 0 and ws(max_query_len=16) != ws(max_query_len=16, kv_dtype=pa.PA_KV_INT8)
     assert ws(kv_dtype=7) == 0
     assert ws(max_query_len=0) == 0
     assert ws(max_query_len=65) == 0  # more than T rows

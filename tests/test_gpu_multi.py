@@ -202,6 +202,46 @@ def test_graph_capture_replays():
     assert torch.equal(eager, replay)
 
 
+@pytest.mark.parametrize("bs,Hq,Hkv,lens,qlen", [
+    (32, 40, 8, [777, 2100, 64], [40, 300, 64]),  # G = 5, block 32, a chunk that is the whole context
+    (16, 8, 8, [129, 1000], [129, 128]),         # G = 1
+    (16, 64, 8, [5000, 17, 4200], [100, 17, 9]),  # G = 8, partitions, columns past one CTA
+    (32, 16, 2, [40, 300], [33, 300]),           # G = 8, block 32, chunks shorter than a tile
+])
+def test_tensor_core_path(oracle, bs, Hq, Hkv, lens, qlen):
+    """Shapes that run on the tcgen05 kernel (bf16 cache, head_dim 128, at least 64
+    (token, head) columns per kv head): ragged chunks, groups that are not powers of
+    two, block size 32, split contexts, and caches whose unused slots hold NaN."""
+    case = workloads.build_multi_case(f"tc-{bs}-{Hq}-{Hkv}", S=len(lens), Hq=Hq, Hkv=Hkv, D=128,
+                                      bs=bs, context_lens=lens, query_lens=qlen, seed=bs + Hq + len(lens),
+                                      row_offset=1, extra_rows=2)
+    _run(case, oracle)
+
+
+def test_tensor_core_error_flags(oracle):
+    """On the tcgen05 path too: a block id beyond the pool is read as zeros and
+    flagged, and the rows stay finite; a context past max_context_len is clamped."""
+    import paged_kv_cache_197_gb300 as pa
+
+    case = workloads.build_multi_case("tc-flags", S=2, Hq=32, Hkv=4, D=128, bs=16,
+                                      context_lens=[90, 700], query_lens=[20, 64], seed=39,
+                                      poison=False).to(DEV)
+    out = torch.empty_like(case.q)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tables = case.block_tables.clone()
+    tables[1, 5] = case.N + 3
+    pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, tables, case.context_lens,
+                                case.query_start, case.scale, 700, 64, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == pa.PA_FLAG_BLOCK_OUT_OF_RANGE
+    assert torch.isfinite(out.float()).all()
+    flag.zero_()
+    pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, case.block_tables,
+                                case.context_lens, case.query_start, case.scale, 600, 64, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == pa.PA_FLAG_CONTEXT_OUT_OF_RANGE
+
+
 def _sequences(case, seqs):
     """The case cut to the listed sequences (their query rows, tables and lengths)."""
     qs = case.query_start.cpu().tolist()
