@@ -68,10 +68,10 @@ NCU_TRAFFIC = {
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
     ("fp8", "0a92d8beb0508d47"): 3144265472 + 5437952,
     ("prefix", "0a92d8beb0508d47"): 72100608 + 1082624,
-    ("verify70b", "0a4d444bf63ed80d"): 656779008 + 18277376,
-    ("prefill8b", "0a4d444bf63ed80d"): 83963392 + 88199936,
-    ("verify70b_fp8", "0a4d444bf63ed80d"): 339652352 + 19790592,
-    ("prefill8b_fp8", "0a4d444bf63ed80d"): 51504128 + 84613632,
+    ("verify70b", "e18995d7f6cbf9f4"): 656804608 + 18492928,
+    ("prefill8b", "46000fc224a6bf3a"): 83975168 + 3320064,
+    ("verify70b_fp8", "e18995d7f6cbf9f4"): 339669248 + 19878144,
+    ("prefill8b_fp8", "e18995d7f6cbf9f4"): 51451648 + 84620800,
 }
 
 
@@ -82,6 +82,17 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def multi_kernel_source(case) -> str:
+    """The source of the kernel a multi-token call runs: the tcgen05 kernel for bf16
+    caches with head_dim 128 and at least 64 (token, head) columns per kv head (the
+    library's own dispatch rule), else the mma.sync one."""
+    qs = case.query_start.cpu()
+    max_q = int((qs[1:] - qs[:-1]).max())
+    if case.kv_dtype == "bf16" and case.D == 128 and max_q * (case.Hq // case.Hkv) >= 64:
+        return "pa_multi_tc.cu"
+    return "pa_multi.cu"
 
 
 def kernel_source_hash(name: str = "pa_decode.cu") -> str:
@@ -353,7 +364,8 @@ def run_ours(args, rank, world, device) -> dict | None:
     peaks = measured_peaks()
     flops = workloads.multi_token_flops(case) if step.multi else 0
     if step.multi:
-        kernel_name = "pa_multi_token_attention call (attention + partition merge)"
+        kernel_name = ("pa_multi_token_attention call (attention + partition merge), kernel in "
+                       + multi_kernel_source(case))
         achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
     elif step.prefix:
         # the grouped path must move each shared block once: the unique bytes are its
@@ -364,7 +376,7 @@ def run_ours(args, rank, world, device) -> dict | None:
     else:
         achieved = nbytes["decode"] / (dec_mean_ms * 1e-3) / 1e9
         kernel_name = "pa_decode call (decode + partition merge)"
-    src_hash = kernel_source_hash("pa_multi.cu" if step.multi else
+    src_hash = kernel_source_hash(multi_kernel_source(case) if step.multi else
                                   "pa_prefix.cu" if step.prefix else "pa_decode.cu")
     traffic = NCU_TRAFFIC.get((args.config, src_hash))
     value = whole_job_gbs(nbytes["total"], world, ms_per_step)

@@ -74,7 +74,8 @@ enum {
                                          its context or than max_query_len: its rows are
                                          not written                                      */
     PA_FLAG_TIMEOUT = 32              /* a kernel's bounded wait for its own copies or
-                                         tensor-core products gave up (the affected
+                                         tensor-core products gave up, or its shared
+                                         memory could not be laid out (the affected
                                          outputs are not written); not expected in normal
                                          operation                                        */
 };

@@ -495,7 +495,7 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int kv_dtype, 
     p.CB = std::max(1, (int)(((int64_t)max_query_len * G + multi_cols_per_cta() - 1) / multi_cols_per_cta()));
     const int64_t units = (int64_t)S * Hkv * p.CB;
     const bool tc = multi_tc_eligible(D, kv_dtype, G, max_query_len);
-    const double slots = (double)device_sms() * (tc ? 1 : 2);
+    const double slots = (double)device_sms() * 2;  // both kernels keep two CTAs per SM
     const int ctx = std::max(max_context_len, 1);
     p.part_tokens = 256;
     if (tc) {

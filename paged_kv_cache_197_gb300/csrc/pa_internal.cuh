@@ -91,8 +91,8 @@ int multi_cols_per_cta();
 cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream);
 // The log-sum-exp merge of multi-token partials (a programmatic dependent launch).
 cudaError_t launch_multi_merge(const MultiArgs &a, int D, int bs, cudaStream_t stream);
-// Whether multi-token attention of this shape runs on the tcgen05 kernel (one CTA per
-// SM) rather than the mma.sync one; plan and launch both follow it.
+// Whether multi-token attention of this shape runs on the tcgen05 kernel rather than
+// the mma.sync one; plan and launch both follow it.
 bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len);
 cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream);
 

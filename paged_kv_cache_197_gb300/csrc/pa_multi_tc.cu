@@ -5,24 +5,27 @@
 // What is computed is the same as the mma.sync kernel in pa_multi.cu (deeplearn.tn,
 // "Les leviers d'optimisation en production": a chunk of new tokens attends the
 // paged cache, each token up to its own position).  One CTA takes 128 columns of one
-// (sequence, kv head, context partition) and streams the partition in 128-token
-// tiles.  Its seven warps have fixed roles, coupled only through mbarriers:
+// (sequence, kv head, context partition) and streams the partition in 64-token
+// tiles; two CTAs share an SM (112 KB of shared memory and 256 tensor-memory columns
+// each), so one's softmax overlaps the other's products.  Its seven warps have fixed
+// roles, coupled only through mbarriers:
 //   * warp 4 copies K tiles, warp 5 V tiles, into two stages each by TMA: per cache
 //     block, two boxes of 64 dims x block-size rows with the 128-byte swizzle, so a
 //     staged tile is the K-major layout the tensor core reads (the block ids come
 //     from the table, one lane per block; entries outside the pool and blocks past
 //     the partition are copied from past the end of the pool, i.e. as zeros);
-//   * warp 6 issues, from one lane, S_t = Q K_t^T (M 128 columns x N 128 tokens,
+//   * warp 6 issues, from one lane, S_t = Q K_t^T (M 128 columns x N 64 tokens,
 //     K 128 dims; two tensor-memory buffers, so S of the next tile is computed while
-//     this one is turned into P) and O += P_t V_t (N 128 dims, K 128 tokens; V read
-//     as an MN-major operand from the same staged tile), and commits each to the
+//     this one is turned into P) and O += P_t V_t (N 128 dims, K 64 tokens; V read as
+//     an MN-major operand from the same staged tile), and commits each to the
 //     barriers that free the stages and wake the row warps;
 //   * warps 0-3 own one row each (tensor-memory lane = thread): they read the row's
 //     scores, mask tokens past its position, keep a running max (raised only when a
 //     tile's max exceeds it by more than 2^8 in the exp2 domain; O is then rescaled in
-//     tensor memory) and sum, write P in bf16 to shared memory in the swizzled
-//     K-major layout, and finally write the output row or its (max, sum, output)
-//     partial for the merge kernel shared with the mma.sync path.
+//     tensor memory) and sum, write P in bf16 to shared memory in the swizzled K-major
+//     layout, and finally write the output row or its (max, sum, output) partial for
+//     the merge kernel shared with the mma.sync path.
+// Tensor memory: S buffers in columns 0-127, O in 128-255.
 // Every wait is bounded (PA_FLAG_TIMEOUT when one gives up; the outputs are then not
 // written).
 #include <cuda.h>
@@ -36,11 +39,17 @@ namespace {
 
 constexpr int kTcThreads = 128;
 constexpr int kTcRows = 128;  // columns per CTA: the M of both products
-constexpr int kTcTile = 128;  // cached tokens per tile: N of S, K of P V
+constexpr int kTcTile = 64;  // cached tokens per tile: N of S, K of P V
 constexpr int kTcD = 128;
 constexpr int kTcTileBytes = kTcTile * kTcD * 2;
-constexpr int kTcAtom = kTcTile * 128;  // one 64-dim half of a tile: 128 rows of 128 B
-constexpr int kTcSmem = 6 * kTcTileBytes + 1024;  // Q, K x2, V x2, P; 1024-byte alignment
+constexpr int kTcAtom = kTcTile * 128;  // one 64-dim half of a K/V tile: kTcTile rows of 128 B
+constexpr int kQAtom = kTcRows * 128;   // one 64-element half of Q or P: 128 rows of 128 B
+constexpr int kQBytes = kTcRows * kTcD * 2;
+constexpr int kPBytes = kTcRows * kTcTile * 2;
+constexpr int kOffK = kQBytes, kOffV = kOffK + 2 * kTcTileBytes, kOffP = kOffV + 2 * kTcTileBytes;
+// Q, K x2, V x2, P, then the barriers inside the 1 KB kept for alignment: 113 KB, so
+// two CTAs fit an SM
+constexpr int kTcSmem = kOffP + kPBytes + 1024;
 constexpr float kTcRescaleLog2 = 8.0f;
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
@@ -166,7 +175,7 @@ __device__ __forceinline__ uint32_t tc_bf16x2(float lo, float hi) {
 // Byte offset of the 16-byte chunk ch (8 bf16 values, ch in [0, 16)) of row r in a
 // 128-row, 128-element K-major tile with 128-byte swizzle.
 __device__ __forceinline__ uint32_t sw128_chunk(int r, int ch) {
-    return (ch >> 3) * kTcAtom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4);
+    return (ch >> 3) * kQAtom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4);
 }
 
 __device__ __forceinline__ void mbar_init_n(uint32_t bar, uint32_t n) {
@@ -193,13 +202,18 @@ struct TcShared {
 };
 
 template <int BS>
-__global__ void __launch_bounds__(kTcAllThreads, 1)
+__global__ void __launch_bounds__(kTcAllThreads, 2)
 multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap) {
-    extern __shared__ unsigned char dsm[];
-    __shared__ TcShared sh;
+    extern __shared__ __align__(1024) unsigned char dsm[];
     unsigned char *base = dsm + ((1024 - (tc_smem(dsm) & 1023)) & 1023);
-    unsigned char *Qs = base, *Ps = base + 5 * kTcTileBytes;
+    // the barriers follow the tiles, inside the 1 KB kept for alignment
+    if ((size_t)(base - dsm) + kOffP + kPBytes + sizeof(TcShared) > (size_t)kTcSmem) {
+        if (threadIdx.x == 0) tc_raise(a.err_flag, PA_FLAG_TIMEOUT);
+        return;
+    }
+    TcShared &sh = *reinterpret_cast<TcShared *>(base + kOffP + kPBytes);
+    unsigned char *Qs = base, *Ps = base + kOffP;
     const uint32_t q_s = tc_smem(Qs), p_s = tc_smem(Ps);
 
     const int part = blockIdx.x;
@@ -269,7 +283,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the tensor core
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(tc_smem(&sh.taddr))
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(tc_smem(&sh.taddr))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -277,7 +291,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.taddr;
-    const uint32_t t_o = tmem + 256;  // O: columns 256..383; S buffers at 0 and 128
+    const uint32_t t_o = tmem + 128;  // O: columns 128..255; S buffers at 0 and 64
 
     if (warp == 4 || warp == 5) {
         // ---- copies: K (warp 4) or V (warp 5) tiles into their two stages; the whole
@@ -309,7 +323,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             if (lane == 0) mbar_expect(tc_smem(is_k ? &sh.kfull[st] : &sh.vfull[st]), kTcTileBytes);
             __syncwarp();
             const uint32_t bar = tc_smem(is_k ? &sh.kfull[st] : &sh.vfull[st]);
-            const uint32_t dst = tc_smem(base + ((is_k ? 1 : 3) + st) * kTcTileBytes);
+            const uint32_t dst = tc_smem(base + (is_k ? kOffK : kOffV) + st * kTcTileBytes);
 #pragma unroll
             for (int i = 0; i < kTcTile / BS; ++i) {
                 const int yi = __shfl_sync(0xffffffffu, y, i);
@@ -330,12 +344,12 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             if (!__all_sync(0xffffffffu, ok)) return false;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t kb = tc_smem(base + (1 + st) * kTcTileBytes);
+                const uint32_t kb = tc_smem(base + kOffK + st * kTcTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTcD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kTcAtom + (kk & 3) * 32;
-                    umma(tmem + st * 128, sw128_desc(q_s + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
-                         bf16_idesc(128, 128, 0), kk > 0);
+                    const uint32_t w = (kk & 3) * 32;
+                    umma(tmem + st * kTcTile, sw128_desc(q_s + (kk >> 2) * kQAtom + w, 16, 1024),
+                         sw128_desc(kb + (kk >> 2) * kTcAtom + w, 16, 1024), bf16_idesc(128, kTcTile, 0), kk > 0);
                 }
                 umma_commit(tc_smem(&sh.sfull[st]));
                 umma_commit(tc_smem(&sh.kfree[st]));
@@ -355,10 +369,10 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t vb = tc_smem(base + (3 + st) * kTcTileBytes);
+                const uint32_t vb = tc_smem(base + kOffV + st * kTcTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kTcTile / 16; ++kk)
-                    umma(t_o, sw128_desc(p_s + (kk >> 2) * kTcAtom + (kk & 3) * 32, 16, 1024),
+                    umma(t_o, sw128_desc(p_s + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024),
                          sw128_desc(vb + kk * 2048, kTcAtom, 1024), bf16_idesc(128, 128, 1), (j > 0 || kk > 0));
                 umma_commit(tc_smem(&sh.odone));
                 umma_commit(tc_smem(&sh.vfree[st]));
@@ -379,7 +393,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             tc_fence_after();
             float sv[kTcTile];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + st * 128 + 32 * q, sv + 32 * q);
+            for (int q = 0; q < kTcTile / 32; ++q) tmem_ld32(tmem + lane_off + st * kTcTile + 32 * q, sv + 32 * q);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(tc_smem(&sh.sfree[st]));
@@ -434,7 +448,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             const float mb = m_run == -INFINITY ? 0.f : m_run;
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
+            for (int ch = 0; ch < kTcTile / 8; ++ch) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -453,9 +467,12 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
                 ok = mbar_wait(tc_smem(&sh.vfull[st]), (j >> 1) & 1);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 const int r_hi = min(kTcTile, (tok_end + BS - 1) / BS * BS - k0);
-                unsigned char *vst = base + (3 + st) * kTcTileBytes;
-                for (int i = tid; i < (r_hi - r_lo) * 16; i += kTcRows)
-                    *reinterpret_cast<uint4 *>(vst + sw128_chunk(r_lo + i / 16, i % 16)) = make_uint4(0u, 0u, 0u, 0u);
+                unsigned char *vst = base + kOffV + st * kTcTileBytes;
+                for (int i = tid; i < (r_hi - r_lo) * 16; i += kTcRows) {
+                    const int r = r_lo + i / 16, ch = i % 16;
+                    *reinterpret_cast<uint4 *>(vst + (ch >> 3) * kTcAtom + (r >> 3) * 1024 + (r & 7) * 128 +
+                                               (((ch & 7) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor core
             tc_fence_before();
@@ -500,7 +517,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     if (tid == 0 && sh.abort) tc_raise(a.err_flag, PA_FLAG_TIMEOUT);
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem) : "memory");
 }
 
 }  // namespace

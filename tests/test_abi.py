@@ -173,9 +173,9 @@ def test_shared_prefix_workspace_and_checks(lib):
 
 
 def test_multi_token_workspace_and_checks(lib):
-    """Multi-token attention: 128 (token, head) columns per CTA.  On the tcgen05 path
-    (bf16 cache, head_dim 128, max_query_len * G >= 64; one CTA per SM) no partition
-    unless the CTAs fill less than half the SMs, then about one wave of partitions
+    """Multi-token attention: 128 (token, head) columns per CTA, two CTAs per SM.  On
+    the tcgen05 path (bf16 cache, head_dim 128, max_query_len * G >= 64) no partition
+    unless the CTAs fill less than half the slots, then about one wave of partitions
     (multiples of 128 tokens, at least 512).  Otherwise no partition when the columns
     give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the best of
     (last-wave fill) x (len / (len + 256)) over 4096..256-token partitions with >= 2
@@ -191,8 +191,8 @@ def test_multi_token_workspace_and_checks(lib):
         units = S * Hkv * cb
         ctx = max(max_ctx, 1)
         if D == 128 and max_q * G >= 64:
-            if units < sms / 2:
-                want = math.ceil(sms / units)
+            if units < sms:
+                want = math.ceil(2 * sms / units)
                 return max(512, -(-(-(-ctx // want)) // 128) * 128)
             return -(-ctx // 64) * 64
         slots = 2 * sms
