@@ -498,9 +498,11 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int kv_dtype, 
     const double slots = (double)device_sms() * 2;  // both kernels keep two CTAs per SM
     const int ctx = std::max(max_context_len, 1);
     p.part_tokens = 256;
-    if (tc) {
-        // whole contexts (partials and their merge cost more than a ragged last wave),
-        // unless the CTAs would fill less than half the SMs: then about one wave
+    if (tc && (int64_t)max_query_len * G >= 64) {
+        // chunks of half a tile of columns and more (compute-heavy): whole contexts
+        // (partials and their merge cost more than a ragged last wave), unless the CTAs
+        // would fill less than half the slots, then about one wave; narrower chunks
+        // (streaming-bound) are planned like the mma.sync kernel's
         p.part_tokens = (int)align_up((size_t)ctx, 64);
         if ((double)units < slots / 2) {
             const int64_t want = (int64_t)std::ceil(slots / (double)units);

@@ -1,6 +1,6 @@
 // Multi-token paged attention on the fifth-generation tensor cores (tcgen05), for
-// bf16 caches with head_dim 128: the prefill-shaped case, where a kv head of a
-// sequence has at least half a tile (64) of (new token, query head) columns.
+// bf16 caches with head_dim 128, when a kv head of a sequence has at least 16 (new
+// token, query head) columns: prefill chunks and draft verification.
 //
 // What is computed is the same as the mma.sync kernel in pa_multi.cu (deeplearn.tn,
 // "Les leviers d'optimisation en production": a chunk of new tokens attends the
@@ -38,6 +38,9 @@ namespace pa {
 namespace {
 
 constexpr int kTcThreads = 128;
+// Narrower chunks (decode-like steps) stay on the mma.sync kernel; from 16 (token, head)
+// columns per kv head up the staged K/V serve enough rows to pay for the idle ones.
+constexpr int kTcMinCols = 16;
 constexpr int kTcRows = 128;  // columns per CTA: the M of both products
 constexpr int kTcTile = 64;  // cached tokens per tile: N of S, K of P V
 constexpr int kTcD = 128;
@@ -583,7 +586,7 @@ cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream) {
 }
 
 bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len) {
-    return kv_dtype == PA_KV_BF16 && D == kTcD && (int64_t)max_query_len * G >= kTcRows / 2;
+    return kv_dtype == PA_KV_BF16 && D == kTcD && (int64_t)max_query_len * G >= kTcMinCols;
 }
 
 }  // namespace pa

@@ -174,9 +174,9 @@ def test_shared_prefix_workspace_and_checks(lib):
 
 def test_multi_token_workspace_and_checks(lib):
     """Multi-token attention: 128 (token, head) columns per CTA, two CTAs per SM.  On
-    the tcgen05 path (bf16 cache, head_dim 128, max_query_len * G >= 64) no partition
-    unless the CTAs fill less than half the slots, then about one wave of partitions
-    (multiples of 128 tokens, at least 512).  Otherwise no partition when the columns
+    the tcgen05 path with chunks of at least 64 columns (bf16 cache, head_dim 128,
+    max_query_len * G >= 64) no partition unless the CTAs fill less than half the
+    slots, then about one wave of partitions (multiples of 128 tokens, at least 512).  Otherwise no partition when the columns
     give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the best of
     (last-wave fill) x (len / (len + 256)) over 4096..256-token partitions with >= 2
     waves (256 as the fallback).  The workspace holds (D + 2) fp32 per query row, head
