@@ -68,8 +68,8 @@ NCU_TRAFFIC = {
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
     ("fp8", "0a92d8beb0508d47"): 3144265472 + 5437952,
     ("prefix", "0a92d8beb0508d47"): 72100608 + 1082624,
-    ("verify70b", "e18995d7f6cbf9f4"): 656804608 + 18492928,
-    ("prefill8b", "bb03486cc05af7b6"): 84019968 + 3249152,
+    ("verify70b", "59527d4a4065d25c"): 656769792 + 18477312,
+    ("prefill8b", "59527d4a4065d25c"): 83939072 + 3315968,
     ("verify70b_fp8", "e18995d7f6cbf9f4"): 339669248 + 19878144,
     ("prefill8b_fp8", "e18995d7f6cbf9f4"): 51451648 + 84620800,
 }

@@ -6,18 +6,18 @@
 // "Les leviers d'optimisation en production": a chunk of new tokens attends the
 // paged cache, each token up to its own position).  One CTA takes 128 columns of one
 // (sequence, kv head, context partition) and streams the partition in 64-token
-// tiles; two CTAs share an SM (112 KB of shared memory and 256 tensor-memory columns
+// tiles; two CTAs share an SM (113 KB of shared memory and 256 tensor-memory columns
 // each), so one's softmax overlaps the other's products.  Its seven warps have fixed
 // roles, coupled only through mbarriers:
-//   * warp 4 copies K tiles, warp 5 V tiles, into two stages each by TMA: per cache
+//   * warp 4 copies K tiles, warp 5 V tiles, into three stages each by TMA: per cache
 //     block, two boxes of 64 dims x block-size rows with the 128-byte swizzle, so a
 //     staged tile is the K-major layout the tensor core reads (the block ids come
 //     from the table, one lane per block; entries outside the pool and blocks past
 //     the partition are copied from past the end of the pool, i.e. as zeros);
 //   * warp 6 issues, from one lane, S_t = Q K_t^T (M 128 columns x N 64 tokens,
-//     K 128 dims; two tensor-memory buffers, so S of the next tile is computed while
-//     this one is turned into P) and O += P_t V_t (N 128 dims, K 64 tokens; V read as
-//     an MN-major operand from the same staged tile), and commits each to the
+//     K 128 dims; Q from tensor memory, where the row threads put it, K from the
+//     staged tile) and O += P_t V_t (N 128 dims, K 64 tokens; P from shared memory, V
+//     read as an MN-major operand from the same staged tile), and commits each to the
 //     barriers that free the stages and wake the row warps;
 //   * warps 0-3 own one row each (tensor-memory lane = thread): they read the row's
 //     scores, mask tokens past its position, keep a running max (raised only when a
@@ -25,7 +25,7 @@
 //     tensor memory) and sum, write P in bf16 to shared memory in the swizzled K-major
 //     layout, and finally write the output row or its (max, sum, output) partial for
 //     the merge kernel shared with the mma.sync path.
-// Tensor memory: S buffers in columns 0-127, O in 128-255.
+// Tensor memory: S in columns 0-63, Q (bf16 pairs) 64-127, O 128-255.
 // Every wait is bounded (PA_FLAG_TIMEOUT when one gives up; the outputs are then not
 // written).
 #include <cuda.h>
@@ -37,7 +37,6 @@
 namespace pa {
 namespace {
 
-constexpr int kTcThreads = 128;
 // Narrower chunks (decode-like steps) stay on the mma.sync kernel; from 16 (token, head)
 // columns per kv head up the staged K/V serve enough rows to pay for the idle ones.
 constexpr int kTcMinCols = 16;
@@ -47,11 +46,13 @@ constexpr int kTcD = 128;
 constexpr int kTcTileBytes = kTcTile * kTcD * 2;
 constexpr int kTcAtom = kTcTile * 128;  // one 64-dim half of a K/V tile: kTcTile rows of 128 B
 constexpr int kQAtom = kTcRows * 128;   // one 64-element half of Q or P: 128 rows of 128 B
-constexpr int kQBytes = kTcRows * kTcD * 2;
 constexpr int kPBytes = kTcRows * kTcTile * 2;
-constexpr int kOffK = kQBytes, kOffV = kOffK + 2 * kTcTileBytes, kOffP = kOffV + 2 * kTcTileBytes;
-// Q, K x2, V x2, P, then the barriers inside the 1 KB kept for alignment: 113 KB, so
-// two CTAs fit an SM
+constexpr int kTcStages = 3;  // K and V tiles in flight per CTA
+constexpr int kOffK = 0, kOffV = kOffK + kTcStages * kTcTileBytes, kOffP = kOffV + kTcStages * kTcTileBytes;
+// tensor memory columns: S (single buffer), Q (bf16 pairs), O
+constexpr uint32_t kTmemS = 0, kTmemQ = 64, kTmemO = 128;
+// K x3, V x3, P, then the barriers inside the 1 KB kept for alignment: 113 KB, so two
+// CTAs fit an SM
 constexpr int kTcSmem = kOffP + kPBytes + 1024;
 constexpr float kTcRescaleLog2 = 8.0f;
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
@@ -119,6 +120,15 @@ __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_
     asm volatile(
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// The same with A (M x 16 bf16) read from tensor memory: lane = row, column c holding
+// elements 2c (low half) and 2c + 1.
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -196,9 +206,9 @@ constexpr int kTcWarps = 7;
 constexpr int kTcAllThreads = kTcWarps * 32;
 
 struct TcShared {
-    uint64_t kfull[2], vfull[2];  // tile landed (TMA transaction count)
-    uint64_t kfree[2], vfree[2];  // stage consumed by S_t / by P V_t (tcgen05.commit)
-    uint64_t sfull[2], sfree[2];  // S_t in tensor memory / read by all 128 rows
+    uint64_t kfull[kTcStages], vfull[kTcStages];  // tile landed (TMA transaction count)
+    uint64_t kfree[kTcStages], vfree[kTcStages];  // stage consumed by S_t / by P V_t
+    uint64_t sfull, sfree;        // S_t in tensor memory / read by all 128 rows
     uint64_t pfull, odone;        // P_t written by all rows / P V_t done
     uint32_t taddr;
     int abort;
@@ -216,8 +226,8 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         return;
     }
     TcShared &sh = *reinterpret_cast<TcShared *>(base + kOffP + kPBytes);
-    unsigned char *Qs = base, *Ps = base + kOffP;
-    const uint32_t q_s = tc_smem(Qs), p_s = tc_smem(Ps);
+    unsigned char *Ps = base + kOffP;
+    const uint32_t p_s = tc_smem(Ps);
 
     const int part = blockIdx.x;
     const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
@@ -260,31 +270,21 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     const int lim_p = min(lim, tok_end - 1);     // ... inside this partition
     int64_t pair = 0;
     if (has) pair = (int64_t)(r0 + ctok(c)) * a.Hq + kvh * a.G + chead(c);
-    if (row_thread) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + pair * kTcD);
-#pragma unroll 4
-        for (int ch = 0; ch < 16; ++ch) {
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (has) x = __ldg(src + ch);
-            *reinterpret_cast<uint4 *>(Qs + sw128_chunk(tid, ch)) = x;
-        }
-    }
     if (tid == 0) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kTcStages; ++i) {
             mbar_init(tc_smem(&sh.kfull[i]));
             mbar_init(tc_smem(&sh.vfull[i]));
             mbar_init(tc_smem(&sh.kfree[i]));
             mbar_init(tc_smem(&sh.vfree[i]));
-            mbar_init(tc_smem(&sh.sfull[i]));
-            mbar_init_n(tc_smem(&sh.sfree[i]), kTcRows);
         }
+        mbar_init(tc_smem(&sh.sfull));
+        mbar_init_n(tc_smem(&sh.sfree), kTcRows);
         mbar_init_n(tc_smem(&sh.pfull), kTcRows);
         mbar_init(tc_smem(&sh.odone));
         sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the tensor core
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(tc_smem(&sh.taddr))
                      : "memory");
@@ -294,7 +294,29 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.taddr;
-    const uint32_t t_o = tmem + 128;  // O: columns 128..255; S buffers at 0 and 64
+    const uint32_t t_o = tmem + kTmemO;
+    // the row's query into tensor memory (lane = row), as bf16 pairs: the A operand of S
+    if (row_thread) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + pair * kTcD);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                if (has) x = __ldg(src + 8 * h + i);
+                w[4 * i] = __uint_as_float(x.x);
+                w[4 * i + 1] = __uint_as_float(x.y);
+                w[4 * i + 2] = __uint_as_float(x.z);
+                w[4 * i + 3] = __uint_as_float(x.w);
+            }
+            tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + kTmemQ + 32 * h, w);
+        }
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     if (warp == 4 || warp == 5) {
         // ---- copies: K (warp 4) or V (warp 5) tiles into their two stages; the whole
@@ -304,7 +326,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         const int oob_row = a.N * a.Hkv * BS;  // a row past the pool: the copy fills zeros
 #pragma unroll 1
         for (int t = 0; t < ntile; ++t) {
-            const int st = t & 1;
+            const int st = t % kTcStages, use = t / kTcStages;
             // lane i < 128 / BS reads the table entry of the tile's block i; entries
             // outside [0, N) are flagged (once, by the K copies of the first column
             // block) and read as zeros, like blocks past the partition
@@ -318,7 +340,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
                     tc_raise(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
             }
             bool ok = true;
-            if (t >= 2) ok = mbar_wait(tc_smem(is_k ? &sh.kfree[st] : &sh.vfree[st]), ((t >> 1) - 1) & 1);
+            if (use > 0) ok = mbar_wait(tc_smem(is_k ? &sh.kfree[st] : &sh.vfree[st]), (use - 1) & 1);
             if (__any_sync(0xffffffffu, !ok || sh.abort != 0)) {
                 if (lane == 0 && !ok) atomicOr(&sh.abort, 1);
                 break;
@@ -341,9 +363,9 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         // ---- tensor-core products in the order S_0, S_1, PV_0, S_2, PV_1, ...: the
         // whole warp waits, lane 0 issues
         auto issue_s = [&](int t) -> bool {
-            const int st = t & 1;
-            bool ok = mbar_wait(tc_smem(&sh.kfull[st]), (t >> 1) & 1);
-            if (ok && t >= 2) ok = mbar_wait(tc_smem(&sh.sfree[st]), ((t >> 1) - 1) & 1);
+            const int st = t % kTcStages;
+            bool ok = mbar_wait(tc_smem(&sh.kfull[st]), (t / kTcStages) & 1);
+            if (ok && t >= 1) ok = mbar_wait(tc_smem(&sh.sfree), (t - 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) return false;
             tc_fence_after();
             if (lane == 0) {
@@ -351,10 +373,10 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
 #pragma unroll
                 for (int kk = 0; kk < kTcD / 16; ++kk) {
                     const uint32_t w = (kk & 3) * 32;
-                    umma(tmem + st * kTcTile, sw128_desc(q_s + (kk >> 2) * kQAtom + w, 16, 1024),
-                         sw128_desc(kb + (kk >> 2) * kTcAtom + w, 16, 1024), bf16_idesc(128, kTcTile, 0), kk > 0);
+                    umma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, sw128_desc(kb + (kk >> 2) * kTcAtom + w, 16, 1024),
+                            bf16_idesc(128, kTcTile, 0), kk > 0);
                 }
-                umma_commit(tc_smem(&sh.sfull[st]));
+                umma_commit(tc_smem(&sh.sfull));
                 umma_commit(tc_smem(&sh.kfree[st]));
             }
             __syncwarp();
@@ -363,9 +385,9 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         bool ok = issue_s(0);
 #pragma unroll 1
         for (int j = 0; ok && j < ntile; ++j) {
-            const int st = j & 1;
+            const int st = j % kTcStages;
             if (j + 1 < ntile) ok = issue_s(j + 1);
-            if (ok) ok = mbar_wait(tc_smem(&sh.pfull), j & 1) && mbar_wait(tc_smem(&sh.vfull[st]), (j >> 1) & 1);
+            if (ok) ok = mbar_wait(tc_smem(&sh.pfull), j & 1) && mbar_wait(tc_smem(&sh.vfull[st]), (j / kTcStages) & 1);
             if (!__all_sync(0xffffffffu, ok && sh.abort == 0)) {
                 ok = false;
                 break;
@@ -390,16 +412,16 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         bool ok = true;
 #pragma unroll 1
         for (int j = 0; j < ntile; ++j) {
-            const int st = j & 1;
-            ok = mbar_wait(tc_smem(&sh.sfull[st]), (j >> 1) & 1);
+            const int st = j % kTcStages;
+            ok = mbar_wait(tc_smem(&sh.sfull), j & 1);
             if (__any_sync(0xffffffffu, !ok || sh.abort != 0)) { ok = false; break; }
             tc_fence_after();
             float sv[kTcTile];
 #pragma unroll
-            for (int q = 0; q < kTcTile / 32; ++q) tmem_ld32(tmem + lane_off + st * kTcTile + 32 * q, sv + 32 * q);
+            for (int q = 0; q < kTcTile / 32; ++q) tmem_ld32(tmem + lane_off + kTmemS + 32 * q, sv + 32 * q);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(tc_smem(&sh.sfree[st]));
+            mbar_arrive(tc_smem(&sh.sfree));
 
             // masked row max, eight independent chains
             const int k0 = tok_begin + j * kTcTile;
@@ -467,7 +489,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             // anything (a zero weight times a NaN is a NaN): zero them in the V stage
             const int r_lo = tok_end - k0;
             if (j == ntile - 1 && r_lo < kTcTile && tok_end % BS != 0) {
-                ok = mbar_wait(tc_smem(&sh.vfull[st]), (j >> 1) & 1);
+                ok = mbar_wait(tc_smem(&sh.vfull[st]), (j / kTcStages) & 1);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 const int r_hi = min(kTcTile, (tok_end + BS - 1) / BS * BS - k0);
                 unsigned char *vst = base + kOffV + st * kTcTileBytes;
