@@ -68,10 +68,12 @@ NCU_TRAFFIC = {
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
     ("fp8", "0a92d8beb0508d47"): 3144265472 + 5437952,
     ("prefix", "0a92d8beb0508d47"): 72100608 + 1082624,
-    ("verify70b", "59527d4a4065d25c"): 656769792 + 18477312,
-    ("prefill8b", "59527d4a4065d25c"): 83939072 + 3315968,
-    ("verify70b_fp8", "e18995d7f6cbf9f4"): 339669248 + 19878144,
-    ("prefill8b_fp8", "e18995d7f6cbf9f4"): 51451648 + 84620800,
+    ("verify70b", "f513785ccf40a75c"): 656770304 + 18690304,
+    ("prefill8b", "f513785ccf40a75c"): 83939840 + 3395072,
+    ("verify70b_fp8", "7cb2d2e42b085f49"): 339659008 + 19772672,
+    # the tcgen05 kernel reading the dequantised bf16 pool (the pass before it reads the
+    # 8-bit blocks once)
+    ("prefill8b_fp8", "f513785ccf40a75c"): 83939840 + 3159808,
 }
 
 
@@ -85,12 +87,12 @@ def measured_peaks() -> dict:
 
 
 def multi_kernel_source(case) -> str:
-    """The source of the kernel a multi-token call runs: the tcgen05 kernel for bf16
-    caches with head_dim 128 and at least 16 (token, head) columns per kv head (the
-    library's own dispatch rule), else the mma.sync one."""
+    """The source of the kernel a multi-token call runs: the tcgen05 kernel for head_dim
+    128 and at least 16 (token, head) columns per kv head with a bf16 cache, 64 with an
+    8-bit one (the library's own dispatch rule), else the mma.sync one."""
     qs = case.query_start.cpu()
     max_q = int((qs[1:] - qs[:-1]).max())
-    if case.kv_dtype == "bf16" and case.D == 128 and max_q * (case.Hq // case.Hkv) >= 16:
+    if case.D == 128 and max_q * (case.Hq // case.Hkv) >= (16 if case.kv_dtype == "bf16" else 64):
         return "pa_multi_tc.cu"
     return "pa_multi.cu"
 

@@ -263,11 +263,15 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
  *   workspace       pa_multi_token_workspace_size(...) bytes (NULL when that is 0);
  *                   contents not preserved.
  * bf16, int8 and fp8 caches (k_scale, v_scale required for the last two); other
- * arguments as pa_decode.  8-bit entries are dequantised on their way through shared
- * memory as fp16 code x scale (the scale rounded to fp16, the product rounded once),
- * the query rows as fp16 scaled by a power of two per row; the products are fp16 with
- * fp32 accumulation.  The dequantised values must lie within fp16's range (|x| <=
- * 65504, the scale above fp16's smallest normal 2^-14 for full precision).
+ * arguments as pa_decode.  With head_dim 128 and max_query_len * Hq / Hkv >= 64
+ * (prefill-shaped calls), 8-bit entries of the attended blocks are first dequantised
+ * into the workspace as bf16 (code x scale, rounded once) and the products are bf16
+ * with fp32 accumulation, as for a bf16 cache.  Otherwise 8-bit entries are
+ * dequantised on their way through shared memory as fp16 code x scale (the scale
+ * rounded to fp16, the product rounded once), the query rows as fp16 scaled by a power
+ * of two per row; the products are fp16 with fp32 accumulation, and the dequantised
+ * values must lie within fp16's range (|x| <= 65504, the scale above fp16's smallest
+ * normal 2^-14 for full precision).
  */
 size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
                                      int max_context_len, int max_query_len);

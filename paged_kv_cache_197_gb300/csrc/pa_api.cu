@@ -482,13 +482,17 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
 struct MultiPlan {
     int CB, part_tokens, max_parts;
     size_t acc_off, ml_off, bytes;
+    // 8-bit caches on the tcgen05 kernel: Mq bf16 blocks per sequence and an identity
+    // table in the workspace (Mq = 0: none)
+    int Mq;
+    size_t kq_off, vq_off, tab_off;
 };
 
 // Fixed cost of one multi-token CTA (q fragments, the join of token slices, the
 // writes) in tokens of streaming: larger than the decode kernel's.
 constexpr double kMultiRampTokens = 256.0;
 
-static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int kv_dtype, int max_context_len,
+static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len,
                             int max_query_len) {
     MultiPlan p{};
     const int G = Hq / Hkv;
@@ -526,11 +530,22 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int kv_dtype, 
         }
     }
     p.max_parts = (ctx + p.part_tokens - 1) / p.part_tokens;
-    if (p.max_parts == 1) return p;
-    const size_t rows = (size_t)T * Hq * p.max_parts;
-    p.acc_off = 0;
-    p.ml_off = align_up(rows * D * sizeof(float), 256);
-    p.bytes = align_up(p.ml_off + rows * 2 * sizeof(float), 256);
+    size_t end = 0;
+    if (p.max_parts > 1) {
+        const size_t rows = (size_t)T * Hq * p.max_parts;
+        p.acc_off = 0;
+        p.ml_off = align_up(rows * D * sizeof(float), 256);
+        end = align_up(p.ml_off + rows * 2 * sizeof(float), 256);
+    }
+    if (tc && kv_dtype != PA_KV_BF16) {
+        p.Mq = (ctx + bs - 1) / bs;
+        const size_t pool = (size_t)S * p.Mq * Hkv * bs * D * 2;
+        p.kq_off = end;
+        p.vq_off = align_up(p.kq_off + pool, 256);
+        p.tab_off = align_up(p.vq_off + pool, 256);
+        end = align_up(p.tab_off + (size_t)S * p.Mq * sizeof(int32_t), 256);
+    }
+    p.bytes = end;
     return p;
 }
 
@@ -553,7 +568,7 @@ size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int b
     if (check_multi_args("pa_multi_token_workspace_size", S, T, Hq, Hkv, D, bs, kv_dtype,
                          max_context_len, max_query_len) != PA_OK)
         return 0;
-    return plan_multi(S, T, Hq, Hkv, D, kv_dtype, max_context_len, max_query_len).bytes;
+    return plan_multi(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len).bytes;
 }
 
 pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
@@ -583,7 +598,7 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
         return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
     if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
         return fail(PA_ERR_INVALID_ARG, "%s: scale must be finite", fn);
-    const MultiPlan plan = plan_multi(S, T, Hq, Hkv, D, kv_dtype, max_context_len, max_query_len);
+    const MultiPlan plan = plan_multi(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len);
     if (plan.bytes && (!workspace || workspace_bytes < plan.bytes))
         return fail(PA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, plan.bytes,
                     workspace ? workspace_bytes : (size_t)0);
@@ -599,8 +614,8 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.query_start = query_start;
-    a.ws_acc = plan.bytes ? (float *)((char *)workspace + plan.acc_off) : nullptr;
-    a.ws_ml = plan.bytes ? (float *)((char *)workspace + plan.ml_off) : nullptr;
+    a.ws_acc = plan.max_parts > 1 ? (float *)((char *)workspace + plan.acc_off) : nullptr;
+    a.ws_ml = plan.max_parts > 1 ? (float *)((char *)workspace + plan.ml_off) : nullptr;
     a.err_flag = err_flag;
     a.M = M;
     a.S = S;
@@ -616,7 +631,24 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
     a.max_context_len = max_context_len;
     a.max_query_len = max_query_len;
     a.scale_log2 = scale * 1.4426950408889634f;
-    launch_multi_token(a, D, bs, kv_dtype, (cudaStream_t)stream);
+    if (plan.Mq > 0) {
+        // 8-bit cache, prefill-shaped: dequantise the attended blocks once, then the bf16
+        // kernel reads them through the identity table
+        uint16_t *kq = (uint16_t *)((char *)workspace + plan.kq_off);
+        uint16_t *vq = (uint16_t *)((char *)workspace + plan.vq_off);
+        int32_t *tab = (int32_t *)((char *)workspace + plan.tab_off);
+        launch_dequant_blocks(a, bs, kv_dtype, plan.Mq, kq, vq, tab, (cudaStream_t)stream);
+        MultiArgs b = a;
+        b.k_cache = kq;
+        b.v_cache = vq;
+        b.k_scale = b.v_scale = nullptr;
+        b.block_tables = tab;
+        b.M = plan.Mq;
+        b.N = S * plan.Mq;
+        launch_multi_token(b, D, bs, PA_KV_BF16, (cudaStream_t)stream);
+    } else {
+        launch_multi_token(a, D, bs, kv_dtype, (cudaStream_t)stream);
+    }
     return check_launch(fn);
 }
 

@@ -91,10 +91,15 @@ int multi_cols_per_cta();
 cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream);
 // The log-sum-exp merge of multi-token partials (a programmatic dependent launch).
 cudaError_t launch_multi_merge(const MultiArgs &a, int D, int bs, cudaStream_t stream);
-// Whether multi-token attention of this shape runs on the tcgen05 kernel rather than
-// the mma.sync one; plan and launch both follow it.
+// Whether multi-token attention of this shape runs on the tcgen05 kernel (8-bit caches
+// after the dequantising pass below) rather than the mma.sync one; plan and launch both
+// follow it.
 bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len);
-cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream);
+cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream);  // bf16 caches
+// 8-bit caches, prefill-shaped calls: the attended blocks dequantised into a bf16 pool
+// (Mq blocks per sequence) and an identity table, both in the workspace.
+cudaError_t launch_dequant_blocks(const MultiArgs &a, int bs, int kv_dtype, int Mq, uint16_t *kq, uint16_t *vq,
+                                  int32_t *tab, cudaStream_t stream);
 
 // ------------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing was launched).

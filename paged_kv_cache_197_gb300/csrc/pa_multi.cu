@@ -716,7 +716,7 @@ cudaError_t launch_multi_kv(const MultiArgs &a, int D, int bs, cudaStream_t stre
 }
 
 cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
-    if (multi_tc_eligible(D, kv_dtype, a.G, a.max_query_len)) return launch_multi_tc(a, bs, stream);
+    if (kv_dtype == PA_KV_BF16 && multi_tc_eligible(D, kv_dtype, a.G, a.max_query_len)) return launch_multi_tc(a, bs, stream);
     if (kv_dtype == PA_KV_INT8) return launch_multi_kv<int8_t>(a, D, bs, stream);
     if (kv_dtype == PA_KV_FP8) return launch_multi_kv<e4m3_tag>(a, D, bs, stream);
     return launch_multi_kv<uint16_t>(a, D, bs, stream);

@@ -1,6 +1,7 @@
-// Multi-token paged attention on the fifth-generation tensor cores (tcgen05), for
-// bf16 caches with head_dim 128, when a kv head of a sequence has at least 16 (new
-// token, query head) columns: prefill chunks and draft verification.
+// Multi-token paged attention on the fifth-generation tensor cores (tcgen05) with
+// head_dim 128, when a kv head of a sequence has at least 16 (new token, query head)
+// columns: prefill chunks and draft verification on bf16 caches, prefill chunks on
+// 8-bit ones.
 //
 // What is computed is the same as the mma.sync kernel in pa_multi.cu (deeplearn.tn,
 // "Les leviers d'optimisation en production": a chunk of new tokens attends the
@@ -28,9 +29,16 @@
 // Tensor memory: S in columns 0-63, Q (bf16 pairs) 64-127, O 128-255.
 // Every wait is bounded (PA_FLAG_TIMEOUT when one gives up; the outputs are then not
 // written).
+// 8-bit caches take this kernel for prefill-shaped chunks (64 columns and more) after a
+// pass that dequantises the blocks each sequence attends, once, into a bf16 pool in
+// the workspace (dequant_blocks_kernel below): converting inside this kernel would
+// repeat the work in every column block of a kv head.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "pa_internal.cuh"
 
@@ -204,6 +212,43 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 constexpr int kTcSoftmaxWarps = 4;
 constexpr int kTcWarps = 7;
 constexpr int kTcAllThreads = kTcWarps * 32;
+
+// Sixteen 8-bit codes as sixteen exact bf16 values (the caller applies the scales): e4m3 through the hardware conversion to fp16 (every e4m3 value is an fp16
+// and a bf16 value); int8 through the fp16 pattern 0x64XX = 1024 + XX with XX = x + 128,
+// less 1152 (exact), then fp16 -> fp32 -> bf16 (exact for |x| <= 127).
+template <typename KV>
+__device__ __forceinline__ void codes_to_bf16(const uint4 &c, uint4 &lo, uint4 &hi) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h[2];
+        if constexpr (std::is_same<KV, int8_t>::value) {
+            const uint32_t u = w[i] ^ 0x80808080u;
+            const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+            const uint32_t b0 = __byte_perm(u, 0x64646464u, 0x4140), b1 = __byte_perm(u, 0x64646464u, 0x4342);
+            const __half2 h0 = __hsub2(*reinterpret_cast<const __half2 *>(&b0), bias);
+            const __half2 h1 = __hsub2(*reinterpret_cast<const __half2 *>(&b1), bias);
+            h[0] = *reinterpret_cast<const uint32_t *>(&h0);
+            h[1] = *reinterpret_cast<const uint32_t *>(&h1);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint32_t pair = (w[i] >> (16 * k)) & 0xffffu;
+                asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+                    : "=r"(h[k])
+                    : "r"(pair));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[k]));
+            out[2 * i + k] = tc_bf16x2(f.x, f.y);
+        }
+    }
+    lo = make_uint4(out[0], out[1], out[2], out[3]);
+    hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
 
 struct TcShared {
     uint64_t kfull[kTcStages], vfull[kTcStages];  // tile landed (TMA transaction count)
@@ -601,14 +646,84 @@ cudaError_t launch_tc_typed(const MultiArgs &a, cudaStream_t stream) {
     return launch_multi_merge(a, kTcD, BS, stream);
 }
 
+struct tc_e4m3 {  // an fp8 (e4m3) cache entry
+    uint8_t bits;
+};
+
+// 8-bit caches, prefill-shaped calls: each block a sequence attends (its first
+// ceil(ctx / bs) table entries) is dequantised once -- code x scale, rounded to bf16 --
+// into a bf16 pool in the workspace, block i of sequence s at s * Mq + i, and row s of
+// an identity table in the workspace names it; the bf16 kernel then reads that pool.
+// A table entry outside [0, N) is flagged and its block written as zeros.
+template <typename KV, int BS>
+__global__ void __launch_bounds__(256) dequant_blocks_kernel(const __grid_constant__ MultiArgs a, int Mq,
+                                                             uint16_t *kq, uint16_t *vq, int32_t *tab) {
+    const int i = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int64_t dblk = (int64_t)s * Mq + i;
+    if (tid == 0) tab[dblk] = (int32_t)dblk;
+    int ctx = a.context_lens[s];
+    ctx = min(max(ctx, 0), min(a.M * BS, a.max_context_len));  // the attention kernel flags it
+    if (i >= (ctx + BS - 1) / BS) return;
+    const int b = a.block_tables[(int64_t)s * a.M + i];
+    const bool valid = b >= 0 && b < a.N;
+    if (!valid && tid == 0 && a.err_flag) atomicOr(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
+    const int rows = a.Hkv * BS;  // the block's rows, all kv heads
+#pragma unroll 1
+    for (int kv = 0; kv < 2; ++kv) {
+        const uint8_t *codes = static_cast<const uint8_t *>(kv ? a.v_cache : a.k_cache);
+        const float *scales = kv ? a.v_scale : a.k_scale;
+        uint16_t *dst = kv ? vq : kq;
+        for (int p = tid; p < rows * (kTcD / 16); p += 256) {
+            const int row = p / (kTcD / 16), q = p % (kTcD / 16);
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+            if (valid) {
+                const int64_t src_row = (int64_t)b * rows + row;
+                const uint4 c = __ldg(reinterpret_cast<const uint4 *>(codes + src_row * kTcD) + q);
+                const float sc = __ldg(scales + src_row);
+                codes_to_bf16<KV>(c, lo, hi);
+                const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                    o[e] = tc_bf16x2(f.x * sc, f.y * sc);
+                }
+                lo = make_uint4(o[0], o[1], o[2], o[3]);
+                hi = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            uint4 *out = reinterpret_cast<uint4 *>(dst + (dblk * rows + row) * kTcD) + 2 * q;
+            out[0] = lo;
+            out[1] = hi;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_blocks(const MultiArgs &a, int bs, int kv_dtype, int Mq, uint16_t *kq, uint16_t *vq,
+                                  int32_t *tab, cudaStream_t stream) {
+    const dim3 grid(Mq, a.S);
+    if (kv_dtype == PA_KV_INT8) {
+        if (bs == 16) dequant_blocks_kernel<int8_t, 16><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
+        else dequant_blocks_kernel<int8_t, 32><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
+    } else {
+        if (bs == 16) dequant_blocks_kernel<tc_e4m3, 16><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
+        else dequant_blocks_kernel<tc_e4m3, 32><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream) {
     return bs == 16 ? launch_tc_typed<16>(a, stream) : launch_tc_typed<32>(a, stream);
 }
 
 bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len) {
-    return kv_dtype == PA_KV_BF16 && D == kTcD && (int64_t)max_query_len * G >= kTcMinCols;
+    if (D != kTcD) return false;
+    const int64_t cols = (int64_t)max_query_len * G;
+    if (kv_dtype == PA_KV_BF16) return cols >= kTcMinCols;
+    // 8-bit caches: through the dequantising pass, which pays where the products
+    // dominate (prefill-shaped chunks)
+    return (kv_dtype == PA_KV_INT8 || kv_dtype == PA_KV_FP8) && cols >= kTcRows / 2;
 }
 
 }  // namespace pa

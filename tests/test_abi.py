@@ -225,9 +225,14 @@ def test_multi_token_workspace_and_checks(lib):
                   max_query_len=8), **k})
     assert ws() > 0
     assert ws(kv_dtype=pa.PA_KV_INT8) == ws() and ws(kv_dtype=pa.PA_KV_FP8) == ws()
-    # 16 tokens x 4 heads reach the tcgen05 path for bf16 only: 16 CTAs of columns fill
-    # less than half the SMs, so the contexts are split for one wave
-    assert ws(max_query_len=16) > 0 and ws(max_query_len=16) != ws(max_query_len=16, kv_dtype=pa.PA_KV_INT8)
+    # 16 tokens x 4 heads: the tcgen05 path's plan for every cache type (16 CTAs of
+    # columns fill less than half the SMs, so the contexts are split for one wave); an
+    # 8-bit cache adds the bf16 pool of the attended blocks (K and V) and its table
+    pool = 4 * (-(-8000 // 16)) * 2 * 16 * 128 * 2
+    table = up(4 * (-(-8000 // 16)) * 4)
+    for dt in (pa.PA_KV_INT8, pa.PA_KV_FP8):
+        assert ws(max_query_len=16, kv_dtype=dt) == ws(max_query_len=16) + 2 * up(pool) + table
+    assert ws(max_query_len=16, D=64) != ws(max_query_len=16)  # head_dim 64: the mma.sync plan
     assert ws(kv_dtype=7) == 0
     assert ws(max_query_len=0) == 0
     assert ws(max_query_len=65) == 0  # more than T rows
