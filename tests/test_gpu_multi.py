@@ -242,6 +242,32 @@ def test_tensor_core_error_flags(oracle):
     assert flag.item() == pa.PA_FLAG_CONTEXT_OUT_OF_RANGE
 
 
+@pytest.mark.parametrize("kv_dtype", ["int8", "fp8"])
+def test_eight_bit_prefill_pass_flags(oracle, kv_dtype):
+    """8-bit prefill-shaped chunks go through the dequantising pass: a block id beyond
+    the pool is flagged there and read as zeros, the other sequences stay exact, and
+    the workspace includes the bf16 pool."""
+    import paged_kv_cache_197_gb300 as pa
+
+    lens, qlen = [300, 700], [100, 64]
+    case = workloads.build_multi_case(f"q-flags-{kv_dtype}", S=2, Hq=16, Hkv=2, D=128, bs=16,
+                                      context_lens=lens, query_lens=qlen, seed=40, kv_dtype=kv_dtype)
+    base = pa.pa_multi_token_workspace_size(2, sum(qlen), 16, 2, 128, 16, pa.PA_KV_BF16, 700, 100)
+    code = {"int8": pa.PA_KV_INT8, "fp8": pa.PA_KV_FP8}[kv_dtype]
+    q8 = pa.pa_multi_token_workspace_size(2, sum(qlen), 16, 2, 128, 16, code, 700, 100)
+    assert q8 > base  # the pool of dequantised blocks
+    bad = workloads.PagedCase(**{**case.__dict__})
+    bad.block_tables = case.block_tables.clone()
+    bad.block_tables[1, 3] = case.N + 5
+    got = helpers.gpu_multi_step(bad, DEV)
+    assert got["flag"] == pa.PA_FLAG_BLOCK_OUT_OF_RANGE
+    assert torch.isfinite(got["out"][torch.arange(sum(qlen), device=DEV)].float()).all()
+    caches = helpers.oracle_caches(case, oracle)
+    sub, rows = _sequences(case, [0])
+    ref = helpers.oracle_multi_out(sub, oracle, caches)
+    helpers.compare(got["out"][rows.to(DEV)], ref, kv_dtype)
+
+
 def _sequences(case, seqs):
     """The case cut to the listed sequences (their query rows, tables and lengths)."""
     qs = case.query_start.cpu().tolist()
