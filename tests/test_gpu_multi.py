@@ -285,10 +285,11 @@ def _sequences(case, seqs):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["verify70b", "prefill8b"])
+@pytest.mark.parametrize("name", ["verify70b", "prefill8b", "verify70b_fp8", "prefill8b_fp8"])
 def test_full_size_sampled(oracle, name):
-    """The full-size multi-token workloads in the launch configuration bench.py times,
-    checked on a sample of sequences."""
+    """The full-size multi-token workloads in the launch configuration bench.py times
+    (bf16 and fp8 caches: both kernels and the dequantising pass), checked on a sample
+    of sequences."""
     case = workloads.CONFIGS[name](device="cpu", poison=True)
     got = helpers.gpu_multi_step(case, DEV)
     assert got["flag"] == 0
@@ -296,4 +297,4 @@ def test_full_size_sampled(oracle, name):
     seqs = [0, case.S - 1]
     sub, rows = _sequences(case, seqs)
     ref = helpers.oracle_multi_out(sub, oracle, caches)
-    helpers.compare(got["out"][rows.to(DEV)], ref, "bf16")
+    helpers.compare(got["out"][rows.to(DEV)], ref, case.kv_dtype)
