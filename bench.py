@@ -306,7 +306,7 @@ def run_ours(args, rank, world, device) -> dict | None:
         step = Step(case, device, stream, shared_prefix=args.shared_prefix)
     nbytes = step_bytes(case)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) \
-        if args.config in FLUSH_L2 else None
+        if args.config in FLUSH_L2 and not args.hot else None
 
     def barrier():
         if world > 1:
@@ -392,6 +392,7 @@ def run_ours(args, rank, world, device) -> dict | None:
                    "pool_blocks": case.N, "total_context_tokens": int(case.context_lens.sum()),
                    "parallelism": f"replicas x{world} (independent sequence shards)",
                    "l2": "flushed before each step" if flush is not None else
+                         "hot: not flushed (--hot)" if args.hot and args.config in FLUSH_L2 else
                          "K/V pools far larger than L2 (no flush needed)",
                    "bytes_per_step": nbytes},
         # tokens attended per second: one per sequence in decode, every new token in a
@@ -624,6 +625,9 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hot", action="store_true",
+                    help="no L2 flush between steps for the workloads that fit in L2 (the "
+                         "cached figure beside the default flushed one)")
     ap.add_argument("--shared-prefix", action="store_true",
                     help="decode through pa_decode_shared_prefix (workloads with a shared prefix)")
     ap.add_argument("--quick", action="store_true",
