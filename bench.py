@@ -543,11 +543,15 @@ def oracle_runner(orc, case, inputs):
         k_scale=ks, v_scale=vs)
 
 
-def time_oracle(case, inputs, budget_s: float) -> dict:
-    """Oracle decode over the first n sequences, n grown until the run takes ~budget_s."""
+def time_oracle(case, inputs, budget_s: float, threads: int | None = None) -> dict:
+    """Oracle decode over the first n sequences, n grown until the run takes ~budget_s
+    (on `threads` host threads, default all)."""
     import oracle
 
     orc = oracle.load()
+    all_threads = orc.num_threads
+    if threads is not None:
+        orc.set_num_threads(threads)
     n, elapsed = 1, 0.0
     run = oracle_runner(orc, case, inputs)
     while True:
@@ -568,7 +572,10 @@ def time_oracle(case, inputs, budget_s: float) -> dict:
     sub = first_sequences(case, n)
     nbytes = workloads.decode_algorithmic_bytes(sub)
     what = "multi-token attention" if case.query_start is not None else "decode"
-    return {"value": round(nbytes / elapsed / 1e9, 4), "unit": UNIT, "cores": orc.num_threads,
+    cores = orc.num_threads
+    if threads is not None:
+        orc.set_num_threads(all_threads)
+    return {"value": round(nbytes / elapsed / 1e9, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle", "seconds": round(elapsed, 3), "repeats": reps, "sequences": n,
             "sample": f"{what} of the first {n} of {case.S} sequences "
                       f"({int(sub.context_lens.sum())} context tokens), fp64 C oracle, "
@@ -576,8 +583,12 @@ def time_oracle(case, inputs, budget_s: float) -> dict:
 
 
 def cpu_baseline(args, case, step, budget_s=20.0) -> dict:
+    """The oracle on all host cores, with its single-core figure beside it."""
     inputs = oracle_sample_inputs(case, step)
-    return time_oracle(case, inputs, budget_s)
+    res = time_oracle(case, inputs, budget_s)
+    one = time_oracle(case, inputs, budget_s / 2, threads=1)
+    res["single_core"] = {"value": one["value"], "cores": one["cores"], "sample": one["sample"]}
+    return res
 
 
 def run_reference(args, rank, world) -> dict | None:

@@ -77,6 +77,8 @@ class Oracle:
         vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_version.restype = i32
         lib.oracle_num_threads.restype = i32
+        lib.oracle_set_num_threads.argtypes = [i32]
+        lib.oracle_set_num_threads.restype = None
         lib.oracle_slot.argtypes = [vp, i64, i32]
         lib.oracle_slot.restype = i64
         lib.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i64]
@@ -109,6 +111,10 @@ class Oracle:
     @property
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads of later calls (timing only: the results do not depend on it)."""
+        self.lib.oracle_set_num_threads(int(n))
 
     # ---------------------------------------------------------------- indexing
     def slot(self, table: np.ndarray, pos: int, bs: int) -> int:

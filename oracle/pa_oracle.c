@@ -566,3 +566,15 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Set the threads of later calls (n >= 1; no effect without OpenMP).  The results do
+   not depend on it: each (sequence, kv head) pair is computed by one thread in a fixed
+   order. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
