@@ -408,6 +408,9 @@ def run_ours(args, rank, world, device) -> dict | None:
         "clocks": clocks,
         "kernel_source": src_hash,
     }
+    if args.config == "gqa70b":
+        # the 70B model decodes through 80 such layers per token
+        res["decode_ms_80_layers"] = round(80 * dec_mean_ms, 3)
     if step.multi:
         tflops = flops / (dec_mean_ms * 1e-3) / 1e12
         res["config"]["new_tokens_per_seq"] = step.max_q
