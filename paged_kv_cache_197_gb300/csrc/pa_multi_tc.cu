@@ -364,7 +364,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     tc_fence_after();
 
     if (warp == 4 || warp == 5) {
-        // ---- copies: K (warp 4) or V (warp 5) tiles into their two stages; the whole
+        // ---- copies: K (warp 4) or V (warp 5) tiles into their three stages; the whole
         // warp follows the loop (waits), lane 0 issues
         const bool is_k = warp == 4;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
@@ -372,7 +372,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
 #pragma unroll 1
         for (int t = 0; t < ntile; ++t) {
             const int st = t % kTcStages, use = t / kTcStages;
-            // lane i < 128 / BS reads the table entry of the tile's block i; entries
+            // lane i < kTcTile / BS reads the table entry of the tile's block i; entries
             // outside [0, N) are flagged (once, by the K copies of the first column
             // block) and read as zeros, like blocks past the partition
             int y = oob_row;
