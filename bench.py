@@ -68,9 +68,10 @@ NCU_TRAFFIC = {
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
     ("fp8", "0a92d8beb0508d47"): 3144265472 + 5437952,
     ("prefix", "0a92d8beb0508d47"): 72100608 + 1082624,
-    ("verify70b", "91323db2ddaade17"): 656770816 + 18649600,
+    # five 1600-token partitions (balanced partition plan); their partials are the writes
+    ("verify70b", "91323db2ddaade17"): 656797696 + 13285120,
     ("prefill8b", "91323db2ddaade17"): 83940352 + 3092992,
-    ("verify70b_fp8", "7cb2d2e42b085f49"): 339659008 + 19772672,
+    ("verify70b_fp8", "5b771ca2846ad7f5"): 340236544 + 13805056,
     # the tcgen05 kernel reading the dequantised bf16 pool (the pass before it reads the
     # 8-bit blocks once)
     ("prefill8b_fp8", "91323db2ddaade17"): 83939328 + 3236096,

@@ -488,9 +488,14 @@ struct MultiPlan {
     size_t kq_off, vq_off, tab_off;
 };
 
-// Fixed cost of one multi-token CTA (q fragments, the join of token slices, the
-// writes) in tokens of streaming: larger than the decode kernel's.
-constexpr double kMultiRampTokens = 256.0;
+// Fixed cost of one multi-token CTA (q fragments or the tensor-memory setup, the join
+// of token slices, the writes, the partial rows the merge reads) in tokens of
+// streaming: larger than the decode kernel's.  Measured on GB300 with balanced
+// partitions, where the score at 256 tokens nearly tied two lengths the longer one
+// was faster: 70B-shaped 4-token verification 5 x 1600 tokens 129.2 us against
+// 7 x 1152 132.7 us; 64 x 3000-token contexts with 16 columns 2 x 1536 148.9 us
+// against 4 x 768 157.0 us.
+constexpr double kMultiRampTokens = 512.0;
 
 static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len,
                             int max_query_len) {
@@ -515,9 +520,19 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int bs, int kv
     } else if ((double)units >= 4.0 * slots && ctx <= 4096) {
         p.part_tokens = (int)align_up((size_t)ctx, 64);
     } else {
+        // n balanced partitions of the longest context (each a multiple of 64 tokens,
+        // so the last one is not a ragged remainder), n chosen by the same score as the
+        // decode plan's.  Against the former choice among 4096, 2048, ..., 256 tokens,
+        // measured on GB300: 70B-shaped 4-token verification 1024 -> 1600 tokens
+        // 134.2 -> 129.2 us (fp8 cache 259.8 -> 245.3), 64 x 3000-token contexts with
+        // 16 columns 2048 -> 1536 156.5 -> 148.9 us, 16 x 6000 with 8 columns 1024 -> 896
+        // 90.3 -> 85.9 us
         double best = -1.0;
-        for (int cand : {4096, 2048, 1024, 512, 256}) {
+        const int nmax = (ctx + 255) / 256;
+        for (int n = 1; n <= nmax; ++n) {
+            const int cand = std::min(4096, std::max(256, (int)align_up((size_t)((ctx + n - 1) / n), 64)));
             const int64_t parts = (ctx + cand - 1) / cand;
+            if (parts != n) continue;  // the same length as a smaller n
             const double waves = (double)(units * parts) / slots;
             if (waves < 2.0 && cand != 256) continue;
             const double fill = waves / std::ceil(waves);

@@ -620,6 +620,8 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
 // Log-sum-exp merge of a column's partitions: out = sum_p 2^(m_p - M) acc_p /
 // sum_p 2^(m_p - M) l_p, M = max_p m_p.  One warp per (new token, query head) of a
 // sequence (grid y); launched as a programmatic dependent of the attention kernel.
+// The workspace is 256-byte aligned and a partial row is D floats, so a lane's slice
+// of PER floats is a 16-byte (D 128) or 8-byte (D 64) aligned vector.
 template <int D, int BS>
 __global__ void __launch_bounds__(128) merge_multi_kernel(const __grid_constant__ MultiArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -651,11 +653,22 @@ __global__ void __launch_bounds__(128) merge_multi_kernel(const __grid_constant_
             lsum += f * ml.y;
         }
         const int cnt = min(32, nparts - p0);
+        // vector loads of whole lane slices, eight partitions' rows in flight at once
+#pragma unroll 8
         for (int q = 0; q < cnt; ++q) {
             const float fq = __shfl_sync(0xffffffffu, f, q);
             const float *src = a.ws_acc + (row0 + p0 + q) * D + lane * PER;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] += fq * src[e];
+            if constexpr (PER == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src);
+                acc[0] += fq * x.x;
+                acc[1] += fq * x.y;
+                acc[2] += fq * x.z;
+                acc[3] += fq * x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2 *>(src);
+                acc[0] += fq * x.x;
+                acc[1] += fq * x.y;
+            }
         }
     }
 #pragma unroll

@@ -178,9 +178,10 @@ def test_multi_token_workspace_and_checks(lib):
     max_query_len * G >= 64) no partition unless the CTAs fill less than half the
     slots, then about one wave of partitions (multiples of 128 tokens, at least 512).  Otherwise no partition when the columns
     give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the best of
-    (last-wave fill) x (len / (len + 256)) over 4096..256-token partitions with >= 2
-    waves (256 as the fallback).  The workspace holds (D + 2) fp32 per query row, head
-    and partition."""
+    (last-wave fill) x (len / (len + 512)) over n balanced partitions of the longest
+    context (ceil(ctx / n) rounded up to 64 tokens, 256..4096) with >= 2 waves (256 as
+    the fallback).  The workspace holds (D + 2) fp32 per query row, head and
+    partition."""
     import math
 
     import paged_kv_cache_197_gb300 as pa
@@ -199,13 +200,16 @@ def test_multi_token_workspace_and_checks(lib):
         if units >= 4 * slots and ctx <= 4096:
             return -(-ctx // 64) * 64
         best, best_p = -1.0, 256
-        for cand in (4096, 2048, 1024, 512, 256):
+        for n in range(1, (ctx + 255) // 256 + 1):
+            cand = min(4096, max(256, -(-(-(-ctx // n)) // 64) * 64))
             parts = -(-ctx // cand)
+            if parts != n:
+                continue
             waves = units * parts / slots
             if waves < 2 and cand != 256:
                 continue
             ln = min(cand, ctx)
-            score = waves / math.ceil(waves) * ln / (ln + 256)
+            score = waves / math.ceil(waves) * ln / (ln + 512)
             if score > best + 1e-9:
                 best, best_p = score, cand
         return best_p
