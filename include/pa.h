@@ -73,11 +73,17 @@ enum {
                                          sequence outside [0, T], decreasing, longer than
                                          its context or than max_query_len: its rows are
                                          not written                                      */
-    PA_FLAG_TIMEOUT = 32              /* a kernel's bounded wait for its own copies or
+    PA_FLAG_TIMEOUT = 32,             /* a kernel's bounded wait for its own copies or
                                          tensor-core products gave up, or its shared
                                          memory could not be laid out (the affected
                                          outputs are not written); not expected in normal
                                          operation                                        */
+    PA_FLAG_FP16_RANGE = 64           /* an 8-bit row staged as fp16 code x scale (the
+                                         shared prefix of pa_decode_shared_prefix, narrow
+                                         pa_multi_token_attention calls) has a scale whose
+                                         largest code leaves fp16's range (scale > 65504 /
+                                         127 for int8, > 65504 / 448 for fp8): the outputs
+                                         that attend it are not finite                    */
 };
 
 /* Version of this ABI (bumped on any signature change). */
@@ -302,7 +308,9 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and remembers it; make that first call before any stream
- * capture.  All calls on a device share the one array, so calls that overlap on
+ * capture.  The remembered address belongs to the device's primary context: after
+ * cudaDeviceReset on that device it is stale, so do not call this entry point
+ * again in a process that reset the device.  All calls on a device share the one array, so calls that overlap on
  * the GPU (on different streams, or from different threads without ordering) race
  * and may corrupt each other's results; order them on one stream.  Nothing in the
  * array needs to start at zero: each call writes every partial result it reads.

@@ -29,6 +29,7 @@ PA_FLAG_CONTEXT_OUT_OF_RANGE = 4
 PA_FLAG_PREFIX_MISMATCH = 8
 PA_FLAG_QUERY_OUT_OF_RANGE = 16
 PA_FLAG_TIMEOUT = 32
+PA_FLAG_FP16_RANGE = 64
 
 EXPORTED = ["pa_version", "pa_status_string", "pa_last_error_string", "pa_reshape_and_cache",
             "pa_quantize_kv", "pa_quantize_kv_fp8", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",

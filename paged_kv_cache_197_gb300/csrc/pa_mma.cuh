@@ -94,6 +94,14 @@ struct e4m3_tag {  // an fp8 (e4m3) cache entry
 // 0x64XX = 1024 + XX with XX = x + 128, less 1152; fp8 (e4m3) by the hardware
 // conversion (every e4m3 value is an fp16 value) -- then one fp16 multiply by the
 // scale (rounded to fp16) per pair.
+// Largest row scale whose staged values code x scale stay finite in fp16: the largest
+// code (127 for int8, 448 for e4m3) times the scale must not pass fp16's 65504.  Rows
+// with a larger scale are flagged (PA_FLAG_FP16_RANGE) by the kernels that stage them.
+template <typename KV>
+__host__ __device__ constexpr float max_f16_scale() {
+    return std::is_same<KV, int8_t>::value ? 65504.0f / 127.0f : 65504.0f / 448.0f;
+}
+
 template <typename KV>
 __device__ __forceinline__ void codes_to_f16(const uint4 &c, float scale, uint4 &lo, uint4 &hi) {
     const __half2 sc2 = __float2half2_rn(scale);

@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "pa_internal.cuh"
@@ -462,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
         constexpr int NPT = kChunk * QPR / kThreads;  // pieces per thread and chunk
         const char *kc8 = static_cast<const char *>(a.k_cache), *vc8 = static_cast<const char *>(a.v_cache);
         float ksr[NPT], vsr[NPT];
+        bool f16_over = false;  // a row whose code x scale leaves fp16's range
         auto issue_raw = [&](int j, int b) {
             const int c0 = tok_begin + j * kChunk;
             unsigned char *rb = raw + b * raw_chunk_bytes<D>();
@@ -485,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
                 }
                 cp_async16(smem_u32(rb + r * D + qc * 16), ksrc, bytes);
                 cp_async16(smem_u32(rb + kChunk * D + r * D + qc * 16), vsrc, bytes);
+                f16_over |= fmaxf(ksr[k], vsr[k]) > max_f16_scale<KV>();
             }
             cp_async_commit();
         };
@@ -520,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
             }
             __syncthreads();  // chunk j + 1 staged
         }
+        if (f16_over) raise_flag(a.err_flag, PA_FLAG_FP16_RANGE);
     }
     // the merge grid may launch now (it still waits for this grid before reading)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -682,14 +686,14 @@ __global__ void __launch_bounds__(128) merge_multi_kernel(const __grid_constant_
 template <typename KV, int D, int BS>
 cudaError_t launch_multi_typed(const MultiArgs &a, cudaStream_t stream) {
     constexpr int SMEM = sizeof(KV) == 1 ? multi_smem_bytes_q<D>() : multi_smem_bytes<D>();
-    static bool configured[64] = {false};
+    static std::atomic<bool> configured[64];  // per device: the shared-memory attribute is set
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(paged_multi_kernel<KV, D, BS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
     paged_multi_kernel<KV, D, BS><<<grid, kThreads, SMEM, stream>>>(a);

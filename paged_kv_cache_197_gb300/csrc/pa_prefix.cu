@@ -26,7 +26,10 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "pa_internal.cuh"
 #include "pa_mma.cuh"
@@ -227,6 +230,10 @@ __global__ void __launch_bounds__(kThreads) grouped_prefix_kernel(const __grid_c
                 vsr[k] = __ldg(a.v_scale + row);
             }
         }
+        bool over = false;  // a row whose code x scale leaves fp16's range
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) over |= fmaxf(ksr[k], vsr[k]) > max_f16_scale<KV>();
+        if (over) raise_flag(a.err_flag, PA_FLAG_FP16_RANGE);
 #pragma unroll
         for (int k = 0; k < NPT; ++k) {
             const int i = tid + k * kThreads, r = i / QPR, qc = i % QPR;
@@ -519,41 +526,48 @@ __global__ void __launch_bounds__(128) merge_prefix_kernel(const __grid_constant
 // The grouped prefix kernel does not depend on the own-token decode, so it runs on a
 // second stream of the library's, forked from and joined back to the caller's stream
 // with events (both captured as graph edges when the caller's stream is capturing).
+// Each (device, caller stream) pair gets its own side stream and events, created on
+// first use and kept until the process exits, so unrelated callers on different
+// streams never wait for each other.  Calls on one caller stream are ordered by that
+// stream; enqueueing on the same caller stream from several host threads at once is
+// not supported (as for any stream-ordered work).
 struct SideStream {
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
 };
 
-cudaError_t side_stream(int dev, SideStream *&out) {
-    static SideStream side[64];
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    SideStream &ss = side[dev];
+cudaError_t side_stream(int dev, cudaStream_t caller, SideStream *&out) {
+    static std::mutex mu;  // guards the map only
+    static std::map<std::pair<int, cudaStream_t>, SideStream> sides;
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream &ss = sides[{dev, caller}];
     if (!ss.stream) {
         cudaError_t e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            sides.erase({dev, caller});
+            return e;
+        }
     }
-    out = &ss;
+    out = &ss;  // std::map nodes never move
     return cudaSuccess;
 }
 
 template <typename KV, int D, int BS>
 cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, int kv_dtype, cudaStream_t stream) {
     constexpr int SMEM = 2 * kPrefixChunk * (D * 2 + 16);
-    static bool configured[64] = {false};
-    static std::mutex mu;  // one enqueue sequence at a time: the events are shared
-    std::lock_guard<std::mutex> lock(mu);
+    static std::atomic<bool> configured[64];  // per device: the shared-memory attribute is set
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(grouped_prefix_kernel<KV, D, BS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     SideStream *ss = nullptr;
-    cudaError_t err = side_stream(dev, ss);
+    cudaError_t err = side_stream(dev, stream, ss);
     if (err != cudaSuccess) return err;
     prefix_setup_kernel<<<(unsigned)((a.S + 7) / 8), 256, 0, stream>>>(a, p, BS);
     const bool grouped = p.n_groups > 0 && p.PP > 0;

@@ -398,6 +398,38 @@ def pin_fp8_quantizer(orc):
     assert ks[0, 0, 1] == 1.0 and not kc.any()
 
 
+def pin_fp8_divisor_by_hand(orc):
+    """The fp8 scale divisor is exactly 448, the largest finite e4m3 value: a row whose
+    absmax is 448 gets scale 1.0 exactly and its codes are e4m3 of the values
+    themselves, worked out by hand (448 -> 0x7e, -224 -> 0xf6, 3 -> 0x44, 2^-9 ->
+    0x01); a row whose absmax is 448 * 2^-5 gets scale 2^-5 exactly.  Two ties pin the
+    division's direction as well: 232 lies halfway between 224 and 240 and goes to 224
+    (even mantissa), 1.1875 halfway between 1.125 and 1.25 goes to 1.25 -- a divisor
+    slightly above 448 pushes 232 past the midpoint (-> 240), one slightly below pulls
+    1.1875 under it (-> 1.125)."""
+    D, bs = 8, 2
+    row = np.array([448.0, -224.0, 3.0, 2.0 ** -9, 232.0, 1.1875, 0.0, -448.0])
+    expect = [0x7E, 0xF6, 0x44, 0x01, 0x76, 0x3A, 0x00, 0xFE]
+    for shift, want_scale in ((0, 1.0), (-5, 2.0 ** -5)):
+        key = to_bf16_bits((row * 2.0 ** shift).reshape(1, 1, D))
+        assert np.array_equal(bf16_bits_to_f64(key).ravel(), row * 2.0 ** shift)
+        kc = np.zeros((1, 1, bs, D), dtype=np.uint8)
+        vc = np.zeros_like(kc)
+        ks = np.zeros((1, 1, bs), dtype=np.float32)
+        vs = np.zeros_like(ks)
+        assert orc.quantize_kv_fp8(key, key, kc, vc, ks, vs, np.array([1], dtype=np.int64), bs) == 0
+        assert ks[0, 0, 1] == np.float32(want_scale), ks[0, 0, 1]
+        assert kc[0, 0, 1].tolist() == expect, [hex(c) for c in kc[0, 0, 1]]
+        assert np.array_equal(kc, vc) and np.array_equal(ks, vs)
+    # and the division is IEEE fp32 (correctly rounded), not a multiply by 1/448: on rows
+    # of random magnitude every scale equals numpy's float32 quotient absmax / 448
+    rng = np.random.default_rng(9)
+    src = to_bf16_bits(rng.standard_normal((256, 16)) * rng.uniform(0.01, 100, size=(256, 1)))
+    _, scales = orc.quantize_pool(src, fp8=True)
+    amax = np.abs(bf16_bits_to_f64(src)).max(axis=1).astype(np.float32)
+    assert np.array_equal(scales, amax / np.float32(448.0))
+
+
 def pin_brute_force_fp8(orc):
     """fp8 cache: attention over e4m3 value x scale, against 40-digit brute force."""
     rng = np.random.default_rng(17)
@@ -488,7 +520,7 @@ def pin_prefill_causality(orc):
 ALL_PINS = [pin_slot_figure, pin_append_places_rows, pin_brute_force_bf16, pin_brute_force_int8,
             pin_closed_forms, pin_block_permutation_invariance, pin_prefix_shared_equals_copied,
             pin_softmax_weights, pin_quantizer_hand_values, pin_copy_blocks, pin_fp8_hand_values,
-            pin_fp8_round_trip_and_ties, pin_fp8_quantizer, pin_brute_force_fp8,
+            pin_fp8_round_trip_and_ties, pin_fp8_quantizer, pin_fp8_divisor_by_hand, pin_brute_force_fp8,
             pin_brute_force_prefill, pin_prefill_causality]
 
 

@@ -50,6 +50,9 @@ MUTANTS = {
     "fp8_decode_bias": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
     "fp8_no_saturation": ("    if (v > 448.0)\n        v = 448.0;\n", ""),
     "fp8_scale_127": ("absmax / 448.0f", "absmax / 127.0f"),
+    "fp8_scale_447": ("absmax / 448.0f", "absmax / 447.0f"),
+    "fp8_scale_449": ("absmax / 448.0f", "absmax / 449.0f"),
+    "fp8_scale_times_reciprocal": ("absmax / 448.0f", "absmax * (1.0f / 448.0f)"),
     "prefill_mask_excludes_self": ("int visible = ctx - L + i + 1;", "int visible = ctx - L + i;"),
     "prefill_no_causal_mask": ("int visible = ctx - L + i + 1;", "int visible = ctx;"),
     "prefill_row_ignores_start": ("int64_t row = (int64_t)query_start[s] + i;", "int64_t row = (int64_t)i;"),

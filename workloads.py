@@ -225,6 +225,41 @@ def build_multi_case(name: str, S: int, Hq: int, Hkv: int, D: int, bs: int, cont
     return case
 
 
+def widen_scales(case: PagedCase, lo: float, hi: float, seed: int, outlier_channels: int = 3,
+                 outlier_factor: float = 20.0) -> PagedCase:
+    """Give every cached and new K/V row (one token of one kv head) its own magnitude:
+    a few fixed channels per kv head are made outliers (x outlier_factor), then each row
+    is rescaled so that its largest |value| is 10^u, u uniform in [log10 lo, log10 hi],
+    and rounded to bf16.  With an 8-bit cache the per-token scales then span the same
+    decades (the dynamic per-token scale of the pages' quantised caches).  NaN poison
+    in unused slots stays NaN.  Modifies and returns the case."""
+    gen = _gen(seed + 7)
+    D, Hkv = case.D, case.Hkv
+    chan = torch.ones((Hkv, D), dtype=torch.float32)
+    for h in range(Hkv):
+        idx = torch.randperm(D, generator=gen)[:outlier_channels]
+        chan[h, idx] = outlier_factor
+
+    def rescale(rows: torch.Tensor, head_axis: int) -> torch.Tensor:
+        x = rows.float()
+        shape = [1] * x.dim()
+        shape[head_axis] = Hkv
+        shape[-1] = D
+        x = x * chan.reshape(shape)
+        amax = torch.nan_to_num(x.abs(), nan=0.0).amax(dim=-1, keepdim=True)
+        u = torch.rand(amax.shape, generator=gen, dtype=torch.float64)
+        target = torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo))).float()
+        return (x * torch.where(amax > 0, target / amax, torch.zeros_like(amax))).to(torch.bfloat16)
+
+    dev = case.k_pool.device
+    case.k_pool = rescale(case.k_pool.cpu(), 1).to(dev)
+    case.v_pool = rescale(case.v_pool.cpu(), 1).to(dev)
+    case.new_key = rescale(case.new_key.cpu(), 1).to(dev)
+    case.new_value = rescale(case.new_value.cpu(), 1).to(dev)
+    case.meta["scale_range"] = (lo, hi)
+    return case
+
+
 # --------------------------------------------------------------------------- configs
 def tiny(seed: int = 0, device="cpu", poison=True) -> PagedCase:
     return build_case("tiny", S=4, Hq=2, Hkv=2, D=64, bs=16, context_lens=[1, 17, 40, 100],
