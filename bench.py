@@ -1,19 +1,26 @@
 """Benchmark of the paged decode step on GB300.
 
-One step = the whole hot path of one decode step of one layer over one batch:
-copy-on-write block copies (prefix workload), append (bf16) or quantise-append
-(int8) of each sequence's new token, then paged decode attention (+ the partition
-merge).  Inputs are seeded and synthetic (workloads.py) and live in HBM before the
-timed region; K/V pools of every workload but `tiny` and `prefix` exceed the 126 MB
-L2, and those two get an L2 flush before every timed step.
+One step = the whole hot path of one decode step over one batch: copy-on-write block
+copies (prefix workload), append (bf16) or quantise-append (int8, fp8) of each
+sequence's new token, then paged decode attention (+ the partition merge).  The
+default workload is the Llama-3-70B-shaped GQA batch (20 sequences x 8000 tokens) run
+through 80 layers, each with its own K/V pools (80 x 655 MB = 52.4 GB resident in
+HBM), its own queries and new tokens, back to back on one stream: a step is one decode
+step of the whole 80-layer model's attention.  Other workloads run one layer
+(`--config`, `--layers`).  Inputs are seeded and synthetic (workloads.py) and live in
+HBM before the timed region; K/V pools of every workload but `tiny`, `prefix` and the
+prefill chunks exceed the 126 MB L2, and those get an L2 flush before every timed step.
 
 Prints ONE JSON line (rank 0).  `value` is whole-job effective bandwidth: the
 algorithmic bytes of all steps on all ranks / the slowest rank's time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config mha13b] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config gqa70b] [--layers L]
+                  [--impl ours|reference]
 
---impl reference times the CPU oracle (fp64 C, all host cores) on a bounded sample
-of the same workload: the comparison baseline, not a target.
+--gpus N without a torchrun environment starts N local ranks itself (one per GPU,
+independent replicas).  --impl reference times the CPU oracle (fp64 C, all host
+cores) on a bounded sample of the same workload: the comparison baseline, not a
+target.
 """
 from __future__ import annotations
 
@@ -76,6 +83,25 @@ NCU_TRAFFIC = {
     # 8-bit blocks once)
     ("prefill8b_fp8", "91323db2ddaade17"): 83939328 + 3236096,
 }
+
+
+# the nominal HBM3e bandwidth of one GB300 (about 8 TB/s), beside the measured copy rate
+NOMINAL_HBM_GBS = 8000.0
+# default number of layers per step: the 70B-shaped workload runs a whole model's 80
+# layers (distinct pools); the others one layer
+DEFAULT_LAYERS = {"gqa70b": 80}
+
+
+def fragmentation_side_metric(case) -> dict:
+    """KV capacity wasted by reserving each sequence's longest allowed context
+    contiguously versus by paging (the pages' comparison: 60-80% against under 4%).  The
+    reservation is the workload's longest context rounded up to a power of two."""
+    longest = int(case.context_lens.max())
+    reserve = 1 << max(0, (longest - 1).bit_length())
+    f = workloads.fragmentation(case, reserve)
+    return {"reserved_tokens_per_seq": reserve,
+            "contiguous_waste": round(f["contiguous_waste"], 4),
+            "paged_waste": round(f["paged_waste"], 4)}
 
 
 def measured_peaks() -> dict:
@@ -182,10 +208,21 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------- steps
-class Step:
-    """The device buffers and the calls of one decode step of one workload."""
+class Layer:
+    """One layer's device state: its K/V pools (and scales), queries, new tokens, output."""
 
-    def __init__(self, case: workloads.PagedCase, device, stream, shared_prefix=False):
+    def __init__(self, k_cache, v_cache, k_scale, v_scale, q, new_key, new_value, out):
+        self.k_cache, self.v_cache, self.k_scale, self.v_scale = k_cache, v_cache, k_scale, v_scale
+        self.q, self.new_key, self.new_value, self.out = q, new_key, new_value, out
+
+
+class Step:
+    """The device buffers and the calls of one decode step of one workload, over
+    `layers` layers that share the batch's block tables, lengths and slots (as the
+    layers of one model do) but each hold their own cache, queries and new tokens."""
+
+    def __init__(self, case: workloads.PagedCase, device, stream, shared_prefix=False, layers=1,
+                 seed=0):
         import paged_kv_cache_197_gb300 as pa
 
         self.pa = pa
@@ -195,26 +232,41 @@ class Step:
         c = case
         self.int8 = c.kv_dtype in ("int8", "fp8")  # quantised cache with per-token scales
         self.quant = pa.pa_quantize_kv_fp8 if c.kv_dtype == "fp8" else pa.pa_quantize_kv
-        if self.int8:
-            N, Hkv, bs, D = c.k_pool.shape
-            self.k_cache = torch.empty((N, Hkv, bs, D), dtype=torch.uint8 if c.kv_dtype == "fp8" else torch.int8,
-                                       device=device)
-            self.v_cache = torch.empty_like(self.k_cache)
-            self.k_scale = torch.empty((N, Hkv, bs), dtype=torch.float32, device=device)
-            self.v_scale = torch.empty_like(self.k_scale)
-            slots = torch.arange(N * bs, dtype=torch.int64, device=device)
-            rows = lambda p: p.permute(0, 2, 1, 3).reshape(N * bs, Hkv, D).contiguous()  # noqa: E731
-            self.quant(rows(c.k_pool), rows(c.v_pool), self.k_cache, self.v_cache,
-                       self.k_scale, self.v_scale, slots, stream=stream)
-            torch.cuda.synchronize(device)
-            self.source = (c.k_pool.cpu(), c.v_pool.cpu())  # for the CPU baseline only
-            c.k_pool = c.v_pool = None  # the bf16 source is not part of the step
-            torch.cuda.empty_cache()
-        else:
-            self.k_cache, self.v_cache = c.k_pool, c.v_pool
-            self.k_scale = self.v_scale = None
+        self.layers = []
+        pool_shape = tuple(c.k_pool.shape)
+        for li in range(layers):
+            if li == 0:
+                k_src, v_src, q, nk, nv = c.k_pool, c.v_pool, c.q, c.new_key, c.new_value
+            else:  # the next layer: fresh values of the same shapes, same bookkeeping
+                g = torch.Generator(device=device)
+                g.manual_seed(seed * 1000 + li)
+                rnd = lambda shape: torch.randn(shape, generator=g, device=device,  # noqa: E731
+                                                dtype=torch.float32).to(torch.bfloat16)
+                q, nk, nv = rnd(c.q.shape), rnd(c.new_key.shape), rnd(c.new_value.shape)
+                k_src, v_src = rnd(pool_shape), rnd(pool_shape)
+            if self.int8:
+                N, Hkv, bs, D = pool_shape
+                k_cache = torch.empty((N, Hkv, bs, D),
+                                      dtype=torch.uint8 if c.kv_dtype == "fp8" else torch.int8,
+                                      device=device)
+                v_cache = torch.empty_like(k_cache)
+                k_scale = torch.empty((N, Hkv, bs), dtype=torch.float32, device=device)
+                v_scale = torch.empty_like(k_scale)
+                slots = torch.arange(N * bs, dtype=torch.int64, device=device)
+                rows = lambda p: p.permute(0, 2, 1, 3).reshape(N * bs, Hkv, D).contiguous()  # noqa: E731
+                self.quant(rows(k_src), rows(v_src), k_cache, v_cache, k_scale, v_scale, slots,
+                           stream=stream)
+                torch.cuda.synchronize(device)
+                if li == 0:
+                    self.source = (c.k_pool.cpu(), c.v_pool.cpu())  # for the CPU baseline only
+                    c.k_pool = c.v_pool = None  # the bf16 source is not part of the step
+                del k_src, v_src
+                torch.cuda.empty_cache()
+            else:
+                k_cache, v_cache, k_scale, v_scale = k_src, v_src, None, None
+            self.layers.append(Layer(k_cache, v_cache, k_scale, v_scale, q, nk, nv,
+                                     torch.empty_like(c.q)))
         self.max_ctx = int(c.context_lens.max())
-        self.out = torch.empty_like(c.q)
         self.flag = torch.zeros(1, dtype=torch.int32, device=device)
         self.cow = c.cow_pairs.cpu()
         cow_launches = math.ceil(self.cow.shape[0] / 256) if self.cow.shape[0] else 0
@@ -222,68 +274,72 @@ class Step:
         self.prefix = int(c.meta.get("prefix_tokens", 0)) if shared_prefix else 0
         if shared_prefix and not self.prefix:
             raise SystemExit("--shared-prefix needs a workload with a shared prefix")
+        k0 = self.layers[0].k_cache
         if self.multi:
             self.max_q = max(c.meta["query_lens"])
             n = pa.pa_multi_token_workspace_size(c.S, c.q.shape[0], c.Hq, c.Hkv, c.D, c.bs,
-                                                 pa.kv_dtype_of(self.k_cache), self.max_ctx,
-                                                 self.max_q)
+                                                 pa.kv_dtype_of(k0), self.max_ctx, self.max_q)
             self.ws = torch.empty(n, dtype=torch.uint8, device=device) if n else None
             # append + attention (+ merge when split) + COW copies
-            self.launches = 1 + 1 + (1 if self.ws is not None else 0) + cow_launches
+            per_layer = 1 + 1 + (1 if self.ws is not None else 0) + cow_launches
         elif self.prefix:
             # one group: every sequence of the batch shares the prompt's blocks
             self.group_start = torch.tensor([0, c.S], dtype=torch.int32, device=device)
             self.group_prefix = torch.tensor([self.prefix], dtype=torch.int32, device=device)
             n = pa.pa_decode_shared_prefix_workspace_size(c.S, c.Hq, c.Hkv, c.D, c.bs,
-                                                          pa.kv_dtype_of(self.k_cache),
+                                                          pa.kv_dtype_of(k0),
                                                           self.max_ctx, c.S, self.prefix)
             self.ws = torch.empty(n, dtype=torch.uint8, device=device)
             # append + COW copies + setup, grouped prefix, own-token decode, merge
-            self.launches = 1 + cow_launches + 4
+            per_layer = 1 + cow_launches + 4
         else:
-            self.ws = pa.decode_workspace(c.q, self.k_cache, self.max_ctx)
+            self.ws = pa.decode_workspace(c.q, k0, self.max_ctx)
             # append (or quantise-append) + decode (+ merge when split) + COW copies
-            self.launches = 1 + 1 + (1 if self.ws is not None else 0) + cow_launches
+            per_layer = 1 + 1 + (1 if self.ws is not None else 0) + cow_launches
+        self.launches = per_layer * len(self.layers)
 
-    def write_cache(self, new_key, new_value, slots):
+    def write_cache(self, L: Layer, new_key, new_value, slots):
         if self.cow.shape[0]:
-            self.pa.pa_copy_blocks(self.k_cache, self.v_cache, self.cow, k_scale=self.k_scale,
-                                   v_scale=self.v_scale, stream=self.stream)
+            self.pa.pa_copy_blocks(L.k_cache, L.v_cache, self.cow, k_scale=L.k_scale,
+                                   v_scale=L.v_scale, stream=self.stream)
         if self.int8:
-            self.quant(new_key, new_value, self.k_cache, self.v_cache, self.k_scale,
-                       self.v_scale, slots, err_flag=self.flag, stream=self.stream)
+            self.quant(new_key, new_value, L.k_cache, L.v_cache, L.k_scale, L.v_scale, slots,
+                       err_flag=self.flag, stream=self.stream)
         else:
-            self.pa.pa_reshape_and_cache(new_key, new_value, self.k_cache, self.v_cache, slots,
+            self.pa.pa_reshape_and_cache(new_key, new_value, L.k_cache, L.v_cache, slots,
                                          err_flag=self.flag, stream=self.stream)
 
-    def decode(self, q, tables, lens, out, query_start=None):
+    def decode(self, L: Layer, q, tables, lens, out, query_start=None):
         if self.multi:
             self.pa.pa_multi_token_attention(
-                out, q, self.k_cache, self.v_cache, tables, lens,
+                out, q, L.k_cache, L.v_cache, tables, lens,
                 self.case.query_start if query_start is None else query_start, self.case.scale,
-                self.max_ctx, self.max_q, workspace=self.ws, k_scale=self.k_scale,
-                v_scale=self.v_scale, err_flag=self.flag, stream=self.stream)
+                self.max_ctx, self.max_q, workspace=self.ws, k_scale=L.k_scale,
+                v_scale=L.v_scale, err_flag=self.flag, stream=self.stream)
             return
         if self.prefix:
-            self.pa.pa_decode_shared_prefix(out, q, self.k_cache, self.v_cache, tables, lens,
+            self.pa.pa_decode_shared_prefix(out, q, L.k_cache, L.v_cache, tables, lens,
                                             self.case.scale, self.max_ctx, self.group_start,
                                             self.group_prefix, self.case.S, self.prefix,
-                                            workspace=self.ws, k_scale=self.k_scale,
-                                            v_scale=self.v_scale, err_flag=self.flag,
+                                            workspace=self.ws, k_scale=L.k_scale,
+                                            v_scale=L.v_scale, err_flag=self.flag,
                                             stream=self.stream)
             return
-        self.pa.pa_decode(out, q, self.k_cache, self.v_cache, tables, lens, self.case.scale,
-                          self.max_ctx, workspace=self.ws, k_scale=self.k_scale,
-                          v_scale=self.v_scale, err_flag=self.flag, stream=self.stream)
+        self.pa.pa_decode(out, q, L.k_cache, L.v_cache, tables, lens, self.case.scale,
+                          self.max_ctx, workspace=self.ws, k_scale=L.k_scale,
+                          v_scale=L.v_scale, err_flag=self.flag, stream=self.stream)
 
     def run(self, dec_events=None):
+        """One step: every layer's append and decode in order.  dec_events, if given,
+        holds one (start, end) event pair per layer around its decode call."""
         c = self.case
-        self.write_cache(c.new_key, c.new_value, c.slot_mapping)
-        if dec_events is not None:
-            dec_events[0].record(self.stream)
-        self.decode(c.q, c.block_tables, c.context_lens, self.out)
-        if dec_events is not None:
-            dec_events[1].record(self.stream)
+        for li, L in enumerate(self.layers):
+            self.write_cache(L, L.new_key, L.new_value, c.slot_mapping)
+            if dec_events is not None:
+                dec_events[li][0].record(self.stream)
+            self.decode(L, L.q, c.block_tables, c.context_lens, L.out)
+            if dec_events is not None:
+                dec_events[li][1].record(self.stream)
 
 
 def step_bytes(case) -> dict:
@@ -304,8 +360,10 @@ def run_ours(args, rank, world, device) -> dict | None:
     with torch.cuda.stream(stream):
         case = maker(seed=replica_seed(args.seed, rank), device=device, poison=False)
         torch.cuda.synchronize(device)
-        step = Step(case, device, stream, shared_prefix=args.shared_prefix)
+        step = Step(case, device, stream, shared_prefix=args.shared_prefix, layers=args.layers,
+                    seed=replica_seed(args.seed, rank))
     nbytes = step_bytes(case)
+    n_layers = len(step.layers)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) \
         if args.config in FLUSH_L2 and not args.hot else None
 
@@ -330,8 +388,8 @@ def run_ours(args, rank, world, device) -> dict | None:
             torch.cuda.synchronize(device)
     barrier()
     t0 = time.time()
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    dec_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_layers)] for _ in range(args.steps)]
     if flush is None:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
@@ -353,7 +411,7 @@ def run_ours(args, rank, world, device) -> dict | None:
         total_ms = sum(a.elapsed_time(b) for a, b in spans)
     t1 = time.time()
     clocks = sampler.stop(t_w, t1)
-    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    dec_ms = [a.elapsed_time(b) for per_step in dec_ev for a, b in per_step]
     assert int(step.flag.item()) == 0, f"kernel error flag {int(step.flag.item())}"
 
     # slowest rank sets the job time
@@ -382,7 +440,7 @@ def run_ours(args, rank, world, device) -> dict | None:
     src_hash = kernel_source_hash(multi_kernel_source(case) if step.multi else
                                   "pa_prefix.cu" if step.prefix else "pa_decode.cu")
     traffic = NCU_TRAFFIC.get((args.config, src_hash))
-    value = whole_job_gbs(nbytes["total"], world, ms_per_step)
+    value = whole_job_gbs(nbytes["total"] * n_layers, world, ms_per_step)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -395,23 +453,32 @@ def run_ours(args, rank, world, device) -> dict | None:
                    "l2": "flushed before each step" if flush is not None else
                          "hot: not flushed (--hot)" if args.hot and args.config in FLUSH_L2 else
                          "K/V pools far larger than L2 (no flush needed)",
-                   "bytes_per_step": nbytes},
-        # tokens attended per second: one per sequence in decode, every new token in a
-        # multi-token step
-        "tokens_per_s_per_layer": round(case.q.shape[0] * world / (ms_per_step * 1e-3), 1),
+                   "layers": n_layers,
+                   "bytes_per_layer": nbytes},
+        # tokens attended per second and layer: one per sequence in decode, every new
+        # token in a multi-token step (a step covers n_layers layers)
+        "tokens_per_s_per_layer": round(case.q.shape[0] * n_layers * world / (ms_per_step * 1e-3), 1),
         "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": traffic, "kernel": kernel_name,
-                     "peak_source": peaks["source"], "mean_decode_us": round(dec_mean_ms * 1e3, 2)},
+                     "peak_source": peaks["source"], "mean_decode_us": round(dec_mean_ms * 1e3, 2),
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "decode_calls_timed": len(dec_ms)},
+        "fragmentation": fragmentation_side_metric(case),
         "e2e": e2e,
         "gpu_launches": step.launches * args.steps,
         "clocks": clocks,
         "kernel_source": src_hash,
     }
-    if args.config == "gqa70b":
-        # the 70B model decodes through 80 such layers per token
-        res["decode_ms_80_layers"] = round(80 * dec_mean_ms, 3)
+    if n_layers > 1:
+        # the whole model's attention for one decode step, measured: every layer's append
+        # and decode back to back on one stream, each layer on its own pools
+        res["model_step"] = {"layers": n_layers, "ms": round(ms_per_step, 4),
+                             "decode_calls_ms": round(n_layers * dec_mean_ms, 4),
+                             "tokens_per_s": round(case.q.shape[0] * world / (ms_per_step * 1e-3), 1),
+                             "resident_kv_gb": round(n_layers * nbytes["decode"] / 1e9, 2)}
     if step.multi:
         tflops = flops / (dec_mean_ms * 1e-3) / 1e12
         res["config"]["new_tokens_per_seq"] = step.max_q
@@ -459,22 +526,29 @@ def pack_inputs(tensors: dict, device) -> tuple:
 
 def run_e2e(args, step, case, device, stream, world) -> dict:
     """Same step through the public API with the step's inputs in pinned host memory:
-    each step copies its queries, new K/V, slots, tables and lengths to the device (one
-    copy of a packed buffer) and reads the output back, all inside the timed region."""
-    keys = ["q", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens"]
+    each step copies every layer's queries and new K/V, and the batch's slots, tables
+    and lengths, to the device (one copy of a packed buffer) and reads every layer's
+    output back, all inside the timed region.  The K/V caches are resident state, like
+    weights."""
+    tensors = {k: getattr(case, k).cpu() for k in ("slot_mapping", "block_tables", "context_lens")}
     if step.multi:
-        keys.append("query_start")
-    host_buf, dev_buf, dev, h2d = pack_inputs({k: getattr(case, k).cpu() for k in keys}, device)
-    out_host = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
+        tensors["query_start"] = case.query_start.cpu()
+    for li, L in enumerate(step.layers):
+        for k in ("q", "new_key", "new_value"):
+            tensors[f"{k}{li}"] = getattr(L, k).cpu()
+    host_buf, dev_buf, dev, h2d = pack_inputs(tensors, device)
+    outs = torch.empty((len(step.layers),) + tuple(case.q.shape), dtype=case.q.dtype, device=device)
+    out_host = torch.empty(outs.shape, dtype=case.q.dtype).pin_memory()
     d2h = out_host.numel() * out_host.element_size()
     steps = max(3, min(args.steps, 200))
 
     def one():
         dev_buf.copy_(host_buf, non_blocking=True)
-        step.write_cache(dev["new_key"], dev["new_value"], dev["slot_mapping"])
-        step.decode(dev["q"], dev["block_tables"], dev["context_lens"], step.out,
-                    query_start=dev.get("query_start"))
-        out_host.copy_(step.out, non_blocking=True)
+        for li, L in enumerate(step.layers):
+            step.write_cache(L, dev[f"new_key{li}"], dev[f"new_value{li}"], dev["slot_mapping"])
+            step.decode(L, dev[f"q{li}"], dev["block_tables"], dev["context_lens"], outs[li],
+                        query_start=dev.get("query_start"))
+        out_host.copy_(outs, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -489,7 +563,7 @@ def run_e2e(args, step, case, device, stream, world) -> dict:
         b.record(stream)
         torch.cuda.synchronize(device)
     ms = slowest_rank([a.elapsed_time(b) / steps], device)[0]
-    total = step_bytes(case)["total"]
+    total = step_bytes(case)["total"] * len(step.layers)
     return {"value": round(whole_job_gbs(total, world, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 5),
             "steps": steps, "h2d_copies_per_step": 1}
@@ -606,6 +680,7 @@ def run_reference(args, rank, world) -> dict | None:
         return None
     case = workloads.CONFIGS[args.config](seed=args.seed, device="cpu", poison=False)
     inputs = oracle_sample_inputs(case)
+    oracle.load().set_num_threads(os.cpu_count() or 1)  # a launcher may have set one thread
     per_step = min(3.0, 120.0 / (args.warmup + args.steps))
     info = time_oracle(case, inputs, budget_s=4 * per_step)  # calibrates n
     n = info["sequences"]
@@ -630,12 +705,32 @@ def run_reference(args, rank, world) -> dict | None:
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def free_port() -> int:
+    import socket
+
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        return sock.getsockname()[1]
+
+
+def launch_ranks(n: int, argv: list[str]) -> int:
+    """Run this script as n local ranks (torch.distributed.run, rendezvous on
+    127.0.0.1) and return their exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={free_port()}", str(Path(__file__).resolve()),
+           *argv]
+    return subprocess.run(cmd, cwd=str(ROOT)).returncode
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="mha13b", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="gqa70b", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers per step, each with its own K/V pools (default: 80 for gqa70b, "
+                         "1 otherwise)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -650,8 +745,19 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.layers is None:
+        args.layers = DEFAULT_LAYERS.get(args.config, 1)
+    if args.layers < 1:
+        ap.error("--layers must be at least 1")
 
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one rank per GPU: start them here, as torchrun would
+        sys.exit(launch_ranks(args.gpus, sys.argv[1:]))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {world}: launch one rank per GPU")
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":

@@ -48,7 +48,7 @@ def _stale(output: Path, inputs: list[Path]) -> bool:
 def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) -> Path:
     """Compile and link libpa.so (skipped when it is newer than every source)."""
     BUILD.mkdir(exist_ok=True)
-    headers = sorted(CSRC.glob("*.cuh")) + sorted(INCLUDE.glob("*.h"))
+    headers = sorted(CSRC.glob("*.cuh")) + sorted(CSRC.glob("*.h")) + sorted(INCLUDE.glob("*.h"))
     cc = nvcc()
     objects = []
     jobs = []

@@ -548,6 +548,8 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int bs, int kv
     size_t end = 0;
     if (p.max_parts > 1) {
         const size_t rows = (size_t)T * Hq * p.max_parts;
+        // the partial rows come first: the merge reads them with 16-byte vector loads,
+        // so their offset must stay a multiple of 16 (checked at launch)
         p.acc_off = 0;
         p.ml_off = align_up(rows * D * sizeof(float), 256);
         end = align_up(p.ml_off + rows * 2 * sizeof(float), 256);
@@ -619,6 +621,8 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
                     workspace ? workspace_bytes : (size_t)0);
     if (plan.bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(PA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
+    if (plan.max_parts > 1 && (plan.acc_off % 16 != 0 || plan.ml_off % 16 != 0))
+        return fail(PA_ERR_INVALID_ARG, "%s: internal workspace layout is not 16-byte aligned", fn);
     MultiArgs a{};
     a.out = out;
     a.q = query;

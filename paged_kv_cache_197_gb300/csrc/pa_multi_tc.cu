@@ -38,9 +38,11 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "pa_internal.cuh"
+#include "pa_stages.h"
 
 namespace pa {
 namespace {
@@ -255,6 +257,7 @@ struct TcShared {
     uint64_t kfree[kTcStages], vfree[kTcStages];  // stage consumed by S_t / by P V_t
     uint64_t sfull, sfree;        // S_t in tensor memory / read by all 128 rows
     uint64_t pfull, odone;        // P_t written by all rows / P V_t done
+    uint64_t drain;               // every product issued so far is done (abort path only)
     uint32_t taddr;
     int abort;
 };
@@ -327,6 +330,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         mbar_init_n(tc_smem(&sh.sfree), kTcRows);
         mbar_init_n(tc_smem(&sh.pfull), kTcRows);
         mbar_init(tc_smem(&sh.odone));
+        mbar_init(tc_smem(&sh.drain));
         sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -369,6 +373,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         const bool is_k = warp == 4;
         const CUtensorMap *map = is_k ? &kmap : &vmap;
         const int oob_row = a.N * a.Hkv * BS;  // a row past the pool: the copy fills zeros
+        int issued = 0;
 #pragma unroll 1
         for (int t = 0; t < ntile; ++t) {
             const int st = t % kTcStages, use = t / kTcStages;
@@ -403,6 +408,16 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
                 }
             }
             __syncwarp();
+            issued = t + 1;
+        }
+        if (issued < ntile || sh.abort != 0) {
+            // stopping early: the copies already issued may still be landing in this
+            // block's shared memory; wait (bounded) for the last fill of every stage
+#pragma unroll 1
+            for (int st = 0; st < kTcStages; ++st) {
+                const StageFill f = last_fill(issued, kTcStages, st);
+                if (f.any) mbar_wait(tc_smem(is_k ? &sh.kfull[st] : &sh.vfull[st]), f.parity);
+            }
         }
     } else if (warp == 6) {
         // ---- tensor-core products in the order S_0, S_1, PV_0, S_2, PV_1, ...: the
@@ -449,7 +464,16 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             }
             __syncwarp();
         }
-        if (!ok && lane == 0) atomicOr(&sh.abort, 1);
+        if (!ok) {
+            // stopping early: let every product already issued finish before tensor
+            // memory is released (one more commit tracks all of them; bounded wait)
+            if (lane == 0) {
+                atomicOr(&sh.abort, 1);
+                umma_commit(tc_smem(&sh.drain));
+            }
+            __syncwarp();
+            mbar_wait(tc_smem(&sh.drain), 0);
+        }
     } else {
         // ---- rows: scores, online softmax, P, output
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -630,14 +654,14 @@ cudaError_t launch_tc_typed(const MultiArgs &a, cudaStream_t stream) {
     if ((int64_t)a.N * a.Hkv * BS >= (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // TMA row coordinates
     const int rows = a.N * a.Hkv * BS;
     if (!pool_map(&kmap, a.k_cache, rows, BS) || !pool_map(&vmap, a.v_cache, rows, BS)) return cudaErrorInvalidValue;
-    static bool configured[64] = {false};
+    static std::atomic<bool> configured[64];  // per device: the shared-memory attribute is set
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         const cudaError_t e =
             cudaFuncSetAttribute(multi_tc_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
     multi_tc_kernel<BS><<<grid, kTcAllThreads, kTcSmem, stream>>>(a, kmap, vmap);

@@ -214,8 +214,25 @@ def test_multi_token_workspace_and_checks(lib):
                 best, best_p = score, cand
         return best_p
 
+    # the balanced rule's own properties, over a sweep of contexts, batch shapes and SM
+    # counts: every partition is a multiple of 64 tokens in [256, 4096] (or the whole
+    # context rounded up to 64), and the n partitions of the longest context leave less
+    # than 64 tokens of slack each (no ragged last partition) unless they are of the
+    # shortest length, 256 tokens
+    for sms in (132, 148, 152):
+        for ctx in (1, 63, 255, 256, 257, 1000, 2100, 4095, 4097, 8000, 12345, 32768):
+            for S, Hkv, max_q, G in ((1, 1, 1, 1), (4, 8, 4, 8), (20, 8, 4, 8), (64, 8, 2, 4),
+                                     (256, 8, 1, 4)):
+                pt = plan(S, Hkv * G, Hkv, 64, ctx, max_q, sms=sms)
+                n = -(-ctx // pt)
+                assert pt % 64 == 0, (sms, ctx, S, pt)
+                if n > 1:
+                    assert 256 <= pt <= 4096, (sms, ctx, S, pt)
+                    assert n * pt - ctx < 64 * n or pt == 256, (sms, ctx, S, pt)
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     for S, T, Hq, Hkv, D, max_ctx, max_q in [(20, 80, 64, 8, 128, 8000, 4), (4, 2048, 32, 8, 128, 4096, 512),
+                                             (9, 72, 16, 2, 64, 12345, 8), (3, 12, 8, 8, 64, 4097, 4),
+                                             (64, 128, 32, 8, 64, 3000, 2), (1, 1, 8, 1, 64, 32768, 1),
                                              (7, 40, 16, 2, 64, 2100, 8), (600, 600, 32, 32, 128, 1000, 1),
                                              (1, 128, 32, 8, 128, 32768, 128), (2, 300, 16, 2, 128, 9000, 150)]:
         pt = plan(S, Hq, Hkv, D, max_ctx, max_q)

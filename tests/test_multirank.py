@@ -58,3 +58,36 @@ def test_two_ranks_weak_scaling():
     import bench
 
     assert bench.whole_job_gbs(1_000_000_000, 2, 1.0) == pytest.approx(2000.0)
+
+
+def test_bench_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` outside torchrun starts two local ranks itself (here on the
+    reference arm, which needs no GPU): one JSON line, from rank 0, reporting 2 GPUs."""
+    import json
+    import subprocess
+    import sys
+    from pathlib import Path
+
+    root = Path(__file__).resolve().parents[1]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    proc = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2",
+                           "--config", "tiny", "--steps", "2", "--warmup", "3"],
+                          cwd=root, capture_output=True, text=True, env=env, timeout=300)
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    lines = [l for l in proc.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    res = json.loads(lines[0])
+    assert res["n_gpus"] == 2 and res["impl"] == "reference"
+
+
+def test_bench_gpus_flag_must_match_world_size():
+    import subprocess
+    import sys
+    from pathlib import Path
+
+    root = Path(__file__).resolve().parents[1]
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    proc = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "1",
+                           "--config", "tiny", "--steps", "2", "--warmup", "3"],
+                          cwd=root, capture_output=True, text=True, env=env, timeout=300)
+    assert proc.returncode != 0 and "WORLD_SIZE" in proc.stderr
