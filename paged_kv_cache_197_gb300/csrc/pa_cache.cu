@@ -22,6 +22,10 @@ reshape_and_cache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict_
                          uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                          const int64_t *__restrict__ slot_mapping, int T, int Hkv,
                          int chunks_per_row, int bs, int N, int *err_flag) {
+    // a programmatic dependent of the previous kernel on the stream: wait for it, then
+    // let the next one launch (it waits for this grid in turn)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t total = (int64_t)T * Hkv * 2 * chunks_per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -60,6 +64,8 @@ quantize_kv_kernel(const uint16_t *__restrict__ key, const uint16_t *__restrict_
                    const int64_t *__restrict__ slot_mapping, int T, int Hkv, int bs, int N,
                    int *err_flag) {
     constexpr int PER_LANE = D / 32;  // 4 (D = 128) or 2 (D = 64)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t rows = (int64_t)T * Hkv * 2;
     for (int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
@@ -134,6 +140,8 @@ __global__ void __launch_bounds__(kThreads)
 copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                    float *__restrict__ k_scale, float *__restrict__ v_scale, const CopyPairs pairs,
                    int64_t block_vecs, int scale_elems) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t src = pairs.src[blockIdx.x];
     const int64_t dst = pairs.dst[blockIdx.x];
     if (blockIdx.y < 2) {
@@ -164,11 +172,11 @@ cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value,
                                      cudaStream_t stream) {
     const int chunks = D / 8;
     const int64_t items = (int64_t)T * Hkv * 2 * chunks;
-    reshape_and_cache_kernel<<<grid_for(items, kThreads), kThreads, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(key), reinterpret_cast<const uint4 *>(value),
-        reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), slot_mapping, T,
-        Hkv, chunks, bs, N, err_flag);
-    return cudaGetLastError();
+    return launch_dependent(reshape_and_cache_kernel, dim3(grid_for(items, kThreads)), dim3(kThreads), 0,
+                            stream, reinterpret_cast<const uint4 *>(key),
+                            reinterpret_cast<const uint4 *>(value), reinterpret_cast<uint4 *>(k_cache),
+                            reinterpret_cast<uint4 *>(v_cache), slot_mapping, T, Hkv, chunks, bs, N,
+                            err_flag);
 }
 
 cudaError_t launch_quantize_kv(const uint16_t *key, const uint16_t *value, int8_t *k_cache,
@@ -176,14 +184,10 @@ cudaError_t launch_quantize_kv(const uint16_t *key, const uint16_t *value, int8_
                                const int64_t *slot_mapping, int T, int Hkv, int D, int bs, int N,
                                int *err_flag, cudaStream_t stream) {
     const int64_t warps = (int64_t)T * Hkv * 2;
-    const int grid = grid_for(warps, kThreads / 32);
-    if (D == 128)
-        quantize_kv_kernel<128, false><<<grid, kThreads, 0, stream>>>(
-            key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
-    else
-        quantize_kv_kernel<64, false><<<grid, kThreads, 0, stream>>>(
-            key, value, k_cache, v_cache, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
-    return cudaGetLastError();
+    const dim3 grid(grid_for(warps, kThreads / 32));
+    return launch_dependent(D == 128 ? quantize_kv_kernel<128, false> : quantize_kv_kernel<64, false>, grid,
+                            dim3(kThreads), 0, stream, key, value, k_cache, v_cache, k_scale, v_scale,
+                            slot_mapping, T, Hkv, bs, N, err_flag);
 }
 
 cudaError_t launch_quantize_kv_fp8(const uint16_t *key, const uint16_t *value, uint8_t *k_cache,
@@ -191,15 +195,11 @@ cudaError_t launch_quantize_kv_fp8(const uint16_t *key, const uint16_t *value, u
                                    const int64_t *slot_mapping, int T, int Hkv, int D, int bs,
                                    int N, int *err_flag, cudaStream_t stream) {
     const int64_t warps = (int64_t)T * Hkv * 2;
-    const int grid = grid_for(warps, kThreads / 32);
+    const dim3 grid(grid_for(warps, kThreads / 32));
     int8_t *kc = reinterpret_cast<int8_t *>(k_cache), *vc = reinterpret_cast<int8_t *>(v_cache);
-    if (D == 128)
-        quantize_kv_kernel<128, true><<<grid, kThreads, 0, stream>>>(
-            key, value, kc, vc, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
-    else
-        quantize_kv_kernel<64, true><<<grid, kThreads, 0, stream>>>(
-            key, value, kc, vc, k_scale, v_scale, slot_mapping, T, Hkv, bs, N, err_flag);
-    return cudaGetLastError();
+    return launch_dependent(D == 128 ? quantize_kv_kernel<128, true> : quantize_kv_kernel<64, true>, grid,
+                            dim3(kThreads), 0, stream, key, value, kc, vc, k_scale, v_scale, slot_mapping, T,
+                            Hkv, bs, N, err_flag);
 }
 
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
@@ -214,10 +214,10 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, float *k_scale, flo
             pairs.dst[i] = (int)block_mapping[2 * (base + i) + 1];
         }
         dim3 grid(count, k_scale ? 3 : 2);
-        copy_blocks_kernel<<<grid, kThreads, 0, stream>>>(
-            reinterpret_cast<uint4 *>(k_cache), reinterpret_cast<uint4 *>(v_cache), k_scale,
-            v_scale, pairs, block_vecs, scale_elems_per_block);
-        cudaError_t err = cudaGetLastError();
+        cudaError_t err = launch_dependent(copy_blocks_kernel, grid, dim3(kThreads), 0, stream,
+                                           reinterpret_cast<uint4 *>(k_cache),
+                                           reinterpret_cast<uint4 *>(v_cache), k_scale, v_scale, pairs,
+                                           block_vecs, scale_elems_per_block);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;

@@ -470,6 +470,9 @@ paged_decode_kernel(const DecodeArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
 
+    // everything this kernel reads may come from the kernel before it on the stream
+    // (a programmatic dependent launch): wait for that grid before any load
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int ctx = checked_context(a, s, BS, part == 0 && blockIdx.y == 0 && tid == 0);
     // tokens before `start` (a shared prefix, attended by the grouped prefix kernel)
     // are skipped; start is a multiple of the block size
@@ -648,6 +651,9 @@ paged_decode_kernel(const DecodeArgs a) {
 template <int D, int BS>
 __global__ void __launch_bounds__(128) merge_partitions_kernel(const __grid_constant__ DecodeArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the next kernel on the stream may launch now (it waits for this grid to finish
+    // before it reads anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int PER = D / 32;  // output values per lane
     const int lane = threadIdx.x & 31;
     const int64_t pair = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // s * Hq + h
@@ -704,9 +710,11 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const __grid_cons
 
 template <typename KV, int D, int BS, int TILE>
 cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
+    // a programmatic dependent of the kernel before it on the stream (an append, the
+    // previous layer's merge): it launches while that kernel drains and waits for it
+    // before reading
     dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
-    paged_decode_kernel<KV, D, BS, TILE><<<grid, kThreads, 0, stream>>>(a);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE>, grid, dim3(kThreads), 0, stream, a);
     if (err != cudaSuccess || a.max_parts == 1 || a.partials_only) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((int64_t)a.S * a.Hq + 3) / 4));

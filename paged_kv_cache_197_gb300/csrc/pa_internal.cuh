@@ -101,6 +101,25 @@ cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream);  /
 cudaError_t launch_dequant_blocks(const MultiArgs &a, int bs, int kv_dtype, int Mq, uint16_t *kq, uint16_t *vq,
                                   int32_t *tab, cudaStream_t stream);
 
+// Launch `kernel` as a programmatic dependent of the kernel before it on `stream`: it
+// may be scheduled while that kernel drains, and must execute griddepcontrol.wait
+// before it reads or writes anything that kernel may touch.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // ------------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing was launched).
 cudaError_t launch_reshape_and_cache(const uint16_t *key, const uint16_t *value, uint16_t *k_cache,
