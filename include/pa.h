@@ -78,12 +78,11 @@ enum {
                                          memory could not be laid out (the affected
                                          outputs are not written); not expected in normal
                                          operation                                        */
-    PA_FLAG_FP16_RANGE = 64           /* an 8-bit row staged as fp16 code x scale (the
-                                         shared prefix of pa_decode_shared_prefix, narrow
-                                         pa_multi_token_attention calls) has a scale whose
-                                         largest code leaves fp16's range (scale > 65504 /
-                                         127 for int8, > 65504 / 448 for fp8): the outputs
-                                         that attend it are not finite                    */
+    PA_FLAG_FP16_RANGE = 64           /* pa_decode_shared_prefix: an 8-bit row of a shared
+                                         prefix, staged as fp16 code x scale, has a scale
+                                         whose largest code leaves fp16's range (scale >
+                                         65504 / 127 for int8, > 65504 / 448 for fp8): the
+                                         outputs that attend it are not finite            */
 };
 
 /* Version of this ABI (bumped on any signature change). */
@@ -272,12 +271,10 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
  * arguments as pa_decode.  With head_dim 128 and max_query_len * Hq / Hkv >= 64
  * (prefill-shaped calls), 8-bit entries of the attended blocks are first dequantised
  * into the workspace as bf16 (code x scale, rounded once) and the products are bf16
- * with fp32 accumulation, as for a bf16 cache.  Otherwise 8-bit entries are
- * dequantised on their way through shared memory as fp16 code x scale (the scale
- * rounded to fp16, the product rounded once), the query rows as fp16 scaled by a power
- * of two per row; the products are fp16 with fp32 accumulation, and the dequantised
- * values must lie within fp16's range (|x| <= 65504, the scale above fp16's smallest
- * normal 2^-14 for full precision).
+ * with fp32 accumulation, as for a bf16 cache.  Otherwise the codes pass through
+ * shared memory as exact fp16 values and the query rows as fp16 scaled by a power of
+ * two per row; the products are fp16 with fp32 accumulation, the key scale multiplies
+ * the score and the value scale the softmax weight in fp32 (no range limit).
  */
 size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
                                      int max_context_len, int max_query_len);

@@ -129,6 +129,32 @@ __device__ __forceinline__ void codes_to_f16(const uint4 &c, float scale, uint4 
     hi = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
+// 8-bit caches: sixteen codes of one row as sixteen exact fp16 values (two 16-byte
+// words), without the row's scale: int8 through the fp16 pattern 0x64XX = 1024 + XX
+// with XX = x + 128, less 1152; fp8 (e4m3) by the hardware conversion.
+template <typename KV>
+__device__ __forceinline__ void codes_to_f16_exact(const uint4 &c, uint4 &lo, uint4 &hi) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (std::is_same<KV, int8_t>::value) {
+            const uint32_t u = w[i] ^ 0x80808080u;
+            const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+            const uint32_t b0 = __byte_perm(u, 0x64646464u, 0x4140), b1 = __byte_perm(u, 0x64646464u, 0x4342);
+            const __half2 h0 = __hsub2(*reinterpret_cast<const __half2 *>(&b0), bias);
+            const __half2 h1 = __hsub2(*reinterpret_cast<const __half2 *>(&b1), bias);
+            out[2 * i] = *reinterpret_cast<const uint32_t *>(&h0);
+            out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+        } else {
+            out[2 * i] = e4m3x2_to_f16x2(w[i] & 0xffffu);
+            out[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
+        }
+    }
+    lo = make_uint4(out[0], out[1], out[2], out[3]);
+    hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
 __device__ __forceinline__ void mma16816_f16(float *c, const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "

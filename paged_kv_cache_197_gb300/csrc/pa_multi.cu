@@ -187,16 +187,23 @@ __device__ __forceinline__ void attend_tokens(float (&o)[D / 8][4], float (&m)[2
     }
 }
 
-// The step of attend_tokens for 8-bit caches: K and V rows are fp16 (code x scale),
-// the query rows fp16 scaled by a power of two per row (rs[h] = softmax scale x 2^-sig
-// of row gq + 8h), the weights fp16; products f16 with fp32 accumulation.
+// The step of attend_tokens for 8-bit caches.  K and V rows are the exact codes as
+// fp16; the query rows fp16 scaled by a power of two per row (rs[h] = softmax scale x
+// 2^-sig of row gq + 8h); ksc / vsc the staged tokens' key and value scales.  A score
+// is (q . code) x rs x key scale, in fp32.  The value scale multiplies the softmax
+// weight fed to the fp16 product, in units of 2^ve (ve: the exponent of the largest
+// value scale this warp has seen, O rescaled when it grows), so weight x scale stays
+// below 1; the running sum takes the weights alone.  No value leaves fp16's range
+// whatever the scales.
 template <int D, int NTW>
-__device__ __forceinline__ void attend_tokens_q(float (&o)[D / 8][4], float (&m)[2], float (&l)[2],
-                                                uint32_t qaddr, uint32_t kb, uint32_t vb, int tok0,
-                                                bool full, const int (&lim)[2], const float (&rs)[2], int t) {
+__device__ __forceinline__ void attend_tokens_q(float (&o)[D / 8][4], float (&m)[2], float (&l)[2], int &ve,
+                                                uint32_t qaddr, uint32_t kb, uint32_t vb, const float *ksc,
+                                                const float *vsc, int tok0, bool full, const int (&lim)[2],
+                                                const float (&rs)[2], int t) {
     constexpr int RS = 2 * D + 16;
     constexpr int KC = D / 16;
     constexpr int DT = D / 8;
+    const int lane = threadIdx.x & 31;
     float sc[NTW][4];
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
@@ -217,11 +224,9 @@ __device__ __forceinline__ void attend_tokens_q(float (&o)[D / 8][4], float (&m)
     for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            float x = sc[nt][c] * rs[c >> 1];
-            if (!full) {
-                const int tok = tok0 + nt * 8 + 2 * t + (c & 1);
-                x = tok <= lim[c >> 1] ? x : -INFINITY;
-            }
+            const int j = nt * 8 + 2 * t + (c & 1);  // token of the slice
+            float x = sc[nt][c] * rs[c >> 1] * ksc[j];
+            if (!full) x = tok0 + j <= lim[c >> 1] ? x : -INFINITY;
             sc[nt][c] = x;
             mx[c >> 1] = fmaxf(mx[c >> 1], x);
         }
@@ -236,15 +241,29 @@ __device__ __forceinline__ void attend_tokens_q(float (&o)[D / 8][4], float (&m)
         m[h] = mnew;
         l[h] *= alpha[h];
     }
-    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+    // the largest value scale of the slice's tokens: O in units of 2^ve
+    float vmax = 0.f;
+    for (int j = lane; j < NTW * 8; j += 32) vmax = fmaxf(vmax, vsc[j]);
 #pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-            o[dt][0] *= alpha[0];
-            o[dt][1] *= alpha[0];
-            o[dt][2] *= alpha[1];
-            o[dt][3] *= alpha[1];
+    for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+    float grow = 1.f;
+    if (vmax > 0.f) {
+        const int e = exponent_above(vmax);
+        if (e > ve) {
+            grow = ve < -200 ? 0.f : ldexpf(1.f, ve - e);
+            ve = e;
         }
     }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f || grow != 1.f)) {
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+            o[dt][0] *= alpha[0] * grow;
+            o[dt][1] *= alpha[0] * grow;
+            o[dt][2] *= alpha[1] * grow;
+            o[dt][3] *= alpha[1] * grow;
+        }
+    }
+    const float vmul = ldexpf(1.f, -ve);
 #pragma unroll
     for (int kk = 0; kk < NTW / 2; ++kk) {
         float p[2][4];
@@ -252,8 +271,10 @@ __device__ __forceinline__ void attend_tokens_q(float (&o)[D / 8][4], float (&m)
         for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                p[u][c] = ex2(sc[2 * kk + u][c] - base[c >> 1]);
-                l[c >> 1] += p[u][c];
+                const int j = (2 * kk + u) * 8 + 2 * t + (c & 1);
+                const float w = ex2(sc[2 * kk + u][c] - base[c >> 1]);
+                l[c >> 1] += w;
+                p[u][c] = w * (vsc[j] * vmul);
             }
         const uint32_t pa[4] = {f16x2(p[0][0], p[0][1]), f16x2(p[0][2], p[0][3]),
                                 f16x2(p[1][0], p[1][1]), f16x2(p[1][2], p[1][3])};
@@ -269,7 +290,7 @@ __device__ __forceinline__ void attend_tokens_q(float (&o)[D / 8][4], float (&m)
 
 template <typename KV, int D, int BS>
 __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_constant__ MultiArgs a) {
-    constexpr bool QUANT = sizeof(KV) == 1;  // int8 / fp8 cache: fp16 code x scale, fp16 products
+    constexpr bool QUANT = sizeof(KV) == 1;  // int8 / fp8 cache: exact fp16 codes, fp32 scales, fp16 products
     constexpr int ROW = D * 2;          // bytes of one token row (bf16)
     constexpr int RS = ROW + 16;        // padded shared-memory row stride
     constexpr int STAGE = kChunk * RS;  // one K (or V) stage
@@ -280,8 +301,9 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     __shared__ int s_blk[kMaxPartBlocks];
     __shared__ float s_ml[kWarps][kColsPerWarp][2];  // each warp's (max, sum) per row
     // 8-bit caches: each query row's softmax scale x 2^-sig (its fp16 copy is scaled
-    // by 2^sig)
+    // by 2^sig), and the staged chunk's key and value scales
     __shared__ float s_qs[QUANT ? kColsPerCta : 1];
+    __shared__ float s_sc[QUANT ? 2 * kChunk : 1];
 
     const int part = blockIdx.x;
     const int kvh = blockIdx.y / a.CB, cb = blockIdx.y % a.CB;
@@ -412,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
 #pragma unroll
     for (int dt = 0; dt < DT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    int ve = -1000;  // 8-bit caches: O is kept in units of 2^ve (no value scale seen yet)
     // ldmatrix lane addresses: Q as A (rows = columns), K as B (rows = tokens), V as
     // B transposed (rows = tokens), the last two at the slice's first token
     const uint32_t qaddr = smem_u32(qs) + (grp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * RS + (lane >> 4) * 16;
@@ -428,10 +451,11 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
             const uint32_t vb = smem_u32(vs + buf * STAGE) + vrow;
             const bool full = tok0 + width - 1 <= warp_lo;  // every row sees all: no mask
             if constexpr (QUANT) {
+                const float *ksc = s_sc + slice * width, *vsc = s_sc + kChunk + slice * width;
                 if (slices == 1)
-                    attend_tokens_q<D, 8>(o, m, l, qaddr, kb, vb, tok0, full, lim, rs, t);
+                    attend_tokens_q<D, 8>(o, m, l, ve, qaddr, kb, vb, ksc, vsc, tok0, full, lim, rs, t);
                 else
-                    attend_tokens_q<D, 4>(o, m, l, qaddr, kb, vb, tok0, full, lim, rs, t);
+                    attend_tokens_q<D, 4>(o, m, l, ve, qaddr, kb, vb, ksc, vsc, tok0, full, lim, rs, t);
             } else {
                 if (slices == 1)
                     attend_tokens<D, 8>(o, m, l, qaddr, kb, vb, tok0, full, lim, a.scale_log2, t);
@@ -457,13 +481,12 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
         // 8-bit caches: the next chunk's codes are copied raw (cp.async) into the other
         // of two raw buffers, and its rows' scales loaded into registers, while the
         // current chunk is computed; each thread then converts the pieces it copied
-        // itself (its own completed copies need no barrier) to fp16, code x scale, in the
-        // single K and V stage.
+        // itself (its own completed copies need no barrier) to exact fp16 codes in the
+        // single K and V stage, and the rows' scales go beside them.
         constexpr int QPR = D / 16;                  // 16-code pieces per row
         constexpr int NPT = kChunk * QPR / kThreads;  // pieces per thread and chunk
         const char *kc8 = static_cast<const char *>(a.k_cache), *vc8 = static_cast<const char *>(a.v_cache);
         float ksr[NPT], vsr[NPT];
-        bool f16_over = false;  // a row whose code x scale leaves fp16's range
         auto issue_raw = [&](int j, int b) {
             const int c0 = tok_begin + j * kChunk;
             unsigned char *rb = raw + b * raw_chunk_bytes<D>();
@@ -487,7 +510,6 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
                 }
                 cp_async16(smem_u32(rb + r * D + qc * 16), ksrc, bytes);
                 cp_async16(smem_u32(rb + kChunk * D + r * D + qc * 16), vsrc, bytes);
-                f16_over |= fmaxf(ksr[k], vsr[k]) > max_f16_scale<KV>();
             }
             cp_async_commit();
         };
@@ -497,14 +519,18 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
             for (int k = 0; k < NPT; ++k) {
                 const int i = tid + k * kThreads, r = i / QPR, qc = i % QPR;
                 uint4 lo, hi;
-                codes_to_f16<KV>(*reinterpret_cast<const uint4 *>(rb + r * D + qc * 16), ksr[k], lo, hi);
+                codes_to_f16_exact<KV>(*reinterpret_cast<const uint4 *>(rb + r * D + qc * 16), lo, hi);
                 uint4 *kd = reinterpret_cast<uint4 *>(ks + r * RS + qc * 32);
                 kd[0] = lo;
                 kd[1] = hi;
-                codes_to_f16<KV>(*reinterpret_cast<const uint4 *>(rb + kChunk * D + r * D + qc * 16), vsr[k], lo, hi);
+                codes_to_f16_exact<KV>(*reinterpret_cast<const uint4 *>(rb + kChunk * D + r * D + qc * 16), lo, hi);
                 uint4 *vd = reinterpret_cast<uint4 *>(vs + r * RS + qc * 32);
                 vd[0] = lo;
                 vd[1] = hi;
+                if (qc == 0) {  // rows past the partition or of a skipped block: scale 0
+                    s_sc[r] = ksr[k];
+                    s_sc[kChunk + r] = vsr[k];
+                }
             }
         };
         issue_raw(0, 0);
@@ -523,7 +549,6 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
             }
             __syncthreads();  // chunk j + 1 staged
         }
-        if (f16_over) raise_flag(a.err_flag, PA_FLAG_FP16_RANGE);
     }
     // the merge grid may launch now (it still waits for this grid before reading)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -532,6 +557,16 @@ __global__ void __launch_bounds__(kThreads, 2) paged_multi_kernel(const __grid_c
     for (int h = 0; h < 2; ++h) {
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+    }
+    if constexpr (QUANT) {  // O back from units of 2^ve
+        const float f = ve < -200 ? 1.f : ldexpf(1.f, ve);
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+            o[dt][0] *= f;
+            o[dt][1] *= f;
+            o[dt][2] *= f;
+            o[dt][3] *= f;
+        }
     }
     if (slices > 1) {
         // leave each warp's state in shared memory (the stages are free: every warp

@@ -10,11 +10,14 @@ with the stated bars applied per output row in units of that row's magnitude
 (helpers.compare_row_scaled).
 
   - pa_decode (exact 8-bit path, no fp16 range limit): magnitudes 1e-3 .. 1e3;
-  - pa_decode_shared_prefix and narrow pa_multi_token_attention calls stage 8-bit rows
-    as fp16 code x scale, documented for scales inside fp16's normal range: magnitudes
-    0.03 .. 3000 (every scale between 2^-14 and 65504 / 448);
-  - beyond fp16's range the staging paths raise PA_FLAG_FP16_RANGE, while pa_decode
-    still matches the oracle.
+  - narrow pa_multi_token_attention calls (exact codes, scales in fp32): 1e-3 .. 1e3;
+  - prefill-shaped multi-token calls attend bf16(code x scale): 1e-3 .. 1e3, against
+    the oracle on those values;
+  - pa_decode_shared_prefix stages a shared prefix as fp16 code x scale, documented for
+    scales inside fp16's normal range: magnitudes 0.03 .. 3000 (every scale between
+    2^-14 and 65504 / 448);
+  - beyond fp16's range the shared-prefix path raises PA_FLAG_FP16_RANGE, while
+    pa_decode and the multi-token path still match the oracle.
 """
 import numpy as np
 import pytest
@@ -98,10 +101,58 @@ def _multi(case, orc, expect_flag=0):
 
 
 @pytest.mark.parametrize("kv_dtype", ["int8", "fp8"])
+def test_multi_token_narrow(oracle, kv_dtype):
+    """Draft verification (few new tokens per sequence: the mma.sync kernel, exact codes,
+    scales in fp32), per-token magnitudes over six decades."""
+    lens, qlen = [5, 100, 1300, 2100], [4, 3, 4, 2]
+    case = workloads.build_multi_case(f"wide-verify-{kv_dtype}", S=len(lens), Hq=32, Hkv=8, D=128,
+                                      bs=16, context_lens=lens, query_lens=qlen, seed=81,
+                                      kv_dtype=kv_dtype)
+    workloads.widen_scales(case, *DECODE_RANGE, seed=82)
+    _multi(case, oracle)
+
+
+def _bf16_dequantised(codes, scales, kv_dtype, orc) -> np.ndarray:
+    """bf16 bits of code x scale (fp32 product, rounded once to bf16): the values a
+    prefill-shaped 8-bit call attends (include/pa.h)."""
+    if kv_dtype == "fp8":
+        table = np.array([orc.fp8_decode(c) for c in range(256)], dtype=np.float32)
+        vals = table[codes]
+    else:
+        vals = codes.astype(np.float32)
+    x = vals * scales[..., None].astype(np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+@pytest.mark.parametrize("kv_dtype", ["int8", "fp8"])
+def test_multi_token_prefill(oracle, kv_dtype):
+    """Prefill-shaped calls (the 8-bit blocks dequantised to bf16, then the tcgen05
+    kernel), per-token magnitudes over six decades: compared with the oracle on the same
+    dequantised values, bf16(code x scale) -- the reading this path takes."""
+    lens, qlen = [300, 1000], [300, 130]
+    case = workloads.build_multi_case(f"wide-prefill-{kv_dtype}", S=len(lens), Hq=16, Hkv=4, D=128,
+                                      bs=16, context_lens=lens, query_lens=qlen, seed=83,
+                                      kv_dtype=kv_dtype)
+    workloads.widen_scales(case, *DECODE_RANGE, seed=84)
+    got = helpers.gpu_multi_step(case, DEV)
+    assert got["flag"] == 0
+    kc, vc, ks, vs = helpers.oracle_caches(case, oracle)
+    assert np.array_equal(got["k_cache"].cpu().numpy(), kc)
+    assert np.array_equal(got["k_scale"].cpu().numpy().view(np.uint32), ks.view(np.uint32))
+    kq = _bf16_dequantised(kc, np.nan_to_num(ks), kv_dtype, oracle)
+    vq = _bf16_dequantised(vc, np.nan_to_num(vs), kv_dtype, oracle)
+    ref = oracle.paged_prefill(helpers.bits(case.q), kq, vq, case.block_tables.cpu().numpy(),
+                               case.context_lens.cpu().numpy(), case.query_start.cpu().numpy(), case.scale)
+    rows = helpers.covered_rows(case)
+    helpers.compare_row_scaled(got["out"][torch.as_tensor(rows, device=DEV)], ref[rows], "bf16")
+
+
+@pytest.mark.parametrize("kv_dtype", ["int8", "fp8"])
 def test_fp16_range_flag(oracle, kv_dtype):
     """Rows of magnitude 1e5..2e5: their scales put code x scale beyond fp16's 65504, so
-    the two fp16-staging paths raise PA_FLAG_FP16_RANGE; pa_decode, which keeps the
-    codes exact and applies the scales in fp32, still matches the oracle."""
+    the shared-prefix path, which stages a shared prefix as fp16 code x scale, raises
+    PA_FLAG_FP16_RANGE; pa_decode and narrow multi-token calls, which keep the codes
+    exact and apply the scales in fp32, still match the oracle."""
     prefix = 64
     lens = [prefix + 40, prefix + 9]
     case = workloads.build_case(f"f16-range-{kv_dtype}", S=2, Hq=16, Hkv=2, D=128, bs=16,
@@ -113,4 +164,4 @@ def test_fp16_range_flag(oracle, kv_dtype):
                                        context_lens=[50, 70], query_lens=[2, 3], seed=93,
                                        kv_dtype=kv_dtype)
     workloads.widen_scales(multi, 1e5, 2e5, seed=94)
-    _multi(multi, oracle, expect_flag=pa_mod.PA_FLAG_FP16_RANGE)
+    _multi(multi, oracle)
