@@ -70,6 +70,8 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
+    # the decode kernel launched as a programmatic dependent (griddepcontrol.wait first)
+    ("gqa70b", "b150daeb73620bab"): 655764736 + 5164800,
     ("mha13b", "0a92d8beb0508d47"): 1392700672 + 3298304,
     ("gqa70b", "0a92d8beb0508d47"): 655764224 + 5198848,
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
@@ -277,8 +279,10 @@ class Step:
         k0 = self.layers[0].k_cache
         if self.multi:
             self.max_q = max(c.meta["query_lens"])
-            n = pa.pa_multi_token_workspace_size(c.S, c.q.shape[0], c.Hq, c.Hkv, c.D, c.bs,
-                                                 pa.kv_dtype_of(k0), self.max_ctx, self.max_q)
+            # sized for the tokens the batch holds (the 8-bit prefill pool)
+            n = pa.pa_multi_token_workspace_size_for_tokens(c.S, c.q.shape[0], c.Hq, c.Hkv, c.D, c.bs,
+                                                            pa.kv_dtype_of(k0), self.max_ctx, self.max_q,
+                                                            int(c.context_lens.sum()))
             self.ws = torch.empty(n, dtype=torch.uint8, device=device) if n else None
             # append + attention (+ merge when split) + COW copies
             per_layer = 1 + 1 + (1 if self.ws is not None else 0) + cow_launches

@@ -78,11 +78,16 @@ enum {
                                          memory could not be laid out (the affected
                                          outputs are not written); not expected in normal
                                          operation                                        */
-    PA_FLAG_FP16_RANGE = 64           /* pa_decode_shared_prefix: an 8-bit row of a shared
+    PA_FLAG_FP16_RANGE = 64,          /* pa_decode_shared_prefix: an 8-bit row of a shared
                                          prefix, staged as fp16 code x scale, has a scale
                                          whose largest code leaves fp16's range (scale >
                                          65504 / 127 for int8, > 65504 / 448 for fp8): the
                                          outputs that attend it are not finite            */
+    PA_FLAG_WORKSPACE_SHORT = 128     /* pa_multi_token_attention, 8-bit cache, prefill-
+                                         shaped call: the workspace's dequantised pool could
+                                         not hold every attended block; the blocks beyond
+                                         it were read as zeros (PA_FLAG_BLOCK_OUT_OF_RANGE
+                                         may be raised for them as well)                  */
 };
 
 /* Version of this ABI (bumped on any signature change). */
@@ -270,7 +275,7 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
  * bf16, int8 and fp8 caches (k_scale, v_scale required for the last two); other
  * arguments as pa_decode.  With head_dim 128 and max_query_len * Hq / Hkv >= 64
  * (prefill-shaped calls), 8-bit entries of the attended blocks are first dequantised
- * into the workspace as bf16 (code x scale, rounded once) and the products are bf16
+ * into the workspace's pool as bf16 (code x scale, rounded once) and the products are bf16
  * with fp32 accumulation, as for a bf16 cache.  Otherwise the codes pass through
  * shared memory as exact fp16 values and the query rows as fp16 scaled by a power of
  * two per row; the products are fp16 with fp32 accumulation, the key scale multiplies
@@ -278,6 +283,21 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
  */
 size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
                                      int max_context_len, int max_query_len);
+
+/*
+ * The same for a batch whose context lengths add up to at most total_context_tokens
+ * (a host-side bound the caller's scheduler knows).  For prefill-shaped calls on an
+ * 8-bit cache the workspace holds a bf16 pool of the attended blocks, sequences packed
+ * back to back: pa_multi_token_workspace_size sizes it for every sequence at
+ * max_context_len (S x ceil(max_context_len / bs) blocks), this call for the tokens
+ * the batch holds (ceil(total / bs) + S blocks).  pa_multi_token_attention takes a
+ * workspace of any size from the smaller of the two: its pool holds as many blocks
+ * as the rest of the workspace has room for; attended blocks beyond that are read as
+ * zeros and PA_FLAG_WORKSPACE_SHORT is raised.  Returns 0 for invalid arguments.
+ */
+size_t pa_multi_token_workspace_size_for_tokens(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                                int max_context_len, int max_query_len,
+                                                int64_t total_context_tokens);
 
 pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
                                    const void *v_cache, const float *k_scale,

@@ -30,11 +30,13 @@ PA_FLAG_PREFIX_MISMATCH = 8
 PA_FLAG_QUERY_OUT_OF_RANGE = 16
 PA_FLAG_TIMEOUT = 32
 PA_FLAG_FP16_RANGE = 64
+PA_FLAG_WORKSPACE_SHORT = 128
 
 EXPORTED = ["pa_version", "pa_status_string", "pa_last_error_string", "pa_reshape_and_cache",
             "pa_quantize_kv", "pa_quantize_kv_fp8", "pa_copy_blocks", "pa_decode_workspace_size", "pa_decode",
             "pa_decode_noalloc", "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix",
-            "pa_multi_token_workspace_size", "pa_multi_token_attention"]
+            "pa_multi_token_workspace_size", "pa_multi_token_workspace_size_for_tokens",
+            "pa_multi_token_attention"]
 PA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -87,6 +89,8 @@ def load_library(path: Path | str | None = None) -> ctypes.CDLL:
     lib.pa_decode_shared_prefix.restype = i32
     lib.pa_multi_token_workspace_size.argtypes = [i32] * 9
     lib.pa_multi_token_workspace_size.restype = sz
+    lib.pa_multi_token_workspace_size_for_tokens.argtypes = [i32] * 9 + [i64]
+    lib.pa_multi_token_workspace_size_for_tokens.restype = sz
     lib.pa_multi_token_attention.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, vp, i32,
                                              i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, sz,
                                              vp, vp]
@@ -369,10 +373,17 @@ def pa_multi_token_workspace_size(S: int, T: int, Hq: int, Hkv: int, D: int, bs:
         S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len))
 
 
+def pa_multi_token_workspace_size_for_tokens(S: int, T: int, Hq: int, Hkv: int, D: int, bs: int,
+                                             kv_dtype: int, max_context_len: int, max_query_len: int,
+                                             total_context_tokens: int) -> int:
+    return int(load_library().pa_multi_token_workspace_size_for_tokens(
+        S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len, int(total_context_tokens)))
+
+
 def pa_multi_token_attention(out, query, k_cache, v_cache, block_tables, context_lens,
                              query_start, scale: float, max_context_len: int,
                              max_query_len: int, workspace=None, k_scale=None, v_scale=None,
-                             err_flag=None, stream=None) -> None:
+                             err_flag=None, stream=None, total_context_tokens=None) -> None:
     """Several new tokens per sequence attend the paged cache, each up to its own
     position: query/out [T][Hq][D] bf16, sequence s owning rows
     query_start[s] .. query_start[s+1]-1.  workspace defaults to a fresh allocation."""
@@ -397,8 +408,13 @@ def pa_multi_token_attention(out, query, k_cache, v_cache, block_tables, context
             or block_tables.shape[0] != S or query_start.shape[0] != S + 1:
         raise ValueError("pa_multi_token_attention: shape mismatch")
     if workspace is None:
-        n = pa_multi_token_workspace_size(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len,
-                                          max_query_len)
+        if total_context_tokens is None:
+            n = pa_multi_token_workspace_size(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len,
+                                              max_query_len)
+        else:
+            n = pa_multi_token_workspace_size_for_tokens(S, T, Hq, Hkv, D, bs, kv_dtype,
+                                                         max_context_len, max_query_len,
+                                                         total_context_tokens)
         workspace = torch.empty(n, dtype=torch.uint8, device=query.device) if n else None
     ws_bytes = 0
     if workspace is not None:

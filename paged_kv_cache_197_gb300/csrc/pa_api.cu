@@ -482,10 +482,13 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
 struct MultiPlan {
     int CB, part_tokens, max_parts;
     size_t acc_off, ml_off, bytes;
-    // 8-bit caches on the tcgen05 kernel: Mq bf16 blocks per sequence and an identity
-    // table in the workspace (Mq = 0: none)
+    // 8-bit caches on the tcgen05 kernel: the dequantised pool (Mq = ceil(max context /
+    // bs) table entries per sequence; Mq = 0: none): the table [S][Mq] and the sequences'
+    // pool offsets [S + 1] at tab_off and off_off, then K and V pools of pool_blocks
+    // blocks of block_bytes each from kq_off
     int Mq;
-    size_t kq_off, vq_off, tab_off;
+    size_t tab_off, off_off, kq_off, block_bytes;
+    int64_t pool_blocks;
 };
 
 // Fixed cost of one multi-token CTA (q fragments or the tensor-memory setup, the join
@@ -497,8 +500,10 @@ struct MultiPlan {
 // against 4 x 768 157.0 us.
 constexpr double kMultiRampTokens = 512.0;
 
+// pool_blocks_hint: blocks the dequantised pool must hold (an upper bound of the blocks
+// the sequences attend), or -1 for the largest need, S * Mq.
 static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len,
-                            int max_query_len) {
+                            int max_query_len, int64_t pool_blocks_hint = -1) {
     MultiPlan p{};
     const int G = Hq / Hkv;
     p.CB = std::max(1, (int)(((int64_t)max_query_len * G + multi_cols_per_cta() - 1) / multi_cols_per_cta()));
@@ -556,11 +561,13 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int bs, int kv
     }
     if (tc && kv_dtype != PA_KV_BF16) {
         p.Mq = (ctx + bs - 1) / bs;
-        const size_t pool = (size_t)S * p.Mq * Hkv * bs * D * 2;
-        p.kq_off = end;
-        p.vq_off = align_up(p.kq_off + pool, 256);
-        p.tab_off = align_up(p.vq_off + pool, 256);
-        end = align_up(p.tab_off + (size_t)S * p.Mq * sizeof(int32_t), 256);
+        p.tab_off = end;
+        p.off_off = align_up(p.tab_off + (size_t)S * p.Mq * sizeof(int32_t), 256);
+        p.kq_off = align_up(p.off_off + (size_t)(S + 1) * sizeof(int32_t), 256);
+        p.block_bytes = (size_t)Hkv * bs * D * 2;  // a multiple of 256
+        const int64_t most = (int64_t)S * p.Mq;
+        p.pool_blocks = pool_blocks_hint < 0 ? most : std::min(most, std::max<int64_t>(pool_blocks_hint, 1));
+        end = p.kq_off + 2 * (size_t)p.pool_blocks * p.block_bytes;
     }
     p.bytes = end;
     return p;
@@ -586,6 +593,18 @@ size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int b
                          max_context_len, max_query_len) != PA_OK)
         return 0;
     return plan_multi(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len).bytes;
+}
+
+size_t pa_multi_token_workspace_size_for_tokens(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
+                                                int max_context_len, int max_query_len,
+                                                int64_t total_context_tokens) {
+    if (check_multi_args("pa_multi_token_workspace_size_for_tokens", S, T, Hq, Hkv, D, bs, kv_dtype,
+                         max_context_len, max_query_len) != PA_OK ||
+        total_context_tokens < 0)
+        return 0;
+    // sum_s ceil(ctx_s / bs) <= sum_s ctx_s / bs + S
+    const int64_t blocks = (total_context_tokens + bs - 1) / bs + S;
+    return plan_multi(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len, blocks).bytes;
 }
 
 pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
@@ -616,8 +635,11 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
     if (!(scale == scale) || scale == __builtin_inff() || scale == -__builtin_inff())
         return fail(PA_ERR_INVALID_ARG, "%s: scale must be finite", fn);
     const MultiPlan plan = plan_multi(S, T, Hq, Hkv, D, bs, kv_dtype, max_context_len, max_query_len);
-    if (plan.bytes && (!workspace || workspace_bytes < plan.bytes))
-        return fail(PA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, plan.bytes,
+    // the dequantised pool holds as many blocks as the workspace leaves room for, at
+    // least one (pa_multi_token_workspace_size_for_tokens sizes it for the attended ones)
+    const size_t need = plan.Mq > 0 ? plan.kq_off + 2 * plan.block_bytes : plan.bytes;
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(PA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                     workspace ? workspace_bytes : (size_t)0);
     if (plan.bytes && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(PA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", fn);
@@ -653,17 +675,20 @@ pa_status pa_multi_token_attention(pa_bf16 *out, const pa_bf16 *query, const voi
     if (plan.Mq > 0) {
         // 8-bit cache, prefill-shaped: dequantise the attended blocks once, then the bf16
         // kernel reads them through the identity table
+        const int64_t cap = std::min<int64_t>((int64_t)S * plan.Mq,
+                                              (int64_t)((workspace_bytes - plan.kq_off) / (2 * plan.block_bytes)));
         uint16_t *kq = (uint16_t *)((char *)workspace + plan.kq_off);
-        uint16_t *vq = (uint16_t *)((char *)workspace + plan.vq_off);
+        uint16_t *vq = (uint16_t *)((char *)workspace + plan.kq_off + (size_t)cap * plan.block_bytes);
         int32_t *tab = (int32_t *)((char *)workspace + plan.tab_off);
-        launch_dequant_blocks(a, bs, kv_dtype, plan.Mq, kq, vq, tab, (cudaStream_t)stream);
+        int32_t *off = (int32_t *)((char *)workspace + plan.off_off);
+        launch_dequant_blocks(a, bs, kv_dtype, plan.Mq, kq, vq, tab, off, cap, (cudaStream_t)stream);
         MultiArgs b = a;
         b.k_cache = kq;
         b.v_cache = vq;
         b.k_scale = b.v_scale = nullptr;
         b.block_tables = tab;
         b.M = plan.Mq;
-        b.N = S * plan.Mq;
+        b.N = (int)cap;
         launch_multi_token(b, D, bs, PA_KV_BF16, (cudaStream_t)stream);
     } else {
         launch_multi_token(a, D, bs, kv_dtype, (cudaStream_t)stream);

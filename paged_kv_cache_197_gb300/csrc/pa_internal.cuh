@@ -97,9 +97,10 @@ cudaError_t launch_multi_merge(const MultiArgs &a, int D, int bs, cudaStream_t s
 bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len);
 cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream);  // bf16 caches
 // 8-bit caches, prefill-shaped calls: the attended blocks dequantised into a bf16 pool
-// (Mq blocks per sequence) and an identity table, both in the workspace.
+// of `cap` blocks, sequences packed back to back (offsets off[S + 1]), and the table
+// [S][Mq] of pool slots, all in the workspace.
 cudaError_t launch_dequant_blocks(const MultiArgs &a, int bs, int kv_dtype, int Mq, uint16_t *kq, uint16_t *vq,
-                                  int32_t *tab, cudaStream_t stream);
+                                  int32_t *tab, int32_t *off, int64_t cap, cudaStream_t stream);
 
 // Launch `kernel` as a programmatic dependent of the kernel before it on `stream`: it
 // may be scheduled while that kernel drains, and must execute griddepcontrol.wait

@@ -679,15 +679,65 @@ struct tc_e4m3 {  // an fp8 (e4m3) cache entry
 // into a bf16 pool in the workspace, block i of sequence s at s * Mq + i, and row s of
 // an identity table in the workspace names it; the bf16 kernel then reads that pool.
 // A table entry outside [0, N) is flagged and its block written as zeros.
+// Where each sequence's dequantised blocks start in the pool: off[s] = sum over s' < s
+// of the blocks its context covers, off[S] the total (one CTA; S values).
+template <int BS>
+__global__ void __launch_bounds__(256) pool_offsets_kernel(const __grid_constant__ MultiArgs a, int32_t *off) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ int wsum[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int carry = 0;
+    for (int base = 0; base < a.S; base += 256) {
+        const int s = base + tid;
+        int n = 0;
+        if (s < a.S) {
+            const int ctx = min(max(a.context_lens[s], 0), min(a.M * BS, a.max_context_len));
+            n = (ctx + BS - 1) / BS;
+        }
+        int v = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane == 31) wsum[warp] = v;
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            before += w < warp ? wsum[w] : 0;
+            total += wsum[w];
+        }
+        if (s < a.S) off[s] = carry + before + v - n;
+        carry += total;
+        __syncthreads();
+    }
+    if (tid == 0) off[a.S] = carry;
+}
+
+// The blocks a sequence attends, dequantised to bf16 (code x scale, rounded once) into
+// a pool of `cap` blocks, sequences back to back from off[s]; tab[s][i] is the pool slot
+// of the sequence's block i (its block table for the tcgen05 kernel).  A block beyond
+// the pool's capacity is left out (slot -1, read as zeros) and PA_FLAG_WORKSPACE_SHORT
+// raised.
 template <typename KV, int BS>
 __global__ void __launch_bounds__(256) dequant_blocks_kernel(const __grid_constant__ MultiArgs a, int Mq,
-                                                             uint16_t *kq, uint16_t *vq, int32_t *tab) {
+                                                             uint16_t *kq, uint16_t *vq, int32_t *tab,
+                                                             const int32_t *off, int64_t cap) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int i = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
-    const int64_t dblk = (int64_t)s * Mq + i;
-    if (tid == 0) tab[dblk] = (int32_t)dblk;
     int ctx = a.context_lens[s];
     ctx = min(max(ctx, 0), min(a.M * BS, a.max_context_len));  // the attention kernel flags it
-    if (i >= (ctx + BS - 1) / BS) return;
+    const bool attended = i < (ctx + BS - 1) / BS;
+    const int64_t dblk = (int64_t)off[s] + i;
+    const bool fits = dblk < cap;
+    if (tid == 0) {
+        tab[(int64_t)s * Mq + i] = (attended && fits) ? (int32_t)dblk : -1;
+        if (attended && !fits && a.err_flag) atomicOr(a.err_flag, PA_FLAG_WORKSPACE_SHORT);
+    }
+    if (!attended || !fits) return;
     const int b = a.block_tables[(int64_t)s * a.M + i];
     const bool valid = b >= 0 && b < a.N;
     if (!valid && tid == 0 && a.err_flag) atomicOr(a.err_flag, PA_FLAG_BLOCK_OUT_OF_RANGE);
@@ -725,16 +775,21 @@ __global__ void __launch_bounds__(256) dequant_blocks_kernel(const __grid_consta
 }  // namespace
 
 cudaError_t launch_dequant_blocks(const MultiArgs &a, int bs, int kv_dtype, int Mq, uint16_t *kq, uint16_t *vq,
-                                  int32_t *tab, cudaStream_t stream) {
+                                  int32_t *tab, int32_t *off, int64_t cap, cudaStream_t stream) {
+    cudaError_t err = bs == 16 ? launch_dependent(pool_offsets_kernel<16>, dim3(1), dim3(256), 0, stream, a, off)
+                               : launch_dependent(pool_offsets_kernel<32>, dim3(1), dim3(256), 0, stream, a, off);
+    if (err != cudaSuccess) return err;
     const dim3 grid(Mq, a.S);
-    if (kv_dtype == PA_KV_INT8) {
-        if (bs == 16) dequant_blocks_kernel<int8_t, 16><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
-        else dequant_blocks_kernel<int8_t, 32><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
-    } else {
-        if (bs == 16) dequant_blocks_kernel<tc_e4m3, 16><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
-        else dequant_blocks_kernel<tc_e4m3, 32><<<grid, 256, 0, stream>>>(a, Mq, kq, vq, tab);
-    }
-    return cudaGetLastError();
+    const int32_t *coff = off;
+    if (kv_dtype == PA_KV_INT8)
+        return bs == 16 ? launch_dependent(dequant_blocks_kernel<int8_t, 16>, grid, dim3(256), 0, stream, a, Mq, kq, vq,
+                                           tab, coff, cap)
+                        : launch_dependent(dequant_blocks_kernel<int8_t, 32>, grid, dim3(256), 0, stream, a, Mq, kq, vq,
+                                           tab, coff, cap);
+    return bs == 16 ? launch_dependent(dequant_blocks_kernel<tc_e4m3, 16>, grid, dim3(256), 0, stream, a, Mq, kq, vq,
+                                       tab, coff, cap)
+                    : launch_dependent(dequant_blocks_kernel<tc_e4m3, 32>, grid, dim3(256), 0, stream, a, Mq, kq, vq,
+                                       tab, coff, cap);
 }
 
 cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream) {

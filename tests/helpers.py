@@ -147,7 +147,8 @@ def compare_row_scaled(got: torch.Tensor, ref: np.ndarray, kv_dtype: str):
     return float(err.max()), float(err.mean())
 
 
-def gpu_multi_step(case: workloads.PagedCase, device, max_query_len=None, max_context_len=None):
+def gpu_multi_step(case: workloads.PagedCase, device, max_query_len=None, max_context_len=None,
+                   workspace_bytes=None):
     """Append every new token, then multi-token attention, on the GPU.  Output rows of
     no sequence stay NaN.  Returns dict(out, k_cache, v_cache, flag)."""
     import paged_kv_cache_197_gb300 as pa
@@ -179,9 +180,12 @@ def gpu_multi_step(case: workloads.PagedCase, device, max_query_len=None, max_co
     if max_query_len is None:
         max_query_len = max(1, max(case.meta["query_lens"]))
     out = torch.full_like(c.q, float("nan"))
+    ws = None
+    if workspace_bytes is not None:  # a given size (else the binding sizes it)
+        ws = torch.empty(workspace_bytes, dtype=torch.uint8, device=device)
     pa.pa_multi_token_attention(out, c.q, k_cache, v_cache, c.block_tables, c.context_lens,
                                 c.query_start, case.scale, max_context_len, max_query_len,
-                                k_scale=k_scale, v_scale=v_scale, err_flag=flag)
+                                workspace=ws, k_scale=k_scale, v_scale=v_scale, err_flag=flag)
     torch.cuda.synchronize(device)
     return dict(out=out, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
                 flag=int(flag.item()))

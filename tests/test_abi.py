@@ -248,11 +248,21 @@ def test_multi_token_workspace_and_checks(lib):
     assert ws(kv_dtype=pa.PA_KV_INT8) == ws() and ws(kv_dtype=pa.PA_KV_FP8) == ws()
     # 16 tokens x 4 heads: the tcgen05 path's plan for every cache type (16 CTAs of
     # columns fill less than half the SMs, so the contexts are split for one wave); an
-    # 8-bit cache adds the bf16 pool of the attended blocks (K and V) and its table
-    pool = 4 * (-(-8000 // 16)) * 2 * 16 * 128 * 2
-    table = up(4 * (-(-8000 // 16)) * 4)
+    # 8-bit cache adds the table of pool slots [S][Mq], the sequences' pool offsets
+    # [S + 1], and the bf16 pool of the attended blocks (K and V), at most S x Mq blocks
+    Mq = -(-8000 // 16)
+    block = 2 * 16 * 128 * 2
+    table = up(4 * Mq * 4) + up(4 * 5)
     for dt in (pa.PA_KV_INT8, pa.PA_KV_FP8):
-        assert ws(max_query_len=16, kv_dtype=dt) == ws(max_query_len=16) + 2 * up(pool) + table
+        assert ws(max_query_len=16, kv_dtype=dt) == ws(max_query_len=16) + table + 2 * 4 * Mq * block
+        # sized for the tokens the batch holds: ceil(total / bs) + S blocks
+        for total in (1, 5000, 16000, 32000):
+            got = pa.pa_multi_token_workspace_size_for_tokens(4, 64, 8, 2, 128, 16, dt, 8000, 16, total)
+            blocks = min(4 * Mq, -(-total // 16) + 4)
+            assert got == ws(max_query_len=16) + table + 2 * blocks * block
+        assert pa.pa_multi_token_workspace_size_for_tokens(4, 64, 8, 2, 128, 16, dt, 8000, 16, -1) == 0
+    # bf16 caches and narrow chunks have no pool: the token count changes nothing
+    assert pa.pa_multi_token_workspace_size_for_tokens(4, 64, 8, 2, 128, 16, 0, 8000, 16, 77) == ws(max_query_len=16)
     assert ws(max_query_len=16, D=64) != ws(max_query_len=16)  # head_dim 64: the mma.sync plan
     assert ws(kv_dtype=7) == 0
     assert ws(max_query_len=0) == 0
@@ -298,3 +308,24 @@ def test_binding_rejects_host_tensors(lib):
     x = torch.zeros((2, 4, 128), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pa.pa_decode(x, x, x, x, x, x, 0.1, 16)
+
+
+def test_eight_bit_prefill_workspace_scales_with_tokens(lib):
+    """A prefill-shaped 8-bit call over a 256-sequence batch with log-uniform lengths in
+    [128, 32768]: sized for the tokens it holds, the workspace is under twice the bf16
+    bytes of the blocks it attends, where sizing every sequence at the longest context
+    would take over five times that."""
+    import paged_kv_cache_197_gb300 as pa
+    import workloads
+
+    lens = workloads.int8_lengths(256, seed=4)
+    S, Hq, Hkv, D, bs, max_q = 256, 32, 8, 128, 32, 16
+    T = S * max_q
+    total = sum(lens)
+    attended = sum(-(-c // bs) for c in lens) * Hkv * bs * D * 2 * 2  # bf16 K and V
+    tight = pa.pa_multi_token_workspace_size_for_tokens(S, T, Hq, Hkv, D, bs, pa.PA_KV_FP8, max(lens), max_q,
+                                                         total)
+    loose = pa.pa_multi_token_workspace_size(S, T, Hq, Hkv, D, bs, pa.PA_KV_FP8, max(lens), max_q)
+    assert attended < tight <= 2 * attended
+    assert loose > 5 * attended
+

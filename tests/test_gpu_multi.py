@@ -298,3 +298,36 @@ def test_full_size_sampled(oracle, name):
     sub, rows = _sequences(case, seqs)
     ref = helpers.oracle_multi_out(sub, oracle, caches)
     helpers.compare(got["out"][rows.to(DEV)], ref, case.kv_dtype)
+
+
+@pytest.mark.parametrize("kv_dtype", ["int8", "fp8"])
+def test_eight_bit_pool_sized_for_tokens(oracle, kv_dtype):
+    """Prefill-shaped 8-bit calls dequantise the attended blocks into a pool packed
+    sequence after sequence: a workspace sized for the batch's tokens gives the same
+    result as one sized for every sequence at the longest context; one whose pool is
+    short by a block raises PA_FLAG_WORKSPACE_SHORT (the block left out is read as
+    zeros; the attention kernel may flag its table entry as out of range too)."""
+    import paged_kv_cache_197_gb300 as pa
+
+    lens, qlen = [300, 1000, 77, 650], [300, 130, 1, 64]
+    case = workloads.build_multi_case(f"pool-{kv_dtype}", S=4, Hq=16, Hkv=4, D=128, bs=16, context_lens=lens,
+                                      query_lens=qlen, seed=35, kv_dtype=kv_dtype)
+    T = case.q.shape[0]
+    dt = pa.PA_KV_INT8 if kv_dtype == "int8" else pa.PA_KV_FP8
+    tight = pa.pa_multi_token_workspace_size_for_tokens(4, T, 16, 4, 128, 16, dt, max(lens), max(qlen), sum(lens))
+    loose = pa.pa_multi_token_workspace_size(4, T, 16, 4, 128, 16, dt, max(lens), max(qlen))
+    assert tight < loose
+    caches = helpers.oracle_caches(case, oracle)
+    ref = helpers.oracle_multi_out(case, oracle, caches)
+    rows = helpers.covered_rows(case)
+    got = helpers.gpu_multi_step(case, DEV, workspace_bytes=tight)
+    assert got["flag"] == 0
+    helpers.compare(got["out"][torch.as_tensor(rows, device=DEV)], ref[rows], kv_dtype)
+    # the exact need: every attended block, none to spare
+    need = sum(-(-c // 16) for c in lens)
+    block = 4 * 16 * 128 * 2
+    short = tight - 2 * block * (-(-sum(lens) // 16) + 4 - need) - 2 * block
+    got = helpers.gpu_multi_step(case, DEV, workspace_bytes=short)
+    assert got["flag"] & pa.PA_FLAG_WORKSPACE_SHORT
+    assert got["flag"] & ~(pa.PA_FLAG_WORKSPACE_SHORT | pa.PA_FLAG_BLOCK_OUT_OF_RANGE) == 0
+
