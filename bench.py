@@ -72,6 +72,9 @@ L2_BYTES = 126 * 1024 * 1024
 NCU_TRAFFIC = {
     # the decode kernel launched as a programmatic dependent (griddepcontrol.wait first)
     ("gqa70b", "b150daeb73620bab"): 655764736 + 5164800,
+    ("mha13b", "b150daeb73620bab"): 1392701696 + 3443712,
+    ("int8", "b150daeb73620bab"): 3144388864 + 5860352,
+    ("fp8", "b150daeb73620bab"): 3144270848 + 5449984,
     ("mha13b", "0a92d8beb0508d47"): 1392700672 + 3298304,
     ("gqa70b", "0a92d8beb0508d47"): 655764224 + 5198848,
     ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
@@ -87,8 +90,10 @@ NCU_TRAFFIC = {
 }
 
 
-# the nominal HBM3e bandwidth of one GB300 (about 8 TB/s), beside the measured copy rate
+# the nominal HBM3e bandwidth of one GB300 (about 8 TB/s) and its dense bf16 tensor
+# rate, beside the measured copy rate and cuBLAS rate
 NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
 # default number of layers per step: the 70B-shaped workload runs a whole model's 80
 # layers (distinct pools); the others one layer
 DEFAULT_LAYERS = {"gqa70b": 80}
@@ -499,6 +504,8 @@ def run_ours(args, rank, world, device) -> dict | None:
             res["roofline"].update({"bound": "tensor", "achieved": round(tflops, 1), "peak": tpeak,
                                     "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4),
                                     "peak_source": peaks["source"] + " (cuBLAS bf16 burst)",
+                                    "nominal_peak": NOMINAL_BF16_TFLOPS,
+                                    "frac_of_nominal": round(tflops / NOMINAL_BF16_TFLOPS, 4),
                                     "hbm_gbs": round(achieved, 1)})
         else:
             res["roofline"]["tflops"] = round(tflops, 1)
