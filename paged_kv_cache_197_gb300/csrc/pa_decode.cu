@@ -46,6 +46,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPartBlocks = 256;  // 4096-token partitions of 16-token blocks
 constexpr int kHeadsPerCta = 8;
+constexpr int kMergeInRegs = 16;  // partitions whose partial rows the merge loads at once
 
 // ------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void ldg16(uint32_t *w, const void *p) {
@@ -453,7 +454,7 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
     }
 }
 
-template <typename KV, int D, int BS, int TILE>
+template <typename KV, int D, int BS, int TILE, bool PER_TOKEN>
 __global__ void __launch_bounds__(kThreads)
 paged_decode_kernel(const DecodeArgs a) {
     using G_ = Geo<KV, D, TILE>;
@@ -463,7 +464,7 @@ paged_decode_kernel(const DecodeArgs a) {
     __shared__ float s_l[kWarps][kHeadsPerCta];
     __shared__ __align__(16) float s_o[kWarps][kHeadsPerCta][D];
 
-    const int part = blockIdx.x;
+    const int part = PER_TOKEN ? blockIdx.x / a.Lq : blockIdx.x;
     const int kvh = blockIdx.y / a.head_chunks;
     const int chunk = blockIdx.y % a.head_chunks;
     const int s = blockIdx.z;
@@ -473,10 +474,24 @@ paged_decode_kernel(const DecodeArgs a) {
     // everything this kernel reads may come from the kernel before it on the stream
     // (a programmatic dependent launch): wait for that grid before any load
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int ctx = checked_context(a, s, BS, part == 0 && blockIdx.y == 0 && tid == 0);
+    const bool reporter = blockIdx.x == 0 && blockIdx.y == 0 && tid == 0;
+    int ctx = checked_context(a, s, BS, reporter);
+    int row = s;  // the q / out row
+    if constexpr (PER_TOKEN) {
+        // new token i of sequence s: rows [r0, r1) of the call, causal limit ctx - L + i + 1
+        const int i = blockIdx.x - part * a.Lq;
+        const int r0 = a.query_start[s], r1 = a.query_start[s + 1], L = r1 - r0;
+        if (!(r0 >= 0 && r1 <= a.T && L >= 0 && L <= ctx && L <= a.Lq)) {
+            if (reporter) raise_flag(a.err_flag, PA_FLAG_QUERY_OUT_OF_RANGE);
+            return;
+        }
+        if (i >= L) return;
+        ctx = ctx - L + i + 1;
+        row = r0 + i;
+    }
     // tokens before `start` (a shared prefix, attended by the grouped prefix kernel)
     // are skipped; start is a multiple of the block size
-    const int start = a.start_tokens ? min(a.start_tokens[s], ctx) : 0;
+    const int start = (!PER_TOKEN && a.start_tokens) ? min(a.start_tokens[s], ctx) : 0;
     const int nparts = max(1, (ctx - start + a.part_tokens - 1) / a.part_tokens);
     if (part >= nparts) return;
     const int tok_begin = start + part * a.part_tokens;
@@ -498,7 +513,7 @@ paged_decode_kernel(const DecodeArgs a) {
     // q fragments: lane (g, t) holds head g's values at the K-row positions it owns
     uint32_t qw[G_::QW];
     if (g < nh) {
-        const char *qrow = reinterpret_cast<const char *>(a.q + ((int64_t)s * a.Hq + h0 + g) * D);
+        const char *qrow = reinterpret_cast<const char *>(a.q + ((int64_t)row * a.Hq + h0 + g) * D);
 #pragma unroll
         for (int c = 0; c < G_::K_CHUNKS; ++c)
             ldg_bytes<32 / G_::ELEM>(&qw[c * (8 / G_::ELEM)],
@@ -626,18 +641,18 @@ paged_decode_kernel(const DecodeArgs a) {
         uint32_t packed[DPT / 2];
 #pragma unroll
         for (int e = 0; e < DPT / 2; ++e) packed[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-        uint16_t *dst = a.out + ((int64_t)s * a.Hq + h) * D + d0;
+        uint16_t *dst = a.out + ((int64_t)row * a.Hq + h) * D + d0;
         if constexpr (DPT == 8)
             *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         else
             *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
     } else {
-        const int64_t row = ((int64_t)s * a.Hq + h) * a.max_parts + part;
-        float *dst = a.ws_acc + row * D + d0;
+        const int64_t prow = ((int64_t)row * a.Hq + h) * a.max_parts + part;
+        float *dst = a.ws_acc + prow * D + d0;
 #pragma unroll
         for (int e = 0; e < DPT; e += 4)
             *reinterpret_cast<float4 *>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-        if ((tid & 15) == 0) *reinterpret_cast<float2 *>(a.ws_ml + row * 2) = make_float2(mmax, lsum);
+        if ((tid & 15) == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(mmax, lsum);
     }
 }
 
@@ -659,10 +674,68 @@ __global__ void __launch_bounds__(128) merge_partitions_kernel(const __grid_cons
     const int64_t pair = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);  // s * Hq + h
     if (pair >= (int64_t)a.S * a.Hq) return;
     const int s = (int)(pair / a.Hq);
+    const int64_t row0 = pair * a.max_parts;
+    if (a.max_parts <= kMergeInRegs) {
+        // every partition's (max, sum) and this lane's slice of every partial row are
+        // loaded at once, with the context length: one round trip; rows of partitions
+        // past the context are loaded but never used (they may hold anything)
+        const int ctx_raw = a.context_lens[s];
+        float2 ml = make_float2(-INFINITY, 0.0f);
+        if (lane < a.max_parts) ml = *reinterpret_cast<const float2 *>(a.ws_ml + (row0 + lane) * 2);
+        float v[kMergeInRegs][PER];
+#pragma unroll
+        for (int q = 0; q < kMergeInRegs; ++q) {
+            if (q < a.max_parts) {
+                const float *src = a.ws_acc + (row0 + q) * D + lane * PER;
+                if constexpr (PER == 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src);
+                    v[q][0] = x.x;
+                    v[q][1] = x.y;
+                    v[q][2] = x.z;
+                    v[q][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2 *>(src);
+                    v[q][0] = x.x;
+                    v[q][1] = x.y;
+                }
+            }
+        }
+        const int lim = min(a.M * BS, a.max_context_len);
+        const int ctx = ctx_raw < 0 ? 0 : min(ctx_raw, lim);
+        const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
+        if (nparts <= 1) return;  // the decode kernel wrote the output itself
+        const bool mine = lane < nparts;
+        float mmax = mine ? ml.x : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
+        const float mbase = mmax == -INFINITY ? 0.0f : mmax;
+        const float f = mine ? fast_exp2(ml.x - mbase) : 0.0f;
+        float lsum = mine ? f * ml.y : 0.0f;
+        float acc[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMergeInRegs; ++q) {
+            const float fq = __shfl_sync(0xffffffffu, f, q);
+            if (q < nparts) {
+#pragma unroll
+                for (int e = 0; e < PER; ++e) acc[e] += fq * v[q][e];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+        uint16_t *dst = a.out + pair * D + lane * PER;
+        if constexpr (PER == 4)
+            *reinterpret_cast<uint2 *>(dst) =
+                make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+        else
+            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        return;
+    }
     const int ctx = checked_context(a, s, BS, false);
     const int nparts = (ctx + a.part_tokens - 1) / a.part_tokens;
     if (nparts <= 1) return;  // the decode kernel wrote the output itself
-    const int64_t row0 = pair * a.max_parts;
     float mmax = -INFINITY;
     for (int p = lane; p < nparts; p += 32) mmax = fmaxf(mmax, a.ws_ml[(row0 + p) * 2]);
 #pragma unroll
@@ -714,7 +787,7 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     // previous layer's merge): it launches while that kernel drains and waits for it
     // before reading
     dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
-    cudaError_t err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE>, grid, dim3(kThreads), 0, stream, a);
+    cudaError_t err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE, false>, grid, dim3(kThreads), 0, stream, a);
     if (err != cudaSuccess || a.max_parts == 1 || a.partials_only) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((int64_t)a.S * a.Hq + 3) / 4));
@@ -736,6 +809,18 @@ cudaError_t launch_bs(const DecodeArgs &a, int bs, cudaStream_t stream) {
     return launch_typed<KV, D, 32, ONE_BYTE ? 32 : 16>(a, stream);
 }
 
+// Per-token mode: the new tokens of one partition are consecutive CTAs, so the CTAs
+// reading the same K/V tiles run side by side and all but the first hit L2.
+template <typename KV, int D>
+cudaError_t launch_rows_bs(const DecodeArgs &a, int bs, cudaStream_t stream) {
+    constexpr bool ONE_BYTE = sizeof(KV) == 1;
+    const dim3 grid((unsigned)(a.max_parts * a.Lq), a.Hkv * a.head_chunks, a.S);
+    if (bs == 16)
+        return launch_dependent(paged_decode_kernel<KV, D, 16, 16, true>, grid, dim3(kThreads), 0, stream, a);
+    return launch_dependent(paged_decode_kernel<KV, D, 32, ONE_BYTE ? 32 : 16, true>, grid, dim3(kThreads), 0,
+                            stream, a);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
@@ -745,6 +830,15 @@ cudaError_t launch_decode(const DecodeArgs &a, int D, int bs, int kv_dtype, cuda
     if (kv_dtype == PA_KV_FP8)
         return D == 128 ? launch_bs<e4m3_t, 128>(a, bs, stream) : launch_bs<e4m3_t, 64>(a, bs, stream);
     return D == 128 ? launch_bs<int8_t, 128>(a, bs, stream) : launch_bs<int8_t, 64>(a, bs, stream);
+}
+
+cudaError_t launch_decode_rows(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
+    if (!a.query_start || a.Lq <= 0 || a.start_tokens || a.partials_only) return cudaErrorInvalidValue;
+    if (kv_dtype == PA_KV_BF16)
+        return D == 128 ? launch_rows_bs<uint16_t, 128>(a, bs, stream) : launch_rows_bs<uint16_t, 64>(a, bs, stream);
+    if (kv_dtype == PA_KV_FP8)
+        return D == 128 ? launch_rows_bs<e4m3_t, 128>(a, bs, stream) : launch_rows_bs<e4m3_t, 64>(a, bs, stream);
+    return D == 128 ? launch_rows_bs<int8_t, 128>(a, bs, stream) : launch_rows_bs<int8_t, 64>(a, bs, stream);
 }
 
 }  // namespace pa

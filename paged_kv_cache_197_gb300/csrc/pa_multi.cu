@@ -44,6 +44,7 @@ constexpr int kColsPerWarp = 16;                   // two mma n-tiles of 8 colum
 constexpr int kColsPerCta = kWarps * kColsPerWarp;  // 128
 constexpr int kChunk = 64;                         // tokens per shared-memory stage
 constexpr int kMaxPartBlocks = 4096 / 16;          // block ids of one partition
+constexpr int kPerTokenMaxQuery = 8;               // longest chunk served one CTA per token
 
 __device__ __forceinline__ void raise_flag(int *err_flag, int bit) {
     if (err_flag) atomicOr(err_flag, bit);
@@ -767,8 +768,55 @@ cudaError_t launch_multi_kv(const MultiArgs &a, int D, int bs, cudaStream_t stre
     return bs == 16 ? launch_multi_typed<KV, 64, 16>(a, stream) : launch_multi_typed<KV, 64, 32>(a, stream);
 }
 
+bool multi_per_token_eligible(int D, int kv_dtype, int G, int max_query_len) {
+    (void)D;
+    (void)G;
+    // draft verification with an 8-bit cache: the decode kernel keeps the codes in
+    // registers and converts each tile once per CTA, where the mma.sync kernel converts
+    // through shared memory between barriers (measured on GB300 with an fp8 cache,
+    // 70B-shaped 4-token verification: 263 us on the mma.sync kernel)
+    return (kv_dtype == PA_KV_INT8 || kv_dtype == PA_KV_FP8) && max_query_len <= kPerTokenMaxQuery;
+}
+
+// Per-token mode of the decode kernel: the multi-token arguments as decode arguments,
+// then the multi-token merge over the same [T][Hq][max_parts] partials.
+static cudaError_t launch_multi_per_token(const MultiArgs &m, int D, int bs, int kv_dtype, cudaStream_t stream) {
+    DecodeArgs a{};
+    a.out = m.out;
+    a.q = m.q;
+    a.k_cache = m.k_cache;
+    a.v_cache = m.v_cache;
+    a.k_scale = m.k_scale;
+    a.v_scale = m.v_scale;
+    a.block_tables = m.block_tables;
+    a.context_lens = m.context_lens;
+    a.ws_acc = m.ws_acc;
+    a.ws_ml = m.ws_ml;
+    a.err_flag = m.err_flag;
+    a.M = m.M;
+    a.S = m.S;
+    a.Hq = m.Hq;
+    a.Hkv = m.Hkv;
+    a.G = m.G;
+    a.N = m.N;
+    a.head_chunks = (m.G + 7) / 8;
+    a.part_tokens = m.part_tokens;
+    a.max_parts = m.max_parts;
+    a.max_context_len = m.max_context_len;
+    a.scale_log2 = m.scale_log2;
+    a.query_start = m.query_start;
+    a.T = m.T;
+    a.Lq = m.max_query_len;
+    cudaError_t err = launch_decode_rows(a, D, bs, kv_dtype, stream);
+    if (err != cudaSuccess || m.max_parts == 1) return err;
+    return launch_multi_merge(m, D, bs, stream);
+}
+
 cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
     if (kv_dtype == PA_KV_BF16 && multi_tc_eligible(D, kv_dtype, a.G, a.max_query_len)) return launch_multi_tc(a, bs, stream);
+    if (!multi_tc_eligible(D, kv_dtype, a.G, a.max_query_len) &&
+        multi_per_token_eligible(D, kv_dtype, a.G, a.max_query_len))
+        return launch_multi_per_token(a, D, bs, kv_dtype, stream);
     if (kv_dtype == PA_KV_INT8) return launch_multi_kv<int8_t>(a, D, bs, stream);
     if (kv_dtype == PA_KV_FP8) return launch_multi_kv<e4m3_tag>(a, D, bs, stream);
     return launch_multi_kv<uint16_t>(a, D, bs, stream);

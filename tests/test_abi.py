@@ -180,16 +180,19 @@ def test_multi_token_workspace_and_checks(lib):
     give 4 waves of 2 CTAs per SM and contexts are <= 4096 tokens, else the best of
     (last-wave fill) x (len / (len + 512)) over n balanced partitions of the longest
     context (ceil(ctx / n) rounded up to 64 tokens, 256..4096) with >= 2 waves (256 as
-    the fallback).  The workspace holds (D + 2) fp32 per query row, head and
-    partition."""
+    the fallback).  Narrow chunks (at most 8 new tokens) of an 8-bit cache off the
+    tcgen05 path run on the decode kernel, one CTA per (new token, up to 8 query heads):
+    the same rule with those CTAs as the units.  The workspace
+    holds (D + 2) fp32 per query row, head and partition."""
     import math
 
     import paged_kv_cache_197_gb300 as pa
 
-    def plan(S, Hq, Hkv, D, max_ctx, max_q, sms=152):
+    def plan(S, Hq, Hkv, D, max_ctx, max_q, sms=152, kv=pa.PA_KV_BF16):
         G = Hq // Hkv
         cb = max(1, -(-max_q * G // 128))
-        units = S * Hkv * cb
+        per_token = kv != pa.PA_KV_BF16 and not (D == 128 and max_q * G >= 64) and max_q <= 8
+        units = S * Hkv * -(-G // 8) * max_q if per_token else S * Hkv * cb
         ctx = max(max_ctx, 1)
         if D == 128 and max_q * G >= 64:
             if units < sms:
@@ -223,29 +226,35 @@ def test_multi_token_workspace_and_checks(lib):
         for ctx in (1, 63, 255, 256, 257, 1000, 2100, 4095, 4097, 8000, 12345, 32768):
             for S, Hkv, max_q, G in ((1, 1, 1, 1), (4, 8, 4, 8), (20, 8, 4, 8), (64, 8, 2, 4),
                                      (256, 8, 1, 4)):
-                pt = plan(S, Hkv * G, Hkv, 64, ctx, max_q, sms=sms)
-                n = -(-ctx // pt)
-                assert pt % 64 == 0, (sms, ctx, S, pt)
-                if n > 1:
-                    assert 256 <= pt <= 4096, (sms, ctx, S, pt)
-                    assert n * pt - ctx < 64 * n or pt == 256, (sms, ctx, S, pt)
+                for kv in (pa.PA_KV_BF16, pa.PA_KV_FP8):
+                    pt = plan(S, Hkv * G, Hkv, 64, ctx, max_q, sms=sms, kv=kv)
+                    n = -(-ctx // pt)
+                    assert pt % 64 == 0, (sms, ctx, S, pt)
+                    if n > 1:
+                        assert 256 <= pt <= 4096, (sms, ctx, S, pt)
+                        assert n * pt - ctx < 64 * n or pt == 256, (sms, ctx, S, pt)
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     for S, T, Hq, Hkv, D, max_ctx, max_q in [(20, 80, 64, 8, 128, 8000, 4), (4, 2048, 32, 8, 128, 4096, 512),
                                              (9, 72, 16, 2, 64, 12345, 8), (3, 12, 8, 8, 64, 4097, 4),
                                              (64, 128, 32, 8, 64, 3000, 2), (1, 1, 8, 1, 64, 32768, 1),
                                              (7, 40, 16, 2, 64, 2100, 8), (600, 600, 32, 32, 128, 1000, 1),
                                              (1, 128, 32, 8, 128, 32768, 128), (2, 300, 16, 2, 128, 9000, 150)]:
-        pt = plan(S, Hq, Hkv, D, max_ctx, max_q)
-        parts = -(-max_ctx // pt)
-        rows = T * Hq * parts
-        expect = 0 if parts == 1 else up(up(rows * D * 4) + rows * 2 * 4)
-        got = pa.pa_multi_token_workspace_size(S, T, Hq, Hkv, D, 16, pa.PA_KV_BF16, max_ctx, max_q)
-        assert got == expect, (S, T, got, expect)
+        for kv in (pa.PA_KV_BF16, pa.PA_KV_INT8, pa.PA_KV_FP8):
+            if kv != pa.PA_KV_BF16 and D == 128 and max_q * Hq // Hkv >= 64:
+                continue  # the dequantising pass adds its pool (below)
+            pt = plan(S, Hq, Hkv, D, max_ctx, max_q, kv=kv)
+            parts = -(-max_ctx // pt)
+            rows = T * Hq * parts
+            expect = 0 if parts == 1 else up(up(rows * D * 4) + rows * 2 * 4)
+            got = pa.pa_multi_token_workspace_size(S, T, Hq, Hkv, D, 16, kv, max_ctx, max_q)
+            assert got == expect, (S, T, kv, got, expect)
     ws = lambda **k: pa.pa_multi_token_workspace_size(  # noqa: E731
         **{**dict(S=4, T=64, Hq=8, Hkv=2, D=128, bs=16, kv_dtype=0, max_context_len=8000,
                   max_query_len=8), **k})
     assert ws() > 0
-    assert ws(kv_dtype=pa.PA_KV_INT8) == ws() and ws(kv_dtype=pa.PA_KV_FP8) == ws()
+    # 8 new tokens x 4 heads, 8-bit caches: per-token CTAs, more of them, shorter partitions
+    assert ws(kv_dtype=pa.PA_KV_INT8) == ws(kv_dtype=pa.PA_KV_FP8) != ws()
+    assert ws(kv_dtype=pa.PA_KV_INT8, max_query_len=9) == ws(max_query_len=9)  # past 8: mma.sync
     # 16 tokens x 4 heads: the tcgen05 path's plan for every cache type (16 CTAs of
     # columns fill less than half the SMs, so the contexts are split for one wave); an
     # 8-bit cache adds the table of pool slots [S][Mq], the sequences' pool offsets

@@ -79,6 +79,21 @@ def test_long_context_partitions(oracle, kv_dtype):
     _run(case, oracle)
 
 
+@pytest.mark.parametrize("kv_dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("D,bs,Hq,Hkv", [(128, 32, 8, 2), (64, 16, 24, 2)])
+def test_eight_bit_verification_long_contexts(oracle, kv_dtype, D, bs, Hq, Hkv):
+    """Narrow chunks of an 8-bit cache on the decode kernel's per-token mode: long
+    contexts split into partitions whose boundaries fall between one new token's causal
+    limit and the next's, a chunk of one token on a one-token context, and 12 query
+    heads per kv head (a full and a partial chunk of 8 heads)."""
+    lens = [9000, 4097, 6000, 1, 2049]
+    qlen = [4, 8, 2, 1, 3]
+    case = workloads.build_multi_case(f"long8-{kv_dtype}-{D}-{Hq}", S=len(lens), Hq=Hq, Hkv=Hkv, D=D,
+                                      bs=bs, context_lens=lens, query_lens=qlen, seed=D + Hq + 5,
+                                      row_offset=1, extra_rows=2, kv_dtype=kv_dtype)
+    _run(case, oracle)
+
+
 def test_one_token_matches_decode(oracle):
     """With one new token per sequence the step is the decode step."""
     import paged_kv_cache_197_gb300 as pa
@@ -98,21 +113,23 @@ def test_one_token_matches_decode(oracle):
     helpers.compare(dec, ref, "bf16")
 
 
-def test_bad_offsets_are_skipped(oracle):
+@pytest.mark.parametrize("kv_dtype,D", [("bf16", 64), ("int8", 64), ("fp8", 128)])
+def test_bad_offsets_are_skipped(oracle, kv_dtype, D):
     """A sequence with more new tokens than max_query_len is skipped (QUERY flag, rows
-    untouched); an empty chunk writes nothing; the others are exact."""
+    untouched); an empty chunk writes nothing; the others are exact.  8-bit caches: the
+    decode kernel's per-token mode."""
     import paged_kv_cache_197_gb300 as pa
 
     lens = [50, 400, 90]
     qlen = [3, 9, 0]
-    case = workloads.build_multi_case("bad", S=3, Hq=8, Hkv=2, D=64, bs=16, context_lens=lens,
-                                      query_lens=qlen, seed=34)
+    case = workloads.build_multi_case(f"bad-{kv_dtype}", S=3, Hq=8, Hkv=2, D=D, bs=16, context_lens=lens,
+                                      query_lens=qlen, seed=34, kv_dtype=kv_dtype)
     got = helpers.gpu_multi_step(case, DEV, max_query_len=4)
     assert got["flag"] == pa.PA_FLAG_QUERY_OUT_OF_RANGE
     caches = helpers.oracle_caches(case, oracle)
     ref = helpers.oracle_multi_out(case, oracle, caches)
     assert torch.isnan(got["out"][3:12].float()).all()
-    helpers.compare(got["out"][0:3], ref[0:3], "bf16")
+    helpers.compare(got["out"][0:3], ref[0:3], kv_dtype)
 
 
 def test_rejects_unsupported():
@@ -151,25 +168,32 @@ def test_block_permutation_bit_identical():
     assert torch.equal(a, b)
 
 
-def test_error_flags():
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "fp8"])
+def test_error_flags(kv_dtype):
     """A block id beyond the pool is skipped (read as zeros) and flagged; a context past
     max_context_len is clamped and flagged."""
     import paged_kv_cache_197_gb300 as pa
 
-    case = workloads.build_multi_case("flags", S=2, Hq=8, Hkv=2, D=64, bs=16, context_lens=[90, 300],
-                                      query_lens=[4, 5], seed=37, poison=False).to(DEV)
+    case = workloads.build_multi_case(f"flags-{kv_dtype}", S=2, Hq=8, Hkv=2, D=64, bs=16,
+                                      context_lens=[90, 300], query_lens=[4, 5], seed=37, poison=False,
+                                      kv_dtype=kv_dtype)
+    cached = helpers.gpu_multi_step(case, DEV)
+    assert cached["flag"] == 0
+    case = case.to(DEV)
+    k, v = cached["k_cache"], cached["v_cache"]
+    sc = dict(k_scale=cached["k_scale"], v_scale=cached["v_scale"])
     out = torch.empty_like(case.q)
     flag = torch.zeros(1, dtype=torch.int32, device=DEV)
     tables = case.block_tables.clone()
     tables[1, 2] = case.N + 7
-    pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, tables, case.context_lens,
-                                case.query_start, case.scale, 300, 5, err_flag=flag)
+    pa.pa_multi_token_attention(out, case.q, k, v, tables, case.context_lens,
+                                case.query_start, case.scale, 300, 5, err_flag=flag, **sc)
     torch.cuda.synchronize()
     assert flag.item() == pa.PA_FLAG_BLOCK_OUT_OF_RANGE
     assert torch.isfinite(out.float()).all()
     flag.zero_()
-    pa.pa_multi_token_attention(out, case.q, case.k_pool, case.v_pool, case.block_tables,
-                                case.context_lens, case.query_start, case.scale, 200, 5, err_flag=flag)
+    pa.pa_multi_token_attention(out, case.q, k, v, case.block_tables,
+                                case.context_lens, case.query_start, case.scale, 200, 5, err_flag=flag, **sc)
     torch.cuda.synchronize()
     assert flag.item() == pa.PA_FLAG_CONTEXT_OUT_OF_RANGE
 
