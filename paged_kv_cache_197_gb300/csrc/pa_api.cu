@@ -508,10 +508,12 @@ static MultiPlan plan_multi(int S, int T, int Hq, int Hkv, int D, int bs, int kv
     const int G = Hq / Hkv;
     p.CB = std::max(1, (int)(((int64_t)max_query_len * G + multi_cols_per_cta() - 1) / multi_cols_per_cta()));
     const bool tc = multi_tc_eligible(D, kv_dtype, G, max_query_len);
-    // CTAs per context partition: the decode kernel in per-token mode takes one new
-    // token and up to 8 query heads each
+    // CTAs per context partition: the decode kernel in rows mode takes one or two new
+    // tokens and up to 8 query heads each
     const bool per_token = !tc && multi_per_token_eligible(D, kv_dtype, G, max_query_len);
-    const int64_t units = per_token ? (int64_t)S * Hkv * ((G + 7) / 8) * max_query_len : (int64_t)S * Hkv * p.CB;
+    const int rows = decode_rows_per_cta(max_query_len);
+    const int64_t units = per_token ? (int64_t)S * Hkv * ((G + 7) / 8) * ((max_query_len + rows - 1) / rows)
+                                    : (int64_t)S * Hkv * p.CB;
     const double slots = (double)device_sms() * 2;  // both kernels keep two CTAs per SM
     const int ctx = std::max(max_context_len, 1);
     p.part_tokens = 256;

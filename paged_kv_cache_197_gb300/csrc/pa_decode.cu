@@ -217,7 +217,7 @@ struct Tile {
     uint32_t k[GEO::K_ROWS][GEO::K_WORDS];
     uint32_t v[GEO::V_TOKS][GEO::V_WORDS];
     float ks, vs;  // int8: scales of token `lane` of the tile
-    int nvalid;    // tokens of the tile inside the context
+    int nvalid;    // tokens of the partition from the tile's first on (>= TILE: all valid)
 };
 
 // V row j of a lane: sub-tile j / 4, token 2t, 2t+1, 2t+8 or 2t+9 of it.
@@ -233,7 +233,7 @@ __device__ __forceinline__ void load_tile(Tile<Geo<KV, D, TILE>> &R, const Decod
     using G_ = Geo<KV, D, TILE>;
     const int tok0 = tok_begin + i * TILE;
     int blk = s_blk[tok0 / BS - blk_begin];
-    R.nvalid = min(TILE, tok_end - tok0);
+    R.nvalid = tok_end - tok0;  // may exceed TILE: tokens of the partition from this tile on
     if (blk < 0) {  // flagged when the table was read: the tile is skipped
         R.nvalid = 0;
         blk = 0;
@@ -284,25 +284,33 @@ __device__ __forceinline__ int out_dim(int mt, int g, int h) {
         return g * (D / 8) + 2 * mt + h;
 }
 
-template <typename KV, int D, int TILE>
+// One warp's online-softmax state for NC column sets.  A column set is the CTA's
+// query heads for one query token: decode has one, a CTA serving several new tokens
+// of a multi-token call one per token.
+template <typename KV, int D, int TILE, int NC>
 struct WarpState {
-    float o[D / 16][4];  // O^T fragments: [d tile][c0..c3]
-    float m[2];          // running max of heads 2t, 2t+1 (log2 units)
-    float l[2];          // running sum, partial over this lane's tokens
-    int ve;              // int8: O is kept in units of 2^ve (ve >= exponent of every value scale so far)
-    float ps[2];         // int8: sum of the fp16 weights fed to the value product, heads 2t, 2t+1
+    float o[NC][D / 16][4];  // O^T fragments: [set][d tile][c0..c3]
+    float m[NC][2];          // running max of heads 2t, 2t+1 (log2 units)
+    float l[NC][2];          // running sum, partial over this lane's tokens
+    int ve;                  // 8-bit: O is kept in units of 2^ve (ve >= exponent of every value scale so far)
+    float ps[NC][2];         // int8: sum of the fp16 weights fed to the value product, heads 2t, 2t+1
 };
 
-template <typename KV, int D, int TILE>
-__device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
-                                             Tile<Geo<KV, D, TILE>> &R, const uint32_t *qw,
-                                             const float (&qb)[2], float scale_log2, int g, int t) {
+// Consume one tile for NC column sets.  Set c sees the tile's first R.nvalid - cut[c]
+// tokens (its own causal limit); every K and V entry is converted once and feeds the
+// products of all sets.
+template <typename KV, int D, int TILE, int NC>
+__device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE, NC> &st, Tile<Geo<KV, D, TILE>> &R,
+                                             const uint32_t (&qw)[NC][Geo<KV, D, TILE>::QW],
+                                             const float (&qb)[NC][2], const float (&scale_log2)[NC],
+                                             const int (&cut)[NC], int g, int t) {
     using G_ = Geo<KV, D, TILE>;
     // ---- scores S[token][head] for the tile's 16-token sub-tiles
-    float sc[G_::SUB][4];
+    float sc[NC][G_::SUB][4];
 #pragma unroll
     for (int s = 0; s < G_::SUB; ++s) {
-        sc[s][0] = sc[s][1] = sc[s][2] = sc[s][3] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) sc[c][s][0] = sc[c][s][1] = sc[c][s][2] = sc[c][s][3] = 0.0f;
 #pragma unroll
         for (int kc = 0; kc < G_::KSTEPS; ++kc) {
             uint32_t a0, a1, a2, a3;
@@ -311,58 +319,73 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
                 a2 = R.k[2 * s][2 * kc + 1];
                 a1 = R.k[2 * s + 1][2 * kc];
                 a3 = R.k[2 * s + 1][2 * kc + 1];
-                mma_bf16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) mma_bf16(sc[c][s], a0, a1, a2, a3, qw[c][2 * kc], qw[c][2 * kc + 1]);
             } else {
                 k8x4_to_f16<KV>(R.k[2 * s][kc], a0, a2);
                 k8x4_to_f16<KV>(R.k[2 * s + 1][kc], a1, a3);
-                mma_f16(sc[s], a0, a1, a2, a3, qw[2 * kc], qw[2 * kc + 1]);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) mma_f16(sc[c][s], a0, a1, a2, a3, qw[c][2 * kc], qw[c][2 * kc + 1]);
             }
         }
     }
-    // ---- online softmax over the tile (log2 domain)
-    float x[G_::SUB][4];
-    float mx[2] = {-INFINITY, -INFINITY};
+    // ---- online softmax over the tile (log2 domain), per column set
+    float ksc[G_::SUB][2];  // 8-bit: key scales of tokens g and g + 8 of each sub-tile
+    if constexpr (G_::ELEM == 1) {
 #pragma unroll
-    for (int s = 0; s < G_::SUB; ++s)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int tok = 16 * s + g + 8 * (c >> 1);
-            float v = (G_::BIASED ? sc[s][c] - qb[c & 1] : sc[s][c]) * scale_log2;
-            if constexpr (G_::ELEM == 1) v *= __shfl_sync(0xffffffffu, R.ks, tok);
-            v = tok < R.nvalid ? v : -INFINITY;
-            x[s][c] = v;
-            mx[c & 1] = fmaxf(mx[c & 1], v);
-        }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
-        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
-        mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
-    }
-    float alpha[2], base[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const float mnew = fmaxf(st.m[j], mx[j]);
-        base[j] = mnew == -INFINITY ? 0.0f : mnew;
-        alpha[j] = fast_exp2(st.m[j] - base[j]);
-        st.m[j] = mnew;
-    }
-    if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll
-        for (int mt = 0; mt < G_::MT; ++mt) {
-            st.o[mt][0] *= alpha[0];
-            st.o[mt][1] *= alpha[1];
-            st.o[mt][2] *= alpha[0];
-            st.o[mt][3] *= alpha[1];
-        }
-        st.l[0] *= alpha[0];
-        st.l[1] *= alpha[1];
-        if constexpr (G_::BIASED) {
-            st.ps[0] *= alpha[0];
-            st.ps[1] *= alpha[1];
+        for (int s = 0; s < G_::SUB; ++s) {
+            ksc[s][0] = __shfl_sync(0xffffffffu, R.ks, 16 * s + g);
+            ksc[s][1] = __shfl_sync(0xffffffffu, R.ks, 16 * s + g + 8);
         }
     }
-    // int8: keep the weights p * v_scale below 1 in fp16 by working in units of 2^ve,
+    float x[NC][G_::SUB][4];
+    float base[NC][2];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int lim = R.nvalid - cut[c];
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int s = 0; s < G_::SUB; ++s)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = 16 * s + g + 8 * (e >> 1);
+                float v = (G_::BIASED ? sc[c][s][e] - qb[c][e & 1] : sc[c][s][e]) * scale_log2[c];
+                if constexpr (G_::ELEM == 1) v *= ksc[s][e >> 1];
+                v = tok < lim ? v : -INFINITY;
+                x[c][s][e] = v;
+                mx[e & 1] = fmaxf(mx[e & 1], v);
+            }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+        }
+        float alpha[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float mnew = fmaxf(st.m[c][j], mx[j]);
+            base[c][j] = mnew == -INFINITY ? 0.0f : mnew;
+            alpha[j] = fast_exp2(st.m[c][j] - base[c][j]);
+            st.m[c][j] = mnew;
+        }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
+#pragma unroll
+            for (int mt = 0; mt < G_::MT; ++mt) {
+                st.o[c][mt][0] *= alpha[0];
+                st.o[c][mt][1] *= alpha[1];
+                st.o[c][mt][2] *= alpha[0];
+                st.o[c][mt][3] *= alpha[1];
+            }
+            st.l[c][0] *= alpha[0];
+            st.l[c][1] *= alpha[1];
+            if constexpr (G_::BIASED) {
+                st.ps[c][0] *= alpha[0];
+                st.ps[c][1] *= alpha[1];
+            }
+        }
+    }
+    // 8-bit: keep the weights p * v_scale below 1 in fp16 by working in units of 2^ve,
     // ve the exponent of the largest value scale seen so far (O rescaled when it grows)
     float vmul = 1.0f;
     if constexpr (G_::ELEM == 1) {
@@ -374,15 +397,18 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
             if (e > st.ve) {
                 const float f = st.ve < -200 ? 0.0f : ldexpf(1.0f, st.ve - e);
 #pragma unroll
-                for (int mt = 0; mt < G_::MT; ++mt) {
-                    st.o[mt][0] *= f;
-                    st.o[mt][1] *= f;
-                    st.o[mt][2] *= f;
-                    st.o[mt][3] *= f;
-                }
-                if constexpr (G_::BIASED) {
-                    st.ps[0] *= f;
-                    st.ps[1] *= f;
+                for (int c = 0; c < NC; ++c) {
+#pragma unroll
+                    for (int mt = 0; mt < G_::MT; ++mt) {
+                        st.o[c][mt][0] *= f;
+                        st.o[c][mt][1] *= f;
+                        st.o[c][mt][2] *= f;
+                        st.o[c][mt][3] *= f;
+                    }
+                    if constexpr (G_::BIASED) {
+                        st.ps[c][0] *= f;
+                        st.ps[c][1] *= f;
+                    }
                 }
                 st.ve = e;
             }
@@ -399,32 +425,40 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
     }
 #pragma unroll
     for (int s = 0; s < G_::SUB; ++s) {
-        float p[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            p[c] = fast_exp2(x[s][c] - base[c & 1]);
-            st.l[c & 1] += p[c];
-            if constexpr (G_::ELEM == 1) {
-                const int tok = 16 * s + g + 8 * (c >> 1);
-                const float vsc = __shfl_sync(0xffffffffu, R.vs, tok);
-                p[c] = tok < R.nvalid ? p[c] * (vsc * vmul) : 0.0f;
-            }
+        float vsc[2];  // 8-bit: value scales of tokens g and g + 8 of the sub-tile, in units of 2^ve
+        if constexpr (G_::ELEM == 1) {
+            vsc[0] = __shfl_sync(0xffffffffu, R.vs, 16 * s + g) * vmul;
+            vsc[1] = __shfl_sync(0xffffffffu, R.vs, 16 * s + g + 8) * vmul;
         }
-        // P[head][token] as the B operand: transpose the [token][head] quarters
-        uint32_t b0, b1;
-        if constexpr (G_::ELEM == 2) {
-            b0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
-            b1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
-        } else {
-            const uint32_t w0 = pack_f16x2(p[0], p[1]), w1 = pack_f16x2(p[2], p[3]);
-            if constexpr (G_::BIASED) {  // the weights exactly as the product sees them
-                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w0));
-                const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w1));
-                st.ps[0] += f0.x + f1.x;
-                st.ps[1] += f0.y + f1.y;
+        // P[head][token] of each set as the B operand: transpose the [token][head] quarters
+        uint32_t b0[NC], b1[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const int lim = R.nvalid - cut[c];
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                p[e] = fast_exp2(x[c][s][e] - base[c][e & 1]);
+                st.l[c][e & 1] += p[e];
+                if constexpr (G_::ELEM == 1) {
+                    const int tok = 16 * s + g + 8 * (e >> 1);
+                    p[e] = tok < lim ? p[e] * vsc[e >> 1] : 0.0f;
+                }
             }
-            b0 = movmatrix_trans(w0);
-            b1 = movmatrix_trans(w1);
+            if constexpr (G_::ELEM == 2) {
+                b0[c] = movmatrix_trans(pack_bf16x2(p[0], p[1]));
+                b1[c] = movmatrix_trans(pack_bf16x2(p[2], p[3]));
+            } else {
+                const uint32_t w0 = pack_f16x2(p[0], p[1]), w1 = pack_f16x2(p[2], p[3]);
+                if constexpr (G_::BIASED) {  // the weights exactly as the product sees them
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w0));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w1));
+                    st.ps[c][0] += f0.x + f1.x;
+                    st.ps[c][1] += f0.y + f1.y;
+                }
+                b0[c] = movmatrix_trans(w0);
+                b1[c] = movmatrix_trans(w1);
+            }
         }
         const int j0 = 4 * s;  // V rows 2t, 2t+1, 2t+8, 2t+9 of this sub-tile
 #pragma unroll
@@ -446,25 +480,34 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE> &st,
                 a2 = v8_pair_to_f16<KV>(R.v[j0 + 2][w], R.v[j0 + 3][w], b);
                 a3 = v8_pair_to_f16<KV>(R.v[j0 + 2][w], R.v[j0 + 3][w], b + 1u);
             }
-            if constexpr (G_::ELEM == 2)
-                mma_bf16(st.o[mt], a0, a1, a2, a3, b0, b1);
-            else
-                mma_f16(st.o[mt], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                if constexpr (G_::ELEM == 2)
+                    mma_bf16(st.o[c][mt], a0, a1, a2, a3, b0[c], b1[c]);
+                else
+                    mma_f16(st.o[c][mt], a0, a1, a2, a3, b0[c], b1[c]);
+            }
         }
     }
 }
 
-template <typename KV, int D, int BS, int TILE, bool PER_TOKEN>
+// NT == 0: decode, one query row per sequence (grid x = partition).  NT >= 1: rows
+// mode of a multi-token call, NT consecutive new tokens of a sequence per CTA (grid x =
+// partition x token groups), each token a column set with its own causal limit.
+template <typename KV, int D, int BS, int TILE, int NT>
 __global__ void __launch_bounds__(kThreads)
 paged_decode_kernel(const DecodeArgs a) {
     using G_ = Geo<KV, D, TILE>;
+    constexpr bool ROWS = NT > 0;
+    constexpr int NC = ROWS ? NT : 1;
     static_assert(BS % TILE == 0, "a tile lies inside one block");
     __shared__ int s_blk[kMaxPartBlocks];
     __shared__ float s_m[kWarps][kHeadsPerCta];
     __shared__ float s_l[kWarps][kHeadsPerCta];
     __shared__ __align__(16) float s_o[kWarps][kHeadsPerCta][D];
 
-    const int part = PER_TOKEN ? blockIdx.x / a.Lq : blockIdx.x;
+    const int groups = ROWS ? (a.Lq + NC - 1) / NC : 1;
+    const int part = ROWS ? blockIdx.x / groups : blockIdx.x;
     const int kvh = blockIdx.y / a.head_chunks;
     const int chunk = blockIdx.y % a.head_chunks;
     const int s = blockIdx.z;
@@ -476,22 +519,25 @@ paged_decode_kernel(const DecodeArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const bool reporter = blockIdx.x == 0 && blockIdx.y == 0 && tid == 0;
     int ctx = checked_context(a, s, BS, reporter);
-    int row = s;  // the q / out row
-    if constexpr (PER_TOKEN) {
-        // new token i of sequence s: rows [r0, r1) of the call, causal limit ctx - L + i + 1
-        const int i = blockIdx.x - part * a.Lq;
+    int row0 = s;  // q / out row of column set 0 (set c: row0 + c)
+    int nt = 1;    // column sets in use
+    if constexpr (ROWS) {
+        // new tokens i0 .. i0 + nt - 1 of sequence s: rows [r0, r1) of the call, token i
+        // attends the first ctx - L + i + 1 tokens
+        const int i0 = (blockIdx.x - part * groups) * NC;
         const int r0 = a.query_start[s], r1 = a.query_start[s + 1], L = r1 - r0;
         if (!(r0 >= 0 && r1 <= a.T && L >= 0 && L <= ctx && L <= a.Lq)) {
             if (reporter) raise_flag(a.err_flag, PA_FLAG_QUERY_OUT_OF_RANGE);
             return;
         }
-        if (i >= L) return;
-        ctx = ctx - L + i + 1;
-        row = r0 + i;
+        if (i0 >= L) return;
+        nt = min(NC, L - i0);
+        ctx = ctx - L + i0 + nt;  // the last set's limit
+        row0 = r0 + i0;
     }
     // tokens before `start` (a shared prefix, attended by the grouped prefix kernel)
     // are skipped; start is a multiple of the block size
-    const int start = (!PER_TOKEN && a.start_tokens) ? min(a.start_tokens[s], ctx) : 0;
+    const int start = (!ROWS && a.start_tokens) ? min(a.start_tokens[s], ctx) : 0;
     const int nparts = max(1, (ctx - start + a.part_tokens - 1) / a.part_tokens);
     if (part >= nparts) return;
     const int tok_begin = start + part * a.part_tokens;
@@ -500,6 +546,16 @@ paged_decode_kernel(const DecodeArgs a) {
     const int nblk = max(0, (tok_end - tok_begin + BS - 1) / BS);
     const int h0 = kvh * a.G + chunk * kHeadsPerCta;
     const int nh = min(kHeadsPerCta, a.G - chunk * kHeadsPerCta);
+    // tokens of the partition that set c does not see (its limit is nt - 1 - c below
+    // the last set's); sets past nt see none
+    int cut[NC];
+    if constexpr (ROWS) {
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+            cut[c] = c < nt ? tok_end - min(ctx - (nt - 1 - c), tok_begin + a.part_tokens) : (1 << 30);
+    } else {
+        cut[0] = 0;
+    }
 
     for (int i = tid; i < nblk; i += kThreads) {
         int b = a.block_tables[(int64_t)s * a.M + blk_begin + i];
@@ -511,57 +567,70 @@ paged_decode_kernel(const DecodeArgs a) {
     }
 
     // q fragments: lane (g, t) holds head g's values at the K-row positions it owns
-    uint32_t qw[G_::QW];
-    if (g < nh) {
-        const char *qrow = reinterpret_cast<const char *>(a.q + ((int64_t)row * a.Hq + h0 + g) * D);
+    uint32_t qw[NC][G_::QW];
 #pragma unroll
-        for (int c = 0; c < G_::K_CHUNKS; ++c)
-            ldg_bytes<32 / G_::ELEM>(&qw[c * (8 / G_::ELEM)],
-                                     qrow + 2 * k_dim<G_::ELEM>(c * (16 / G_::ELEM), t));
-    } else {
+    for (int c = 0; c < NC; ++c) {
+        if (g < nh && c < nt) {
+            const char *qrow = reinterpret_cast<const char *>(a.q + ((int64_t)(row0 + c) * a.Hq + h0 + g) * D);
 #pragma unroll
-        for (int i = 0; i < G_::QW; ++i) qw[i] = 0u;
+            for (int k = 0; k < G_::K_CHUNKS; ++k)
+                ldg_bytes<32 / G_::ELEM>(&qw[c][k * (8 / G_::ELEM)],
+                                         qrow + 2 * k_dim<G_::ELEM>(k * (16 / G_::ELEM), t));
+        } else {
+#pragma unroll
+            for (int i = 0; i < G_::QW; ++i) qw[c][i] = 0u;
+        }
     }
-    float scale_log2 = a.scale_log2;
-    float qb[2] = {0.0f, 0.0f};  // int8: score bias per score column
-    if constexpr (G_::ELEM == 1) {
-        // fp16 q for the int8 products: scaled by 2^sig so the largest |q| of the CTA's
-        // heads lands in [2^13, 2^14); the scores are scaled back by 2^-sig
-        float qmax = 0.0f;
+    float scale_log2[NC];
+    float qb[NC][2];  // int8: score bias per score column
 #pragma unroll
-        for (int i = 0; i < G_::QW; ++i)
-            qmax = fmaxf(qmax, fmaxf(fabsf(__uint_as_float(qw[i] << 16)), fabsf(__uint_as_float(qw[i] & 0xffff0000u))));
+    for (int c = 0; c < NC; ++c) {
+        scale_log2[c] = a.scale_log2;
+        qb[c][0] = qb[c][1] = 0.0f;
+        if constexpr (G_::ELEM == 1) {
+            // fp16 q for the 8-bit products: scaled by 2^sig so the largest |q| of the
+            // set's heads lands in [2^13, 2^14); the scores are scaled back by 2^-sig
+            float qmax = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
-        const int sig = qmax > 0.0f ? min(100, max(-100, 14 - exponent_above(qmax))) : 0;
-        const float up = ldexpf(1.0f, sig);
+            for (int i = 0; i < G_::QW; ++i)
+                qmax = fmaxf(qmax, fmaxf(fabsf(__uint_as_float(qw[c][i] << 16)),
+                                         fabsf(__uint_as_float(qw[c][i] & 0xffff0000u))));
 #pragma unroll
-        for (int i = 0; i < G_::QW; ++i)
-            qw[i] = pack_f16x2(__uint_as_float(qw[i] << 16) * up, __uint_as_float(qw[i] & 0xffff0000u) * up);
-        scale_log2 *= ldexpf(1.0f, -sig);
-        if constexpr (G_::BIASED) {
-            // kInt8Bias * sum_d q_d of the fp16 q fed to the score product, for the
-            // heads of this lane's score columns (2t, 2t+1; head g sits in lanes 4g..)
-            float part = 0.0f;
+            for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+            const int sig = qmax > 0.0f ? min(100, max(-100, 14 - exponent_above(qmax))) : 0;
+            const float up = ldexpf(1.0f, sig);
 #pragma unroll
-            for (int i = 0; i < G_::QW; ++i) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qw[i]));
-                part += f.x + f.y;
+            for (int i = 0; i < G_::QW; ++i)
+                qw[c][i] = pack_f16x2(__uint_as_float(qw[c][i] << 16) * up,
+                                      __uint_as_float(qw[c][i] & 0xffff0000u) * up);
+            scale_log2[c] *= ldexpf(1.0f, -sig);
+            if constexpr (G_::BIASED) {
+                // kInt8Bias * sum_d q_d of the fp16 q fed to the score product, for the
+                // heads of this lane's score columns (2t, 2t+1; head g sits in lanes 4g..)
+                float sum = 0.0f;
+#pragma unroll
+                for (int i = 0; i < G_::QW; ++i) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qw[c][i]));
+                    sum += f.x + f.y;
+                }
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                qb[c][0] = kInt8Bias * __shfl_sync(0xffffffffu, sum, 8 * t);
+                qb[c][1] = kInt8Bias * __shfl_sync(0xffffffffu, sum, 8 * t + 4);
             }
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            qb[0] = kInt8Bias * __shfl_sync(0xffffffffu, part, 8 * t);
-            qb[1] = kInt8Bias * __shfl_sync(0xffffffffu, part, 8 * t + 4);
         }
     }
     __syncthreads();
 
-    WarpState<KV, D, TILE> st;
+    WarpState<KV, D, TILE, NC> st;
 #pragma unroll
-    for (int mt = 0; mt < G_::MT; ++mt) st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
-    st.m[0] = st.m[1] = -INFINITY;
-    st.l[0] = st.l[1] = 0.0f;
-    st.ps[0] = st.ps[1] = 0.0f;
+    for (int c = 0; c < NC; ++c) {
+#pragma unroll
+        for (int mt = 0; mt < G_::MT; ++mt) st.o[c][mt][0] = st.o[c][mt][1] = st.o[c][mt][2] = st.o[c][mt][3] = 0.f;
+        st.m[c][0] = st.m[c][1] = -INFINITY;
+        st.l[c][0] = st.l[c][1] = 0.0f;
+        st.ps[c][0] = st.ps[c][1] = 0.0f;
+    }
     st.ve = -1000;  // no value scale seen yet
 
     const int ntiles = (tok_end - tok_begin + TILE - 1) / TILE;
@@ -571,12 +640,12 @@ paged_decode_kernel(const DecodeArgs a) {
     while (i < ntiles) {
         if (i + kWarps < ntiles)
             load_tile<KV, D, BS, TILE>(B, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE>(st, A, qw, qb, scale_log2, g, t);
+        consume_tile<KV, D, TILE, NC>(st, A, qw, qb, scale_log2, cut, g, t);
         i += kWarps;
         if (i >= ntiles) break;
         if (i + kWarps < ntiles)
             load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE>(st, B, qw, qb, scale_log2, g, t);
+        consume_tile<KV, D, TILE, NC>(st, B, qw, qb, scale_log2, cut, g, t);
         i += kWarps;
     }
 
@@ -584,75 +653,85 @@ paged_decode_kernel(const DecodeArgs a) {
     // this grid to finish before reading)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    // ---- per-warp totals, then merge the CTA's warps through shared memory
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 4);
-        st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 8);
-        st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
-    }
-    if (g == 0) {
-        s_m[warp][2 * t] = st.m[0];
-        s_m[warp][2 * t + 1] = st.m[1];
-        s_l[warp][2 * t] = st.l[0];
-        s_l[warp][2 * t + 1] = st.l[1];
-    }
     const float oscale = (G_::ELEM == 1 && st.ve > -200) ? ldexpf(1.0f, st.ve) : 1.0f;
-    float obias[2] = {0.0f, 0.0f};  // int8: kInt8Bias * the weights summed over all tokens
-    if constexpr (G_::BIASED) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float v = st.ps[j];
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            v += __shfl_xor_sync(0xffffffffu, v, 8);
-            v += __shfl_xor_sync(0xffffffffu, v, 16);
-            obias[j] = kInt8Bias * v;
-        }
-    }
-#pragma unroll
-    for (int mt = 0; mt < G_::MT; ++mt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            s_o[warp][2 * t + (c & 1)][out_dim<G_::ELEM, D>(mt, g, c >> 1)] = (st.o[mt][c] - obias[c & 1]) * oscale;
-    __syncthreads();
-
     constexpr int DPT = D / 16;  // output values per thread: 16 threads per head
     const int hj = tid >> 4;
     const int d0 = (tid & 15) * DPT;
-    if (hj >= nh) return;
-    float mmax = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_m[w][hj]);
-    const float mbase = mmax == -INFINITY ? 0.0f : mmax;
-    float acc[DPT];
+    for (int c = 0; c < NC; ++c) {
+        if (c >= nt) break;  // uniform across the CTA
+        if (c > 0) __syncthreads();  // the previous set's reads of shared memory are done
+        // ---- per-warp totals, then merge the CTA's warps through shared memory
 #pragma unroll
-    for (int e = 0; e < DPT; ++e) acc[e] = 0.0f;
-    float lsum = 0.0f;
+        for (int j = 0; j < 2; ++j) {
+            st.l[c][j] += __shfl_xor_sync(0xffffffffu, st.l[c][j], 4);
+            st.l[c][j] += __shfl_xor_sync(0xffffffffu, st.l[c][j], 8);
+            st.l[c][j] += __shfl_xor_sync(0xffffffffu, st.l[c][j], 16);
+        }
+        if (g == 0) {
+            s_m[warp][2 * t] = st.m[c][0];
+            s_m[warp][2 * t + 1] = st.m[c][1];
+            s_l[warp][2 * t] = st.l[c][0];
+            s_l[warp][2 * t + 1] = st.l[c][1];
+        }
+        float obias[2] = {0.0f, 0.0f};  // int8: kInt8Bias * the weights summed over all tokens
+        if constexpr (G_::BIASED) {
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const float f = fast_exp2(s_m[w][hj] - mbase);
-        lsum += f * s_l[w][hj];
+            for (int j = 0; j < 2; ++j) {
+                float v = st.ps[c][j];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                obias[j] = kInt8Bias * v;
+            }
+        }
 #pragma unroll
-        for (int e = 0; e < DPT; ++e) acc[e] += f * s_o[w][hj][d0 + e];
-    }
-    const int h = h0 + hj;
-    if (nparts == 1 && !a.partials_only) {
-        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-        uint32_t packed[DPT / 2];
+        for (int mt = 0; mt < G_::MT; ++mt)
 #pragma unroll
-        for (int e = 0; e < DPT / 2; ++e) packed[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-        uint16_t *dst = a.out + ((int64_t)row * a.Hq + h) * D + d0;
-        if constexpr (DPT == 8)
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        else
-            *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-    } else {
-        const int64_t prow = ((int64_t)row * a.Hq + h) * a.max_parts + part;
-        float *dst = a.ws_acc + prow * D + d0;
+            for (int e = 0; e < 4; ++e)
+                s_o[warp][2 * t + (e & 1)][out_dim<G_::ELEM, D>(mt, g, e >> 1)] =
+                    (st.o[c][mt][e] - obias[e & 1]) * oscale;
+        __syncthreads();
+
+        // set c's partitions: those of its own limit (the last set's for decode)
+        const int nparts_c = ROWS ? max(1, (ctx - (nt - 1 - c) + a.part_tokens - 1) / a.part_tokens) : nparts;
+        if (hj < nh && part < nparts_c) {
+            float mmax = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < DPT; e += 4)
-            *reinterpret_cast<float4 *>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-        if ((tid & 15) == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(mmax, lsum);
+            for (int w = 0; w < kWarps; ++w) mmax = fmaxf(mmax, s_m[w][hj]);
+            const float mbase = mmax == -INFINITY ? 0.0f : mmax;
+            float acc[DPT];
+#pragma unroll
+            for (int e = 0; e < DPT; ++e) acc[e] = 0.0f;
+            float lsum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = fast_exp2(s_m[w][hj] - mbase);
+                lsum += f * s_l[w][hj];
+#pragma unroll
+                for (int e = 0; e < DPT; ++e) acc[e] += f * s_o[w][hj][d0 + e];
+            }
+            const int h = h0 + hj;
+            const int64_t row = row0 + c;
+            if (nparts_c == 1 && !a.partials_only) {
+                const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+                uint32_t packed[DPT / 2];
+#pragma unroll
+                for (int e = 0; e < DPT / 2; ++e) packed[e] = pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+                uint16_t *dst = a.out + (row * a.Hq + h) * D + d0;
+                if constexpr (DPT == 8)
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                else
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+            } else {
+                const int64_t prow = (row * a.Hq + h) * a.max_parts + part;
+                float *dst = a.ws_acc + prow * D + d0;
+#pragma unroll
+                for (int e = 0; e < DPT; e += 4)
+                    *reinterpret_cast<float4 *>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+                if ((tid & 15) == 0) *reinterpret_cast<float2 *>(a.ws_ml + prow * 2) = make_float2(mmax, lsum);
+            }
+        }
     }
 }
 
@@ -787,7 +866,7 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     // previous layer's merge): it launches while that kernel drains and waits for it
     // before reading
     dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
-    cudaError_t err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE, false>, grid, dim3(kThreads), 0, stream, a);
+    cudaError_t err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE, 0>, grid, dim3(kThreads), 0, stream, a);
     if (err != cudaSuccess || a.max_parts == 1 || a.partials_only) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((int64_t)a.S * a.Hq + 3) / 4));
@@ -809,16 +888,22 @@ cudaError_t launch_bs(const DecodeArgs &a, int bs, cudaStream_t stream) {
     return launch_typed<KV, D, 32, ONE_BYTE ? 32 : 16>(a, stream);
 }
 
-// Per-token mode: the new tokens of one partition are consecutive CTAs, so the CTAs
-// reading the same K/V tiles run side by side and all but the first hit L2.
+// Rows mode: NT new tokens per CTA, the token groups of one partition consecutive CTAs
+// (they read the same K/V tiles, so all but the first hit L2).  Several tokens per CTA
+// use 16-token tiles (registers for their column sets).
+template <typename KV, int D, int NT>
+cudaError_t launch_rows_nt(const DecodeArgs &a, int bs, cudaStream_t stream) {
+    constexpr int T32 = (sizeof(KV) == 1 && NT == 1) ? 32 : 16;
+    const dim3 grid((unsigned)(a.max_parts * ((a.Lq + NT - 1) / NT)), a.Hkv * a.head_chunks, a.S);
+    if (bs == 16)
+        return launch_dependent(paged_decode_kernel<KV, D, 16, 16, NT>, grid, dim3(kThreads), 0, stream, a);
+    return launch_dependent(paged_decode_kernel<KV, D, 32, T32, NT>, grid, dim3(kThreads), 0, stream, a);
+}
+
 template <typename KV, int D>
 cudaError_t launch_rows_bs(const DecodeArgs &a, int bs, cudaStream_t stream) {
-    constexpr bool ONE_BYTE = sizeof(KV) == 1;
-    const dim3 grid((unsigned)(a.max_parts * a.Lq), a.Hkv * a.head_chunks, a.S);
-    if (bs == 16)
-        return launch_dependent(paged_decode_kernel<KV, D, 16, 16, true>, grid, dim3(kThreads), 0, stream, a);
-    return launch_dependent(paged_decode_kernel<KV, D, 32, ONE_BYTE ? 32 : 16, true>, grid, dim3(kThreads), 0,
-                            stream, a);
+    if (a.rows_per_cta == 2) return launch_rows_nt<KV, D, 2>(a, bs, stream);
+    return launch_rows_nt<KV, D, 1>(a, bs, stream);
 }
 
 }  // namespace
@@ -832,10 +917,12 @@ cudaError_t launch_decode(const DecodeArgs &a, int D, int bs, int kv_dtype, cuda
     return D == 128 ? launch_bs<int8_t, 128>(a, bs, stream) : launch_bs<int8_t, 64>(a, bs, stream);
 }
 
+int decode_rows_per_cta(int max_query_len) { return max_query_len >= 2 ? 2 : 1; }
+
 cudaError_t launch_decode_rows(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
-    if (!a.query_start || a.Lq <= 0 || a.start_tokens || a.partials_only) return cudaErrorInvalidValue;
-    if (kv_dtype == PA_KV_BF16)
-        return D == 128 ? launch_rows_bs<uint16_t, 128>(a, bs, stream) : launch_rows_bs<uint16_t, 64>(a, bs, stream);
+    if (!a.query_start || a.Lq <= 0 || a.start_tokens || a.partials_only || kv_dtype == PA_KV_BF16 ||
+        (a.rows_per_cta != 1 && a.rows_per_cta != 2))
+        return cudaErrorInvalidValue;
     if (kv_dtype == PA_KV_FP8)
         return D == 128 ? launch_rows_bs<e4m3_t, 128>(a, bs, stream) : launch_rows_bs<e4m3_t, 64>(a, bs, stream);
     return D == 128 ? launch_rows_bs<int8_t, 128>(a, bs, stream) : launch_rows_bs<int8_t, 64>(a, bs, stream);

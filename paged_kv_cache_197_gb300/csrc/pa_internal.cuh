@@ -48,12 +48,13 @@ struct DecodeArgs {
     float scale_log2;  // softmax scale times log2(e)
     const int32_t *start_tokens;  // nullable [S]: tokens to skip (a shared prefix)
     int partials_only;            // write partial results even for a single partition
-    // Per-token mode (multi-token attention of narrow chunks): non-null [S + 1] row
-    // ranges of T query rows.  Grid x is partition x Lq + new token i; token i of
-    // sequence s (row query_start[s] + i) attends the first ctx - L + i + 1 tokens, and
-    // q, out and the partials [T][Hq][max_parts] are indexed by that row.
+    // Rows mode (multi-token attention of narrow chunks): non-null [S + 1] row ranges
+    // of T query rows.  A CTA takes rows_per_cta consecutive new tokens of a sequence
+    // (grid x is partition x token group); token i of sequence s (row query_start[s] +
+    // i) attends the first ctx - L + i + 1 tokens, and q, out and the partials
+    // [T][Hq][max_parts] are indexed by that row.
     const int32_t *query_start;
-    int T, Lq;
+    int T, Lq, rows_per_cta;
 };
 
 // Shared-prefix decode: groups of consecutive sequences whose block tables start with
@@ -97,12 +98,14 @@ int multi_cols_per_cta();
 cudaError_t launch_multi_token(const MultiArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream);
 // The log-sum-exp merge of multi-token partials (a programmatic dependent launch).
 cudaError_t launch_multi_merge(const MultiArgs &a, int D, int bs, cudaStream_t stream);
-// Whether a multi-token call runs on the decode kernel in per-token mode (one CTA per
-// new token, the tokens of a kv head side by side so they share K/V through L2);
-// plan and launch both follow it.
+// Whether a multi-token call runs on the decode kernel in rows mode (a CTA per one or
+// two new tokens, a kv head's token groups side by side so they share K/V through
+// L2); plan and launch both follow it.
 bool multi_per_token_eligible(int D, int kv_dtype, int G, int max_query_len);
-// The decode kernel alone in per-token mode (a programmatic dependent launch); the
-// caller launches the merge.
+// The decode kernel alone in rows mode, 8-bit caches (a programmatic dependent
+// launch); the caller launches the merge.  decode_rows_per_cta: the new tokens one
+// CTA takes for a call of max_query_len new tokens per sequence.
+int decode_rows_per_cta(int max_query_len);
 cudaError_t launch_decode_rows(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream);
 // Whether multi-token attention of this shape runs on the tcgen05 kernel (8-bit caches
 // after the dequantising pass below) rather than the mma.sync one; plan and launch both

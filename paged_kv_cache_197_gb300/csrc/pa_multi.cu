@@ -807,6 +807,7 @@ static cudaError_t launch_multi_per_token(const MultiArgs &m, int D, int bs, int
     a.query_start = m.query_start;
     a.T = m.T;
     a.Lq = m.max_query_len;
+    a.rows_per_cta = decode_rows_per_cta(m.max_query_len);
     cudaError_t err = launch_decode_rows(a, D, bs, kv_dtype, stream);
     if (err != cudaSuccess || m.max_parts == 1) return err;
     return launch_multi_merge(m, D, bs, stream);

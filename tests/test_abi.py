@@ -181,7 +181,7 @@ def test_multi_token_workspace_and_checks(lib):
     (last-wave fill) x (len / (len + 512)) over n balanced partitions of the longest
     context (ceil(ctx / n) rounded up to 64 tokens, 256..4096) with >= 2 waves (256 as
     the fallback).  Narrow chunks (at most 8 new tokens) of an 8-bit cache off the
-    tcgen05 path run on the decode kernel, one CTA per (new token, up to 8 query heads):
+    tcgen05 path run on the decode kernel, one CTA per (two new tokens, up to 8 query heads):
     the same rule with those CTAs as the units.  The workspace
     holds (D + 2) fp32 per query row, head and partition."""
     import math
@@ -192,7 +192,8 @@ def test_multi_token_workspace_and_checks(lib):
         G = Hq // Hkv
         cb = max(1, -(-max_q * G // 128))
         per_token = kv != pa.PA_KV_BF16 and not (D == 128 and max_q * G >= 64) and max_q <= 8
-        units = S * Hkv * -(-G // 8) * max_q if per_token else S * Hkv * cb
+        rows = 2 if max_q >= 2 else 1  # new tokens per decode CTA
+        units = S * Hkv * -(-G // 8) * -(-max_q // rows) if per_token else S * Hkv * cb
         ctx = max(max_ctx, 1)
         if D == 128 and max_q * G >= 64:
             if units < sms:
