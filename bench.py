@@ -84,6 +84,8 @@ NCU_TRAFFIC = {
     ("verify70b", "91323db2ddaade17"): 656797696 + 13285120,
     ("prefill8b", "91323db2ddaade17"): 83940352 + 3092992,
     ("verify70b_fp8", "5b771ca2846ad7f5"): 340236544 + 13805056,
+    # the decode kernel in rows mode (two new tokens per CTA), 2048-token partitions
+    ("verify70b_fp8", "80b6053b89d02567"): 339351296 + 5274368,
     # the tcgen05 kernel reading the dequantised bf16 pool (the pass before it reads the
     # 8-bit blocks once)
     ("prefill8b_fp8", "91323db2ddaade17"): 83939328 + 3236096,
@@ -121,13 +123,17 @@ def measured_peaks() -> dict:
 
 
 def multi_kernel_source(case) -> str:
-    """The source of the kernel a multi-token call runs: the tcgen05 kernel for head_dim
-    128 and at least 16 (token, head) columns per kv head with a bf16 cache, 64 with an
-    8-bit one (the library's own dispatch rule), else the mma.sync one."""
+    """The source of the kernel a multi-token call runs (the library's own dispatch
+    rule): the tcgen05 kernel for head_dim 128 and at least 16 (token, head) columns per
+    kv head with a bf16 cache, 64 with an 8-bit one; else, for an 8-bit cache and at
+    most 8 new tokens per sequence, the decode kernel in rows mode; else the mma.sync
+    one."""
     qs = case.query_start.cpu()
     max_q = int((qs[1:] - qs[:-1]).max())
     if case.D == 128 and max_q * (case.Hq // case.Hkv) >= (16 if case.kv_dtype == "bf16" else 64):
         return "pa_multi_tc.cu"
+    if case.kv_dtype != "bf16" and max_q <= 8:
+        return "pa_decode.cu"
     return "pa_multi.cu"
 
 
