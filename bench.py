@@ -70,6 +70,11 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
+    # column sets (decode: one) and the one-round-trip merge
+    ("gqa70b", "80b6053b89d02567"): 655763968 + 4635904,
+    ("mha13b", "80b6053b89d02567"): 1392701440 + 3301632,
+    ("int8", "80b6053b89d02567"): 3144270848 + 5432320,
+    ("fp8", "80b6053b89d02567"): 3144286464 + 5454592,
     # the decode kernel launched as a programmatic dependent (griddepcontrol.wait first)
     ("gqa70b", "b150daeb73620bab"): 655764736 + 5164800,
     ("mha13b", "b150daeb73620bab"): 1392701696 + 3443712,
