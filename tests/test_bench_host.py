@@ -23,9 +23,11 @@ def _multi(kv_dtype, D, Hq, Hkv, qlen):
     ("bf16", 128, 64, 8, 2, "pa_multi_tc.cu"),   # 16 columns per kv head
     ("bf16", 128, 16, 8, 4, "pa_multi.cu"),      # 8 columns
     ("bf16", 64, 64, 8, 16, "pa_multi.cu"),      # head_dim 64
-    ("fp8", 128, 64, 8, 4, "pa_multi.cu"),       # 32 columns: 8-bit needs 64
+    ("fp8", 128, 64, 8, 4, "pa_decode.cu"),      # 32 columns (8-bit tcgen05 needs 64): rows mode
     ("fp8", 128, 64, 8, 8, "pa_multi_tc.cu"),    # 64 columns
     ("int8", 128, 32, 8, 16, "pa_multi_tc.cu"),
+    ("int8", 64, 8, 2, 8, "pa_decode.cu"),       # head_dim 64, 8 new tokens: rows mode
+    ("int8", 64, 8, 2, 9, "pa_multi.cu"),        # 9 new tokens: the mma.sync kernel
 ])
 def test_multi_kernel_source_follows_dispatch(kv_dtype, D, Hq, Hkv, qlen, src):
     import bench
