@@ -94,6 +94,11 @@ NCU_TRAFFIC = {
     # the tcgen05 kernel reading the dequantised bf16 pool (the pass before it reads the
     # 8-bit blocks once)
     ("prefill8b_fp8", "91323db2ddaade17"): 83939328 + 3236096,
+    # current tcgen05 source; prefill8b_fp8: every kernel of the call (pool offsets,
+    # dequantising pass, tcgen05 kernel), each captured cold
+    ("verify70b", "10421af6d5a0669e"): 656793088 + 13301504,
+    ("prefill8b", "10421af6d5a0669e"): 83941376 + 3069696,
+    ("prefill8b_fp8", "10421af6d5a0669e"): (5632 + 0) + (34645760 + 5123072) + (83940352 + 76544),
 }
 
 
