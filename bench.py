@@ -70,6 +70,13 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
+    # fewer instructions per tile (fused score scale, unmasked full tiles, a vote for
+    # the value exponent)
+    ("gqa70b", "96b88d48f371f5fa"): 655776768 + 4920320,
+    ("mha13b", "96b88d48f371f5fa"): 1392700928 + 3355904,
+    ("int8", "96b88d48f371f5fa"): 3144285696 + 5479168,
+    ("fp8", "96b88d48f371f5fa"): 3144284416 + 5479168,
+    ("verify70b_fp8", "96b88d48f371f5fa"): 339326976 + 4881664,
     # column sets (decode: one) and the one-round-trip merge
     ("gqa70b", "80b6053b89d02567"): 655763968 + 4635904,
     ("mha13b", "80b6053b89d02567"): 1392701440 + 3301632,

@@ -343,18 +343,37 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE, NC> &st, Til
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         const int lim = R.nvalid - cut[c];
+        // one multiplier per (sub-tile, token row): the softmax scale, times the key
+        // scale for an 8-bit cache; int8: the bias comes off in the same fused step
+        float kk[G_::SUB][2], qk[G_::SUB][2][2];
+#pragma unroll
+        for (int s = 0; s < G_::SUB; ++s)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                kk[s][h] = G_::ELEM == 1 ? scale_log2[c] * ksc[s][h] : scale_log2[c];
+                if constexpr (G_::BIASED) {
+                    qk[s][h][0] = qb[c][0] * kk[s][h];
+                    qk[s][h][1] = qb[c][1] * kk[s][h];
+                }
+            }
+#pragma unroll
+        for (int s = 0; s < G_::SUB; ++s)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                x[c][s][e] = G_::BIASED ? fmaf(sc[c][s][e], kk[s][e >> 1], -qk[s][e >> 1][e & 1])
+                                        : sc[c][s][e] * kk[s][e >> 1];
+        if (lim < TILE) {  // a tile the set sees only in part (uniform across the warp)
+#pragma unroll
+            for (int s = 0; s < G_::SUB; ++s)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (16 * s + g + 8 * (e >> 1) >= lim) x[c][s][e] = -INFINITY;
+        }
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int s = 0; s < G_::SUB; ++s)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = 16 * s + g + 8 * (e >> 1);
-                float v = (G_::BIASED ? sc[c][s][e] - qb[c][e & 1] : sc[c][s][e]) * scale_log2[c];
-                if constexpr (G_::ELEM == 1) v *= ksc[s][e >> 1];
-                v = tok < lim ? v : -INFINITY;
-                x[c][s][e] = v;
-                mx[e & 1] = fmaxf(mx[e & 1], v);
-            }
+            for (int e = 0; e < 4; ++e) mx[e & 1] = fmaxf(mx[e & 1], x[c][s][e]);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
@@ -389,12 +408,15 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE, NC> &st, Til
     // ve the exponent of the largest value scale seen so far (O rescaled when it grows)
     float vmul = 1.0f;
     if constexpr (G_::ELEM == 1) {
-        float vmax = (int)(threadIdx.x & 31) < R.nvalid ? R.vs : 0.0f;
+        const float vl = (int)(threadIdx.x & 31) < R.nvalid ? R.vs : 0.0f;
+        // only a tile holding a value scale of a higher exponent raises ve (one vote
+        // instead of a reduction in the common case)
+        if (__any_sync(0xffffffffu, vl > 0.0f && exponent_above(vl) > st.ve)) {
+            float vmax = vl;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-        if (vmax > 0.0f) {
+            for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
             const int e = exponent_above(vmax);
-            if (e > st.ve) {
+            {
                 const float f = st.ve < -200 ? 0.0f : ldexpf(1.0f, st.ve - e);
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -440,9 +462,14 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE, NC> &st, Til
             for (int e = 0; e < 4; ++e) {
                 p[e] = fast_exp2(x[c][s][e] - base[c][e & 1]);
                 st.l[c][e & 1] += p[e];
-                if constexpr (G_::ELEM == 1) {
-                    const int tok = 16 * s + g + 8 * (e >> 1);
-                    p[e] = tok < lim ? p[e] * vsc[e >> 1] : 0.0f;
+                if constexpr (G_::ELEM == 1) p[e] *= vsc[e >> 1];
+            }
+            if constexpr (G_::ELEM == 1) {
+                // tokens the set does not see: a zero weight (their scales may be NaN)
+                if (lim < TILE) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (16 * s + g + 8 * (e >> 1) >= lim) p[e] = 0.0f;
                 }
             }
             if constexpr (G_::ELEM == 2) {
