@@ -70,6 +70,12 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
+    # + rescale slack of 2^8 and fp8 key words converted in one block
+    ("gqa70b", "834753d87ef8f64f"): 655777280 + 5179392,
+    ("mha13b", "834753d87ef8f64f"): 1392741632 + 3417856,
+    ("int8", "834753d87ef8f64f"): 3144293632 + 5563136,
+    ("fp8", "834753d87ef8f64f"): 3144498176 + 5451520,
+    ("verify70b_fp8", "834753d87ef8f64f"): 339325952 + 4805376,
     # fewer instructions per tile (fused score scale, unmasked full tiles, a vote for
     # the value exponent)
     ("gqa70b", "96b88d48f371f5fa"): 655776768 + 4920320,

@@ -47,6 +47,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxPartBlocks = 256;  // 4096-token partitions of 16-token blocks
 constexpr int kHeadsPerCta = 8;
 constexpr int kMergeInRegs = 16;  // partitions whose partial rows the merge loads at once
+constexpr float kRescaleLog2 = 8.0f;  // running-max slack before O is rescaled (log2 units)
 
 // ------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void ldg16(uint32_t *w, const void *p) {
@@ -157,8 +158,9 @@ __device__ __forceinline__ void k8x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &
     if constexpr (sizeof(KV) == 1 && !std::is_same<KV, e4m3_t>::value) {
         i8x4_to_f16(w, lo, hi);
     } else {
-        lo = e4m3x2_to_f16x2(w & 0xffffu);
-        hi = e4m3x2_to_f16x2(w >> 16);
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
     }
 }
 
@@ -383,7 +385,10 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE, NC> &st, Til
         float alpha[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const float mnew = fmaxf(st.m[c][j], mx[j]);
+            // the running max moves only when the tile's max exceeds it by more than
+            // kRescaleLog2 (weights then stay below 2^kRescaleLog2: fine in fp32, and in
+            // fp16 for the 8-bit products, whose weights carry value scales below 1)
+            const float mnew = mx[j] > st.m[c][j] + kRescaleLog2 ? mx[j] : st.m[c][j];
             base[c][j] = mnew == -INFINITY ? 0.0f : mnew;
             alpha[j] = fast_exp2(st.m[c][j] - base[c][j]);
             st.m[c][j] = mnew;
