@@ -338,7 +338,7 @@ constexpr int kShortOwnTokens = 1024;
 // partials per 128-token chunk, own-token partials per partition.
 struct PrefixPlan {
     DecodePlan own;
-    int PP, CB, MP;
+    int PP, CB, MP, chunk;
     size_t start_off, group_off, pacc_off, pml_off, acc_off, ml_off, bytes;
 };
 
@@ -357,7 +357,8 @@ static PrefixPlan plan_prefix(int S, int Hq, int Hkv, int D, int bs, int kv_dtyp
     if (own_len <= kShortOwnTokens) p.own.part_tokens = own_len;
     p.own.part_tokens = (int)align_up((size_t)p.own.part_tokens, 64);  // whole tiles and blocks
     p.MP = std::max(1, (max_context_len + p.own.part_tokens - 1) / p.own.part_tokens);
-    const int chunk = prefix_chunk_tokens();
+    const int chunk = prefix_chunk_tokens(kv_dtype, D);
+    p.chunk = chunk;
     p.PP = (max_prefix_len + chunk - 1) / chunk;
     p.CB = std::max(1, (max_group_size * (Hq / Hkv) + prefix_cols_per_cta() - 1) / prefix_cols_per_cta());
     const size_t rows_pre = (size_t)S * Hq * p.PP, rows_own = (size_t)S * Hq * p.MP;
@@ -472,6 +473,7 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
     p.pml = (float *)(ws + plan.pml_off);
     p.PP = plan.PP;
     p.CB = plan.CB;
+    p.chunk = plan.chunk;
     launch_decode_shared_prefix(a, p, D, bs, kv_dtype, (cudaStream_t)stream);
     return check_launch(fn);
 }

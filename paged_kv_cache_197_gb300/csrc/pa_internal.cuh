@@ -69,9 +69,12 @@ struct PrefixArgs {
     float *pml;                   // [S][Hq][PP][2]
     int PP;                       // prefix chunks of the longest prefix
     int CB;                       // blocks of 128 query columns per kv head
+    int chunk;                    // prefix tokens per partial (prefix_chunk_tokens)
 };
 
-int prefix_chunk_tokens();
+// Prefix tokens per grouped partial: 256 on the tcgen05 path (bf16, head_dim 128),
+// else 128 (the mma.sync grouped kernel stages one chunk in shared memory).
+int prefix_chunk_tokens(int kv_dtype, int D);
 int prefix_cols_per_cta();
 cudaError_t launch_decode_shared_prefix(const DecodeArgs &a, const PrefixArgs &p, int D, int bs, int kv_dtype,
                                         cudaStream_t stream);
@@ -92,6 +95,14 @@ struct MultiArgs {
     int part_tokens, max_parts;    // context partitions (multiple of 64 tokens)
     int max_context_len, max_query_len;
     float scale_log2;
+    // Group mode (the tcgen05 kernel only; shared-prefix decode): non-null [S] prefix
+    // lengths of S groups whose members are the query rows query_start[g] ..
+    // query_start[g + 1] - 1 of the decode queries [T][Hq][D]; every member attends
+    // all of its group's prefix through the first member's block table, no causal
+    // mask, and every column leaves a partial (no direct output).  seq_group [T]: a
+    // member whose entry is not g is left out.
+    const int32_t *group_prefix;
+    const int32_t *seq_group;
 };
 
 int multi_cols_per_cta();
@@ -112,6 +123,8 @@ cudaError_t launch_decode_rows(const DecodeArgs &a, int D, int bs, int kv_dtype,
 // follow it.
 bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len);
 cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream);  // bf16 caches
+// The tcgen05 kernel in group mode (the caller merges the partials).
+cudaError_t launch_multi_tc_groups(const MultiArgs &a, int bs, cudaStream_t stream);
 // 8-bit caches, prefill-shaped calls: the attended blocks dequantised into a bf16 pool
 // of `cap` blocks, sequences packed back to back (offsets off[S + 1]), and the table
 // [S][Mq] of pool slots, all in the workspace.

@@ -257,6 +257,7 @@ struct TcShared {
     uint64_t kfree[kTcStages], vfree[kTcStages];  // stage consumed by S_t / by P V_t
     uint64_t sfull, sfree;        // S_t in tensor memory / read by all 128 rows
     uint64_t pfull, odone;        // P_t written by all rows / P V_t done
+    uint64_t qready;              // Q in tensor memory (all 128 rows)
     uint64_t drain;               // every product issued so far is done (abort path only)
     uint32_t taddr;
     int abort;
@@ -282,27 +283,42 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     const int s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- the sequence, the CTA's columns and its token range (as in pa_multi.cu)
-    int ctx = a.context_lens[s];
+    // ---- the sequence, the CTA's columns and its token range (as in pa_multi.cu); in
+    // group mode blockIdx.z is a group, its members the rows and its prefix the context
+    const bool grouped = a.group_prefix != nullptr;
     const int lim_ctx = min(a.M * BS, a.max_context_len);
-    const bool report = part == 0 && blockIdx.y == 0 && tid == 0;
-    if (ctx < 0 || ctx > lim_ctx) {
-        if (report) tc_raise(a.err_flag, PA_FLAG_CONTEXT_OUT_OF_RANGE);
-        ctx = ctx < 0 ? 0 : lim_ctx;
-    }
+    const bool report = part == 0 && blockIdx.y == 0 && tid == 0 && !grouped;
     const int r0 = a.query_start[s], r1 = a.query_start[s + 1];
     const int L = r1 - r0;
-    if (!(r0 >= 0 && r1 <= a.T && L >= 0 && L <= ctx && L <= a.max_query_len)) {
-        if (report) tc_raise(a.err_flag, PA_FLAG_QUERY_OUT_OF_RANGE);
-        return;
+    int ctx;
+    if (grouped) {
+        // groups the setup pass rejected (their first member is not in them) and
+        // prefixes past the planned maximum have nothing to attend here
+        ctx = a.group_prefix[s];
+        if (!(r0 >= 0 && r1 <= a.T && L >= 1 && L <= a.max_query_len && ctx >= 0 && ctx <= lim_ctx &&
+              a.seq_group[r0] == s))
+            return;
+    } else {
+        ctx = a.context_lens[s];
+        if (ctx < 0 || ctx > lim_ctx) {
+            if (report) tc_raise(a.err_flag, PA_FLAG_CONTEXT_OUT_OF_RANGE);
+            ctx = ctx < 0 ? 0 : lim_ctx;
+        }
+        if (!(r0 >= 0 && r1 <= a.T && L >= 0 && L <= ctx && L <= a.max_query_len)) {
+            if (report) tc_raise(a.err_flag, PA_FLAG_QUERY_OUT_OF_RANGE);
+            return;
+        }
     }
     const int qbase = ctx - L;
     const int ncols = L * a.G;
     const int col0 = cb * kTcRows;
     if (col0 >= ncols) return;
+    const int trow = grouped ? r0 : s;  // the block table read (a group: its first member's)
     auto ctok = [&](int c) { return a.g_shift >= 0 ? c >> a.g_shift : c / a.G; };
     auto chead = [&](int c) { return a.g_shift >= 0 ? c & (a.G - 1) : c % a.G; };
-    const int cta_lim = qbase + ctok(min(ncols, col0 + kTcRows) - 1);
+    // last token column c sees: its own position, or the whole prefix of a group
+    auto col_lim = [&](int c) { return grouped ? ctx - 1 : qbase + ctok(c); };
+    const int cta_lim = col_lim(min(ncols, col0 + kTcRows) - 1);
     const int tok_begin = part * a.part_tokens;
     const int tok_end = min(tok_begin + a.part_tokens, cta_lim + 1);
     if (tok_begin >= tok_end) return;
@@ -313,11 +329,14 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
     // ---- rows: thread tid < 128 owns column col0 + tid
     const bool row_thread = warp < kTcSoftmaxWarps;
     const int c = col0 + tid;
-    const bool has = row_thread && c < ncols;
-    const int lim = has ? qbase + ctok(c) : -1;  // last visible token
-    const int lim_p = min(lim, tok_end - 1);     // ... inside this partition
+    const bool col = row_thread && c < ncols;  // a real (token or member, head) column
     int64_t pair = 0;
-    if (has) pair = (int64_t)(r0 + ctok(c)) * a.Hq + kvh * a.G + chead(c);
+    if (col) pair = (int64_t)(r0 + ctok(c)) * a.Hq + kvh * a.G + chead(c);
+    // a group's member left out by the setup pass computes (its query row exists) but
+    // writes nothing
+    const bool has = col && (!grouped || a.seq_group[r0 + ctok(c)] == s);
+    const int lim = has ? col_lim(c) : -1;  // last visible token
+    const int lim_p = min(lim, tok_end - 1);     // ... inside this partition
     if (tid == 0) {
 #pragma unroll
         for (int i = 0; i < kTcStages; ++i) {
@@ -329,6 +348,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         mbar_init(tc_smem(&sh.sfull));
         mbar_init_n(tc_smem(&sh.sfree), kTcRows);
         mbar_init_n(tc_smem(&sh.pfull), kTcRows);
+        mbar_init_n(tc_smem(&sh.qready), kTcRows);
         mbar_init(tc_smem(&sh.odone));
         mbar_init(tc_smem(&sh.drain));
         sh.abort = 0;
@@ -353,7 +373,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                if (has) x = __ldg(src + 8 * h + i);
+                if (col) x = __ldg(src + 8 * h + i);
                 w[4 * i] = __uint_as_float(x.x);
                 w[4 * i + 1] = __uint_as_float(x.y);
                 w[4 * i + 2] = __uint_as_float(x.z);
@@ -362,10 +382,11 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + kTmemQ + 32 * h, w);
         }
         tmem_wait_st();
+        // the product warp waits for this before the first S; the copy warps start
+        // fetching K and V meanwhile
+        tc_fence_before();
+        mbar_arrive(tc_smem(&sh.qready));
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
 
     if (warp == 4 || warp == 5) {
         // ---- copies: K (warp 4) or V (warp 5) tiles into their three stages; the whole
@@ -383,7 +404,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             int y = oob_row;
             const int idx = t * (kTcTile / BS) + lane;
             if (lane < kTcTile / BS && idx < nblk) {
-                const int b = __ldg(a.block_tables + (int64_t)s * a.M + blk0 + idx);
+                const int b = __ldg(a.block_tables + (int64_t)trow * a.M + blk0 + idx);
                 if (b >= 0 && b < a.N)
                     y = (b * a.Hkv + kvh) * BS;
                 else if (is_k && cb == 0)
@@ -442,7 +463,11 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             __syncwarp();
             return true;
         };
-        bool ok = issue_s(0);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(tc_smem(&sh.qready), 0));
+        if (ok) {
+            tc_fence_after();
+            ok = issue_s(0);
+        }
 #pragma unroll 1
         for (int j = 0; ok && j < ntile; ++j) {
             const int st = j % kTcStages;
@@ -580,7 +605,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             // ---- epilogue: this thread's output row (the tensor-memory loads are
             // warp-wide; rows with nothing to write discard them)
             const bool write = has && tok_begin <= lim;
-            const bool finished = lim < a.part_tokens;
+            const bool finished = lim < a.part_tokens && !grouped;
             const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
             const int64_t prow = pair * a.max_parts + part;
 #pragma unroll 1
@@ -649,7 +674,7 @@ bool pool_map(CUtensorMap *map, const void *pool, int rows, int bs) {
 }
 
 template <int BS>
-cudaError_t launch_tc_typed(const MultiArgs &a, cudaStream_t stream) {
+cudaError_t launch_tc_typed(const MultiArgs &a, bool merge, cudaStream_t stream) {
     CUtensorMap kmap, vmap;
     if ((int64_t)a.N * a.Hkv * BS >= (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // TMA row coordinates
     const int rows = a.N * a.Hkv * BS;
@@ -666,7 +691,7 @@ cudaError_t launch_tc_typed(const MultiArgs &a, cudaStream_t stream) {
     dim3 grid(a.max_parts, a.Hkv * a.CB, a.S);
     multi_tc_kernel<BS><<<grid, kTcAllThreads, kTcSmem, stream>>>(a, kmap, vmap);
     const cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess || a.max_parts == 1) return err;
+    if (err != cudaSuccess || a.max_parts == 1 || !merge) return err;
     return launch_multi_merge(a, kTcD, BS, stream);
 }
 
@@ -793,7 +818,12 @@ cudaError_t launch_dequant_blocks(const MultiArgs &a, int bs, int kv_dtype, int 
 }
 
 cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream) {
-    return bs == 16 ? launch_tc_typed<16>(a, stream) : launch_tc_typed<32>(a, stream);
+    return bs == 16 ? launch_tc_typed<16>(a, true, stream) : launch_tc_typed<32>(a, true, stream);
+}
+
+cudaError_t launch_multi_tc_groups(const MultiArgs &a, int bs, cudaStream_t stream) {
+    if (!a.group_prefix || !a.seq_group || !a.ws_acc || !a.ws_ml) return cudaErrorInvalidValue;
+    return bs == 16 ? launch_tc_typed<16>(a, false, stream) : launch_tc_typed<32>(a, false, stream);
 }
 
 bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len) {

@@ -29,6 +29,7 @@
 #include <atomic>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "pa_internal.cuh"
@@ -39,7 +40,8 @@ namespace {
 
 using namespace tiled;
 
-constexpr int kPrefixChunk = 128;   // prefix tokens per CTA
+constexpr int kPrefixChunk = 128;   // prefix tokens per CTA of the grouped kernel
+constexpr int kPrefixChunkTc = 256;  // prefix tokens per CTA on the tcgen05 path
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kColsPerWarp = 16;    // two mma n-tiles of 8 query columns
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(128) merge_prefix_kernel(const __grid_constant
     const int ctx = checked_ctx(a, s, BS);
     const int start = min(p.seq_start[s], ctx);
     const int nown = max(1, (ctx - start + a.part_tokens - 1) / a.part_tokens);
-    const int npre = p.seq_group[s] >= 0 ? (start + kPrefixChunk - 1) / kPrefixChunk : 0;
+    const int npre = p.seq_group[s] >= 0 ? (start + p.chunk - 1) / p.chunk : 0;
     const int64_t own0 = pair * a.max_parts, pre0 = pair * p.PP;
     const int n = npre + nown;
     auto row_of = [&](int i, const float *&acc, const float *&ml) {
@@ -554,6 +556,41 @@ cudaError_t side_stream(int dev, cudaStream_t caller, SideStream *&out) {
     return cudaSuccess;
 }
 
+// bf16 caches with head_dim 128: each group's prefix on the tcgen05 kernel in group mode
+// (the members' (query head) columns as its rows, 128-token partitions as its chunks),
+// leaving the same partials as the grouped kernel.
+template <int BS>
+cudaError_t launch_prefix_tc(const DecodeArgs &a, const PrefixArgs &p, cudaStream_t stream) {
+    MultiArgs m{};
+    m.out = a.out;
+    m.q = a.q;
+    m.k_cache = a.k_cache;
+    m.v_cache = a.v_cache;
+    m.block_tables = a.block_tables;
+    m.context_lens = a.context_lens;
+    m.query_start = p.group_start;
+    m.ws_acc = p.pacc;
+    m.ws_ml = p.pml;
+    m.err_flag = a.err_flag;
+    m.M = a.M;
+    m.S = p.n_groups;
+    m.T = a.S;
+    m.Hq = a.Hq;
+    m.Hkv = a.Hkv;
+    m.G = a.G;
+    m.N = a.N;
+    m.g_shift = (a.G & (a.G - 1)) == 0 ? __builtin_ctz((unsigned)a.G) : -1;
+    m.CB = p.CB;
+    m.part_tokens = p.chunk;
+    m.max_parts = p.PP;
+    m.max_context_len = p.max_prefix;
+    m.max_query_len = p.max_group_size;
+    m.scale_log2 = a.scale_log2;
+    m.group_prefix = p.group_prefix;
+    m.seq_group = p.seq_group;
+    return launch_multi_tc_groups(m, BS, stream);
+}
+
 template <typename KV, int D, int BS>
 cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, int kv_dtype, cudaStream_t stream) {
     constexpr int SMEM = 2 * kPrefixChunk * (D * 2 + 16);
@@ -574,9 +611,18 @@ cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, int kv
     if (grouped) {
         if ((err = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return err;
         if ((err = cudaStreamWaitEvent(ss->stream, ss->fork, 0)) != cudaSuccess) return err;
-        dim3 grid(p.PP, a.Hkv * p.CB, p.n_groups);
-        grouped_prefix_kernel<KV, D, BS><<<grid, kThreads, SMEM, ss->stream>>>(a, p);
-        if ((err = cudaEventRecord(ss->join, ss->stream)) != cudaSuccess) return err;
+        if constexpr (std::is_same<KV, uint16_t>::value && D == 128) {
+            err = launch_prefix_tc<BS>(a, p, ss->stream);
+        } else if (p.chunk != kPrefixChunk) {
+            err = cudaErrorInvalidValue;
+        } else {
+            dim3 grid(p.PP, a.Hkv * p.CB, p.n_groups);
+            grouped_prefix_kernel<KV, D, BS><<<grid, kThreads, SMEM, ss->stream>>>(a, p);
+            err = cudaGetLastError();
+        }
+        const cudaError_t e = cudaEventRecord(ss->join, ss->stream);  // recorded even on error
+        if (err == cudaSuccess) err = e;
+        if (err != cudaSuccess) return err;
     }
     err = launch_decode(a, D, BS, kv_dtype, stream);  // own tokens, partials only
     if (grouped) {
@@ -590,7 +636,12 @@ cudaError_t launch_prefix_typed(const DecodeArgs &a, const PrefixArgs &p, int kv
 
 }  // namespace
 
-int prefix_chunk_tokens() { return kPrefixChunk; }
+int prefix_chunk_tokens(int kv_dtype, int D) {
+    // the tcgen05 path's CTA pays a longer prologue (tensor memory, barriers, Q staged in
+    // tensor memory) than the grouped kernel's: measured on the shared-prompt workload,
+    // 256-token partials 42.5 us per call against 44.2 with 128 and 44.7 with 512
+    return kv_dtype == PA_KV_BF16 && D == 128 ? kPrefixChunkTc : kPrefixChunk;
+}
 int prefix_cols_per_cta() { return kColsPerCta; }
 
 template <typename KV>

@@ -118,7 +118,8 @@ def test_workspace_size(lib):
 
 def test_shared_prefix_workspace_and_checks(lib):
     """Workspace of the prefix-aware decode: S int32 group ids and S start offsets, then
-    (D + 2) fp32 per query head and 128-token prefix chunk, then (D + 2) fp32 per query
+    (D + 2) fp32 per query head and prefix chunk (256 tokens for a bf16 cache with
+    head_dim 128, the tcgen05 path; else 128), then (D + 2) fp32 per query
     head and own-token partition; partitions sized for max_context_len - max_prefix_len
     (one partition when that is at most 1024 tokens; rounded up to 64 tokens), counted
     over max_context_len; each region 256-byte aligned.  Host checks refuse what the kernels do not take."""
@@ -133,7 +134,7 @@ def test_shared_prefix_workspace_and_checks(lib):
         pt = own if own <= 1024 else part_tokens(units, own)
         pt = -(-pt // 64) * 64
         MP = max(1, -(-max_ctx // pt))
-        PP = -(-max_prefix // 128)
+        PP = -(-max_prefix // (256 if D == 128 else 128))
         pre, own = S * Hq * PP, S * Hq * MP
         size = up(S * 4) + S * 4
         size = up(size) + pre * D * 4
@@ -147,7 +148,9 @@ def test_shared_prefix_workspace_and_checks(lib):
         **{**dict(S=4, Hq=8, Hkv=2, D=128, bs=16, kv_dtype=0, max_context_len=512,
                   max_group_size=4, max_prefix_len=256), **k})
     assert ws() > 0
-    assert ws(kv_dtype=pa.PA_KV_INT8) == ws()
+    assert ws(kv_dtype=pa.PA_KV_INT8) == ws(kv_dtype=pa.PA_KV_FP8)
+    assert ws(kv_dtype=pa.PA_KV_INT8, max_prefix_len=256) > ws(max_prefix_len=256)  # 128-token chunks
+    assert ws(kv_dtype=pa.PA_KV_INT8, D=64) == ws(D=64)
     assert ws(kv_dtype=9) == 0                  # no such cache type
     assert ws(max_prefix_len=200) == 0          # not whole blocks
     assert ws(max_prefix_len=1024) == 0         # longer than any context

@@ -73,12 +73,13 @@ def test_mixed_groups(oracle, kv_dtype):
     _run(case, oracle, groups)
 
 
-def test_groups_wider_than_one_cta(oracle):
+@pytest.mark.parametrize("D", [64, 128])
+def test_groups_wider_than_one_cta(oracle, D):
     """A group with more (member, head) columns (160) than one CTA takes (128), beside a
-    smaller one."""
+    smaller one (head_dim 128: the tcgen05 kernel in group mode, two column blocks)."""
     lens = [700 + 13 * i for i in range(40)] + [900 + 7 * i for i in range(16)]
-    case = workloads.build_case("pfx-wide", S=len(lens), Hq=64, Hkv=16, D=64, bs=32,
-                                context_lens=lens, seed=12)
+    case = workloads.build_case(f"pfx-wide-{D}", S=len(lens), Hq=64, Hkv=16, D=D, bs=32,
+                                context_lens=lens, seed=12 + D)
     _share(case, list(range(40)), 512)
     _share(case, list(range(40, 56)), 640)
     _run(case, oracle, ([0, 40, 56], [512, 640], 40, 640))
