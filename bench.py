@@ -107,6 +107,10 @@ NCU_TRAFFIC = {
     # the tcgen05 kernel reading the dequantised bf16 pool (the pass before it reads the
     # 8-bit blocks once)
     ("prefill8b_fp8", "91323db2ddaade17"): 83939328 + 3236096,
+    # P V issued by row thread 0; prefill8b_fp8: every kernel of the call
+    ("verify70b", "491c378341fcbbee"): 656803584 + 13247744,
+    ("prefill8b", "491c378341fcbbee"): 83943680 + 3076096,
+    ("prefill8b_fp8", "491c378341fcbbee"): (5376 + 0) + (34652672 + 5374720) + (83958016 + 54272),
     # current tcgen05 source; prefill8b_fp8: every kernel of the call (pool offsets,
     # dequantising pass, tcgen05 kernel), each captured cold
     ("verify70b", "10421af6d5a0669e"): 656793088 + 13301504,

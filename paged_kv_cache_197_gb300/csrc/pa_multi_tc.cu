@@ -17,9 +17,11 @@
 //     the partition are copied from past the end of the pool, i.e. as zeros);
 //   * warp 6 issues, from one lane, S_t = Q K_t^T (M 128 columns x N 64 tokens,
 //     K 128 dims; Q from tensor memory, where the row threads put it, K from the
-//     staged tile) and O += P_t V_t (N 128 dims, K 64 tokens; P from shared memory, V
-//     read as an MN-major operand from the same staged tile), and commits each to the
-//     barriers that free the stages and wake the row warps;
+//     staged tile) and commits it to the barriers that free the K stage and wake the
+//     row warps; row thread 0 issues O += P_t V_t (N 128 dims, K 64 tokens; P from
+//     shared memory, V read as an MN-major operand from the same staged tile) as soon
+//     as every row's P is in (no hand-off through warp 6, whose next S may be waiting
+//     for its K tile) and commits it to the barriers that free the V stage and P;
 //   * warps 0-3 own one row each (tensor-memory lane = thread): they read the row's
 //     scores, mask tokens past its position, keep a running max (raised only when a
 //     tile's max exceeds it by more than 2^8 in the exp2 domain; O is then rescaled in
@@ -259,6 +261,7 @@ struct TcShared {
     uint64_t pfull, odone;        // P_t written by all rows / P V_t done
     uint64_t qready;              // Q in tensor memory (all 128 rows)
     uint64_t drain;               // every product issued so far is done (abort path only)
+    uint64_t drain_rows;          // the same for the P V products row thread 0 issued
     uint32_t taddr;
     int abort;
 };
@@ -351,6 +354,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         mbar_init_n(tc_smem(&sh.qready), kTcRows);
         mbar_init(tc_smem(&sh.odone));
         mbar_init(tc_smem(&sh.drain));
+        mbar_init(tc_smem(&sh.drain_rows));
         sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -441,7 +445,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             }
         }
     } else if (warp == 6) {
-        // ---- tensor-core products in the order S_0, S_1, PV_0, S_2, PV_1, ...: the
+        // ---- the score products S_0, S_1, ... (P V is issued by row thread 0): the
         // whole warp waits, lane 0 issues
         auto issue_s = [&](int t) -> bool {
             const int st = t % kTcStages;
@@ -469,25 +473,12 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             ok = issue_s(0);
         }
 #pragma unroll 1
-        for (int j = 0; ok && j < ntile; ++j) {
-            const int st = j % kTcStages;
-            if (j + 1 < ntile) ok = issue_s(j + 1);
-            if (ok) ok = mbar_wait(tc_smem(&sh.pfull), j & 1) && mbar_wait(tc_smem(&sh.vfull[st]), (j / kTcStages) & 1);
+        for (int t = 1; ok && t < ntile; ++t) {
+            ok = issue_s(t);
             if (!__all_sync(0xffffffffu, ok && sh.abort == 0)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t vb = tc_smem(base + kOffV + st * kTcTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < kTcTile / 16; ++kk)
-                    umma(t_o, sw128_desc(p_s + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024),
-                         sw128_desc(vb + kk * 2048, kTcAtom, 1024), bf16_idesc(128, 128, 1), (j > 0 || kk > 0));
-                umma_commit(tc_smem(&sh.odone));
-                umma_commit(tc_smem(&sh.vfree[st]));
-            }
-            __syncwarp();
         }
         if (!ok) {
             // stopping early: let every product already issued finish before tensor
@@ -504,6 +495,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
+        int pv_issued = 0;  // row thread 0: P V products issued
 #pragma unroll 1
         for (int j = 0; j < ntile; ++j) {
             const int st = j % kTcStages;
@@ -596,9 +588,34 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P visible to the tensor core
             tc_fence_before();
             mbar_arrive(tc_smem(&sh.pfull));
+            if (tid == 0) {
+                // P V_j from here: once every row's P is in and V_j has landed
+                const bool pv_ok = mbar_wait(tc_smem(&sh.pfull), j & 1) &&
+                                   mbar_wait(tc_smem(&sh.vfull[st]), (j / kTcStages) & 1);
+                if (pv_ok) {
+                    tc_fence_after();
+                    const uint32_t vb = tc_smem(base + kOffV + st * kTcTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTcTile / 16; ++kk)
+                        umma(t_o, sw128_desc(p_s + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024),
+                             sw128_desc(vb + kk * 2048, kTcAtom, 1024), bf16_idesc(128, 128, 1), (j > 0 || kk > 0));
+                    umma_commit(tc_smem(&sh.odone));
+                    umma_commit(tc_smem(&sh.vfree[st]));
+                    ++pv_issued;
+                } else {
+                    atomicOr(&sh.abort, 1);
+                }
+            }
+            __syncwarp();
         }
         if (ok) ok = mbar_wait(tc_smem(&sh.odone), (ntile - 1) & 1);
         if (!ok) atomicOr(&sh.abort, 1);
+        if (tid == 0 && pv_issued > 0 && !ok) {
+            // stopping early: the products this thread issued finish before tensor memory
+            // is released (bounded wait)
+            umma_commit(tc_smem(&sh.drain_rows));
+            mbar_wait(tc_smem(&sh.drain_rows), 0);
+        }
         tc_fence_after();
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (__all_sync(0xffffffffu, ok)) {
