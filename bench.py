@@ -70,6 +70,12 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
+    # split bf16 / int8 contexts on the single-buffered kernel, three CTAs per SM
+    ("gqa70b", "095e29f621331af4"): 655772416 + 4880640,
+    ("mha13b", "095e29f621331af4"): 1392701440 + 3302144,
+    ("int8", "095e29f621331af4"): 3144270848 + 5010688,
+    ("fp8", "095e29f621331af4"): 3144264192 + 5480192,
+    ("verify70b_fp8", "095e29f621331af4"): 339326464 + 4800768,
     # + rescale slack of 2^8 and fp8 key words converted in one block
     ("gqa70b", "834753d87ef8f64f"): 655777280 + 5179392,
     ("mha13b", "834753d87ef8f64f"): 1392741632 + 3417856,

@@ -526,9 +526,11 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE, NC> &st, Til
 // NT == 0: decode, one query row per sequence (grid x = partition).  NT >= 1: rows
 // mode of a multi-token call, NT consecutive new tokens of a sequence per CTA (grid x =
 // partition x token groups), each token a column set with its own causal limit.
-template <typename KV, int D, int BS, int TILE, int NT>
-__global__ void __launch_bounds__(kThreads)
-paged_decode_kernel(const DecodeArgs a) {
+// SINGLE (decode only): one tile register set per warp instead of two (the next
+// tile is not prefetched), 150-165 registers, three CTAs per SM: twelve warps per SM
+// keep loads in flight where eight double-buffered ones did.
+template <typename KV, int D, int BS, int TILE, int NT, bool SINGLE>
+__device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     using G_ = Geo<KV, D, TILE>;
     constexpr bool ROWS = NT > 0;
     constexpr int NC = ROWS ? NT : 1;
@@ -666,19 +668,27 @@ paged_decode_kernel(const DecodeArgs a) {
     st.ve = -1000;  // no value scale seen yet
 
     const int ntiles = (tok_end - tok_begin + TILE - 1) / TILE;
-    Tile<G_> A, B;
-    int i = warp;
-    if (i < ntiles) load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i, kvh, g, t, lane);
-    while (i < ntiles) {
-        if (i + kWarps < ntiles)
-            load_tile<KV, D, BS, TILE>(B, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE, NC>(st, A, qw, qb, scale_log2, cut, g, t);
-        i += kWarps;
-        if (i >= ntiles) break;
-        if (i + kWarps < ntiles)
-            load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
-        consume_tile<KV, D, TILE, NC>(st, B, qw, qb, scale_log2, cut, g, t);
-        i += kWarps;
+    if constexpr (SINGLE) {
+        Tile<G_> A;
+        for (int i = warp; i < ntiles; i += kWarps) {
+            load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i, kvh, g, t, lane);
+            consume_tile<KV, D, TILE, NC>(st, A, qw, qb, scale_log2, cut, g, t);
+        }
+    } else {
+        Tile<G_> A, B;
+        int i = warp;
+        if (i < ntiles) load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i, kvh, g, t, lane);
+        while (i < ntiles) {
+            if (i + kWarps < ntiles)
+                load_tile<KV, D, BS, TILE>(B, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
+            consume_tile<KV, D, TILE, NC>(st, A, qw, qb, scale_log2, cut, g, t);
+            i += kWarps;
+            if (i >= ntiles) break;
+            if (i + kWarps < ntiles)
+                load_tile<KV, D, BS, TILE>(A, a, s_blk, blk_begin, tok_begin, tok_end, i + kWarps, kvh, g, t, lane);
+            consume_tile<KV, D, TILE, NC>(st, B, qw, qb, scale_log2, cut, g, t);
+            i += kWarps;
+        }
     }
 
     // the dependent merge grid may launch once every CTA got here (it still waits for
@@ -765,6 +775,16 @@ paged_decode_kernel(const DecodeArgs a) {
             }
         }
     }
+}
+
+template <typename KV, int D, int BS, int TILE, int NT>
+__global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs a) {
+    decode_body<KV, D, BS, TILE, NT, false>(a);
+}
+
+template <typename KV, int D, int BS, int TILE>
+__global__ void __launch_bounds__(kThreads, 3) paged_decode_single_kernel(const DecodeArgs a) {
+    decode_body<KV, D, BS, TILE, 0, true>(a);
 }
 
 // Log-sum-exp merge of the partitions of each (sequence, query head):
@@ -898,7 +918,21 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     // previous layer's merge): it launches while that kernel drains and waits for it
     // before reading
     dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
-    cudaError_t err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE, 0>, grid, dim3(kThreads), 0, stream, a);
+    // Split contexts of bf16 and int8 caches take the single-buffered kernel at three
+    // CTAs per SM; unsplit contexts, fp8 caches and the own tokens of a shared-prefix
+    // call the double-buffered one at two.  Measured on GB300 (decode call, us, double
+    // -> single): 70B-shaped bf16 114.1 -> 111.8, int8 522.2 -> 513.7; fp8 513.0 ->
+    // 527.2, 13B-shaped bf16 (no split) 215.8 -> 220.4, shared-prompt call 42.2 -> 43.5.
+    constexpr bool kSingleOk = !std::is_same<KV, e4m3_t>::value;
+    cudaError_t err;
+    if constexpr (kSingleOk) {
+        if (a.max_parts > 1 && !a.start_tokens)
+            err = launch_dependent(paged_decode_single_kernel<KV, D, BS, TILE>, grid, dim3(kThreads), 0, stream, a);
+        else
+            err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE, 0>, grid, dim3(kThreads), 0, stream, a);
+    } else {
+        err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE, 0>, grid, dim3(kThreads), 0, stream, a);
+    }
     if (err != cudaSuccess || a.max_parts == 1 || a.partials_only) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(((int64_t)a.S * a.Hq + 3) / 4));
