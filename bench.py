@@ -70,6 +70,12 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
+    # the single-buffered kernel with its own partition plan (70B-shaped: 8 x 1024)
+    ("gqa70b", "0df180f3524b8e7f"): 655757056 + 4864000,
+    ("mha13b", "0df180f3524b8e7f"): 1392701952 + 3723008,
+    ("int8", "0df180f3524b8e7f"): 3144269312 + 5220096,
+    ("fp8", "0df180f3524b8e7f"): 3144578304 + 5466368,
+    ("verify70b_fp8", "0df180f3524b8e7f"): 339324672 + 4783872,
     # split bf16 / int8 contexts on the single-buffered kernel, three CTAs per SM
     ("gqa70b", "095e29f621331af4"): 655772416 + 4880640,
     ("mha13b", "095e29f621331af4"): 1392701440 + 3302144,

@@ -45,6 +45,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // shaped: 1024 -> 5.67, 768 -> 5.71.
 constexpr int kPartChoices[] = {4096, 3072, 2048, 1536, 1024, 768, 512, 384, 256};
 constexpr int kRampTokens = 64;
+constexpr double kSingleRampTokens = 512.0;  // the single-buffered kernel's (see plan_decode)
 constexpr int kCtasPerSm = 2;
 
 static int device_sms() {
@@ -65,9 +66,9 @@ static int device_sms() {
     return cached[dev];
 }
 
-DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len) {
+DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len,
+                       bool allow_single) {
     (void)bs;
-    (void)kv_dtype;
     DecodePlan p{};
     const int G = Hq / Hkv;
     p.head_chunks = (G + 7) / 8;
@@ -94,6 +95,36 @@ DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int 
         }
     }
     p.max_parts = std::max(1, (max_context_len + p.part_tokens - 1) / p.part_tokens);
+    p.single = false;
+    if (allow_single && p.max_parts > 1 && kv_dtype != PA_KV_FP8) {
+        // Split contexts of bf16 and int8 caches: the single-buffered kernel, three CTAs
+        // per SM.  Its CTAs expose each tile's load latency and rely on the other warps,
+        // so fewer, longer partitions pay: n balanced partitions of the longest context
+        // (as in the multi-token plan) scored by (last-wave fill) x len / (len + 512)
+        // with at least two waves.  Measured on GB300, 70B-shaped decode (8 layers):
+        // 768-token partitions 112.5 us, 1024 110.4, 1600 110.6, 896 121.2, 512 116.1.
+        p.single = true;
+        const double slots3 = (double)device_sms() * 3;
+        const int ctx = std::max(max_context_len, 1);
+        double best = -1.0;
+        int best_len = p.part_tokens;
+        for (int n = 1; n <= (ctx + 255) / 256; ++n) {
+            const int cand = std::min(4096, std::max(256, (int)align_up((size_t)((ctx + n - 1) / n), 64)));
+            const int parts = (ctx + cand - 1) / cand;
+            if (parts != n) continue;  // the same length as a smaller n
+            const double waves = (double)(units * parts) / slots3;
+            if (waves < 2.0 && cand != 256) continue;
+            const double len = (double)std::min(cand, ctx);
+            const double score = waves / std::ceil(waves) * len / (len + kSingleRampTokens);
+            if (score > best + 1e-9) {
+                best = score;
+                best_len = cand;
+            }
+        }
+        p.part_tokens = best_len;
+        p.max_parts = std::max(1, (max_context_len + p.part_tokens - 1) / p.part_tokens);
+        if (p.max_parts == 1) p.single = false;
+    }
     if (p.max_parts == 1) {
         p.ws_acc_off = p.ws_ml_off = p.ws_bytes = 0;
         return p;
@@ -326,6 +357,7 @@ pa_status pa_decode(pa_bf16 *out, const pa_bf16 *query, const void *k_cache,
     a.head_chunks = plan.head_chunks;
     a.part_tokens = plan.part_tokens;
     a.max_parts = plan.max_parts;
+    a.single = plan.single;
     a.max_context_len = max_context_len;
     a.scale_log2 = scale * 1.4426950408889634f;
     launch_decode(a, D, bs, kv_dtype, (cudaStream_t)stream);
@@ -349,7 +381,7 @@ static PrefixPlan plan_prefix(int S, int Hq, int Hkv, int D, int bs, int kv_dtyp
     // max_context_len - max_prefix_len: partitions are sized for that length; longer
     // own ranges (shorter prefixes, sequences in no group) just take more partitions
     const int own_len = std::max(1, max_context_len - max_prefix_len);
-    p.own = plan_decode(S, Hq, Hkv, D, bs, kv_dtype, own_len);
+    p.own = plan_decode(S, Hq, Hkv, D, bs, kv_dtype, own_len, false);
     // short own ranges run next to the grouped prefix kernel, which fills the GPU as
     // well: one partition each (one partial per head for the merge) beats splitting
     // them further (measured: 512-token ranges 48.8 us in one, 52.9 us in 256-token

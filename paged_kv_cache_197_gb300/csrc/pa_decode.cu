@@ -918,15 +918,16 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     // previous layer's merge): it launches while that kernel drains and waits for it
     // before reading
     dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
-    // Split contexts of bf16 and int8 caches take the single-buffered kernel at three
-    // CTAs per SM; unsplit contexts, fp8 caches and the own tokens of a shared-prefix
-    // call the double-buffered one at two.  Measured on GB300 (decode call, us, double
-    // -> single): 70B-shaped bf16 114.1 -> 111.8, int8 522.2 -> 513.7; fp8 513.0 ->
-    // 527.2, 13B-shaped bf16 (no split) 215.8 -> 220.4, shared-prompt call 42.2 -> 43.5.
+    // The plan's choice (DecodePlan::single): split contexts of bf16 and int8 caches on
+    // the single-buffered kernel at three CTAs per SM; unsplit contexts, fp8 caches and
+    // the own tokens of a shared-prefix call on the double-buffered one at two.
+    // Measured on GB300 (decode call, us, double -> single, same partitions): 70B-shaped
+    // bf16 114.1 -> 111.8, int8 522.2 -> 513.7; fp8 513.0 -> 527.2, 13B-shaped bf16 (no
+    // split) 215.8 -> 220.4, shared-prompt call 42.2 -> 43.5.
     constexpr bool kSingleOk = !std::is_same<KV, e4m3_t>::value;
     cudaError_t err;
     if constexpr (kSingleOk) {
-        if (a.max_parts > 1 && !a.start_tokens)
+        if (a.single && !a.start_tokens)
             err = launch_dependent(paged_decode_single_kernel<KV, D, BS, TILE>, grid, dim3(kThreads), 0, stream, a);
         else
             err = launch_dependent(paged_decode_kernel<KV, D, BS, TILE, 0>, grid, dim3(kThreads), 0, stream, a);

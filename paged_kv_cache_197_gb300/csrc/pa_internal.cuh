@@ -25,9 +25,13 @@ struct DecodePlan {
     size_t ws_acc_off;  // byte offsets of the partial outputs and the (max, sum) pairs
     size_t ws_ml_off;
     size_t ws_bytes;    // 0 when max_parts == 1
+    bool single;        // split contexts on the single-buffered kernel (three CTAs per SM)
 };
 
-DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len);
+// allow_single: false where the launch keeps the double-buffered kernel (the own tokens
+// of a shared-prefix call).
+DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int max_context_len,
+                       bool allow_single = true);
 
 // Parameters of the decode and merge kernels.
 struct DecodeArgs {
@@ -48,6 +52,7 @@ struct DecodeArgs {
     float scale_log2;  // softmax scale times log2(e)
     const int32_t *start_tokens;  // nullable [S]: tokens to skip (a shared prefix)
     int partials_only;            // write partial results even for a single partition
+    int single;                   // decode on the single-buffered kernel (DecodePlan::single)
     // Rows mode (multi-token attention of narrow chunks): non-null [S + 1] row ranges
     // of T query rows.  A CTA takes rows_per_cta consecutive new tokens of a sequence
     // (grid x is partition x token group); token i of sequence s (row query_start[s] +

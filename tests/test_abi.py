@@ -93,26 +93,55 @@ def part_tokens(units, max_ctx, slots=304):
     return best_p
 
 
+def single_part_tokens(units, max_ctx, sms=152):
+    """The partition length of a split bf16 or int8 decode, which runs on the
+    single-buffered kernel (three CTAs per SM): n balanced partitions of the longest
+    context scored by (last-wave fill) x len / (len + 512) with >= 2 waves."""
+    import math
+
+    ctx = max(max_ctx, 1)
+    best, best_p = -1.0, None
+    for n in range(1, (ctx + 255) // 256 + 1):
+        cand = min(4096, max(256, -(-(-(-ctx // n)) // 64) * 64))
+        if -(-ctx // cand) != n:
+            continue
+        waves = units * n / (3 * sms)
+        if waves < 2 and cand != 256:
+            continue
+        ln = min(cand, ctx)
+        score = waves / math.ceil(waves) * ln / (ln + 512)
+        if score > best + 1e-9:
+            best, best_p = score, cand
+    return best_p
+
+
 def test_workspace_size(lib):
     """Partition length: no split when the units alone give 6 waves of 2 CTAs per SM (152
     SMs without a GPU) and contexts are <= 4096 tokens; else the best of (last-wave fill)
-    x (len / (len + 64)) among lengths giving >= 3 waves.  The workspace holds (D + 2)
-    fp32 per query head and partition."""
+    x (len / (len + 64)) among lengths giving >= 3 waves.  A split bf16 or int8 decode
+    then runs on the single-buffered kernel with its own partitions
+    (single_part_tokens); fp8 keeps the first.  The workspace holds (D + 2) fp32 per
+    query head and partition."""
     import math
 
     import paged_kv_cache_197_gb300 as pa
 
-    def parts(units, max_ctx, slots=304):
-        return max(1, -(-max_ctx // part_tokens(units, max_ctx, slots)))
+    def parts(units, max_ctx, slots=304, kv=pa.PA_KV_FP8):
+        p = max(1, -(-max_ctx // part_tokens(units, max_ctx, slots)))
+        if p > 1 and kv != pa.PA_KV_FP8:
+            p = max(1, -(-max_ctx // single_part_tokens(units, max_ctx)))
+        return p
 
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
     for S, Hq, Hkv, D, max_ctx in [(64, 40, 40, 128, 2048), (64, 40, 40, 128, 200), (20, 64, 8, 128, 8000), (256, 32, 8, 128, 32768), (2, 8, 2, 64, 1000),
                                    (50, 32, 8, 128, 2512)]:
-        P = parts(S * Hkv * ((Hq // Hkv + 7) // 8), max_ctx)
-        rows = S * Hq * P
-        expect = 0 if P == 1 else up(up(rows * D * 4) + rows * 2 * 4)
-        assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, 16, pa.PA_KV_BF16, max_ctx) == expect
-    assert parts(160, 8000) == 11  # 768-token partitions for the 70B-shaped workload
+        for kv in (pa.PA_KV_BF16, pa.PA_KV_INT8, pa.PA_KV_FP8):
+            P = parts(S * Hkv * ((Hq // Hkv + 7) // 8), max_ctx, kv=kv)
+            rows = S * Hq * P
+            expect = 0 if P == 1 else up(up(rows * D * 4) + rows * 2 * 4)
+            assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, 16, kv, max_ctx) == expect, (S, kv)
+    assert parts(160, 8000) == 11  # fp8: 768-token partitions for the 70B-shaped shape
+    assert parts(160, 8000, kv=pa.PA_KV_BF16) == 8  # bf16: 1024-token partitions
     assert pa.pa_decode_workspace_size(1, 3, 2, 128, 16, 0, 100) == 0  # invalid -> 0
 
 
