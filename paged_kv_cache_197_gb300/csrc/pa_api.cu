@@ -97,14 +97,15 @@ DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int 
     p.max_parts = std::max(1, (max_context_len + p.part_tokens - 1) / p.part_tokens);
     p.single = false;
     if (allow_single && p.max_parts > 1 && kv_dtype != PA_KV_FP8) {
-        // Split contexts of bf16 and int8 caches: the single-buffered kernel, three CTAs
-        // per SM.  Its CTAs expose each tile's load latency and rely on the other warps,
+        // Split contexts of bf16 and int8 caches: the single-buffered kernel, four (bf16)
+        // or three (int8) CTAs per SM.  Its CTAs expose each tile's load latency and rely on the other warps,
         // so fewer, longer partitions pay: n balanced partitions of the longest context
         // (as in the multi-token plan) scored by (last-wave fill) x len / (len + 512)
         // with at least two waves.  Measured on GB300, 70B-shaped decode (8 layers):
         // 768-token partitions 112.5 us, 1024 110.4, 1600 110.6, 896 121.2, 512 116.1.
         p.single = true;
-        const double slots3 = (double)device_sms() * 3;
+        // four CTAs per SM for bf16 caches, three for int8 (paged_decode_single_kernel)
+        const double slots3 = (double)device_sms() * (kv_dtype == PA_KV_BF16 ? 4 : 3);
         const int ctx = std::max(max_context_len, 1);
         double best = -1.0;
         int best_len = p.part_tokens;

@@ -527,7 +527,7 @@ __device__ __forceinline__ void consume_tile(WarpState<KV, D, TILE, NC> &st, Til
 // mode of a multi-token call, NT consecutive new tokens of a sequence per CTA (grid x =
 // partition x token groups), each token a column set with its own causal limit.
 // SINGLE (decode only): one tile register set per warp instead of two (the next
-// tile is not prefetched), 150-165 registers, three CTAs per SM: twelve warps per SM
+// tile is not prefetched), three or four CTAs per SM: twelve or sixteen warps per SM
 // keep loads in flight where eight double-buffered ones did.
 template <typename KV, int D, int BS, int TILE, int NT, bool SINGLE>
 __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
@@ -782,8 +782,10 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
     decode_body<KV, D, BS, TILE, NT, false>(a);
 }
 
+// bf16 (16-token tiles) fits 128 registers: four CTAs per SM; int8 (32-token tiles)
+// three.
 template <typename KV, int D, int BS, int TILE>
-__global__ void __launch_bounds__(kThreads, 3) paged_decode_single_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, sizeof(KV) == 2 ? 4 : 3) paged_decode_single_kernel(const DecodeArgs a) {
     decode_body<KV, D, BS, TILE, 0, true>(a);
 }
 
@@ -919,7 +921,7 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     // before reading
     dim3 grid(a.max_parts, a.Hkv * a.head_chunks, a.S);
     // The plan's choice (DecodePlan::single): split contexts of bf16 and int8 caches on
-    // the single-buffered kernel at three CTAs per SM; unsplit contexts, fp8 caches and
+    // the single-buffered kernel at four (bf16) or three CTAs per SM; unsplit contexts, fp8 caches and
     // the own tokens of a shared-prefix call on the double-buffered one at two.
     // Measured on GB300 (decode call, us, double -> single, same partitions): 70B-shaped
     // bf16 114.1 -> 111.8, int8 522.2 -> 513.7; fp8 513.0 -> 527.2, 13B-shaped bf16 (no

@@ -93,10 +93,11 @@ def part_tokens(units, max_ctx, slots=304):
     return best_p
 
 
-def single_part_tokens(units, max_ctx, sms=152):
+def single_part_tokens(units, max_ctx, sms=152, per_sm=3):
     """The partition length of a split bf16 or int8 decode, which runs on the
-    single-buffered kernel (three CTAs per SM): n balanced partitions of the longest
-    context scored by (last-wave fill) x len / (len + 512) with >= 2 waves."""
+    single-buffered kernel (four CTAs per SM for bf16, three for int8): n balanced
+    partitions of the longest context scored by (last-wave fill) x len / (len + 512)
+    with >= 2 waves."""
     import math
 
     ctx = max(max_ctx, 1)
@@ -105,7 +106,7 @@ def single_part_tokens(units, max_ctx, sms=152):
         cand = min(4096, max(256, -(-(-(-ctx // n)) // 64) * 64))
         if -(-ctx // cand) != n:
             continue
-        waves = units * n / (3 * sms)
+        waves = units * n / (per_sm * sms)
         if waves < 2 and cand != 256:
             continue
         ln = min(cand, ctx)
@@ -129,7 +130,8 @@ def test_workspace_size(lib):
     def parts(units, max_ctx, slots=304, kv=pa.PA_KV_FP8):
         p = max(1, -(-max_ctx // part_tokens(units, max_ctx, slots)))
         if p > 1 and kv != pa.PA_KV_FP8:
-            p = max(1, -(-max_ctx // single_part_tokens(units, max_ctx)))
+            per_sm = 4 if kv == pa.PA_KV_BF16 else 3
+            p = max(1, -(-max_ctx // single_part_tokens(units, max_ctx, per_sm=per_sm)))
         return p
 
     up = lambda x: (x + 255) // 256 * 256  # noqa: E731
@@ -141,7 +143,8 @@ def test_workspace_size(lib):
             expect = 0 if P == 1 else up(up(rows * D * 4) + rows * 2 * 4)
             assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, 16, kv, max_ctx) == expect, (S, kv)
     assert parts(160, 8000) == 11  # fp8: 768-token partitions for the 70B-shaped shape
-    assert parts(160, 8000, kv=pa.PA_KV_BF16) == 8  # bf16: 1024-token partitions
+    assert parts(160, 8000, kv=pa.PA_KV_BF16) == 11  # bf16, four CTAs per SM: 768-token
+    assert parts(160, 8000, kv=pa.PA_KV_INT8) == 8   # int8, three: 1024-token partitions
     assert pa.pa_decode_workspace_size(1, 3, 2, 128, 16, 0, 100) == 0  # invalid -> 0
 
 
