@@ -101,8 +101,10 @@ DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int 
         // or three (int8) CTAs per SM.  Its CTAs expose each tile's load latency and rely on the other warps,
         // so fewer, longer partitions pay: n balanced partitions of the longest context
         // (as in the multi-token plan) scored by (last-wave fill) x len / (len + 512)
-        // with at least two waves.  Measured on GB300, 70B-shaped decode (8 layers):
-        // 768-token partitions 112.5 us, 1024 110.4, 1600 110.6, 896 121.2, 512 116.1.
+        // with at least 1.5 waves.  Measured on GB300, 70B-shaped decode (8 layers,
+        // four CTAs per SM, 608 slots): 1152-token partitions (1.84 waves) 106.6 us,
+        // 768 (2.9) 108.8, 1344 111.9, 512 114.1, 640 115.4, 1024 (2.1 waves) 121.3 --
+        // the order of the score.
         p.single = true;
         // four CTAs per SM for bf16 caches, three for int8 (paged_decode_single_kernel)
         const double slots3 = (double)device_sms() * (kv_dtype == PA_KV_BF16 ? 4 : 3);
@@ -114,7 +116,7 @@ DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int 
             const int parts = (ctx + cand - 1) / cand;
             if (parts != n) continue;  // the same length as a smaller n
             const double waves = (double)(units * parts) / slots3;
-            if (waves < 2.0 && cand != 256) continue;
+            if (waves < 1.5 && cand != 256) continue;
             const double len = (double)std::min(cand, ctx);
             const double score = waves / std::ceil(waves) * len / (len + kSingleRampTokens);
             if (score > best + 1e-9) {

@@ -97,7 +97,7 @@ def single_part_tokens(units, max_ctx, sms=152, per_sm=3):
     """The partition length of a split bf16 or int8 decode, which runs on the
     single-buffered kernel (four CTAs per SM for bf16, three for int8): n balanced
     partitions of the longest context scored by (last-wave fill) x len / (len + 512)
-    with >= 2 waves."""
+    with >= 1.5 waves."""
     import math
 
     ctx = max(max_ctx, 1)
@@ -107,7 +107,7 @@ def single_part_tokens(units, max_ctx, sms=152, per_sm=3):
         if -(-ctx // cand) != n:
             continue
         waves = units * n / (per_sm * sms)
-        if waves < 2 and cand != 256:
+        if waves < 1.5 and cand != 256:
             continue
         ln = min(cand, ctx)
         score = waves / math.ceil(waves) * ln / (ln + 512)
@@ -143,8 +143,8 @@ def test_workspace_size(lib):
             expect = 0 if P == 1 else up(up(rows * D * 4) + rows * 2 * 4)
             assert pa.pa_decode_workspace_size(S, Hq, Hkv, D, 16, kv, max_ctx) == expect, (S, kv)
     assert parts(160, 8000) == 11  # fp8: 768-token partitions for the 70B-shaped shape
-    assert parts(160, 8000, kv=pa.PA_KV_BF16) == 11  # bf16, four CTAs per SM: 768-token
-    assert parts(160, 8000, kv=pa.PA_KV_INT8) == 8   # int8, three: 1024-token partitions
+    assert parts(160, 8000, kv=pa.PA_KV_BF16) == 7  # bf16, four CTAs per SM: 1152-token
+    assert parts(160, 8000, kv=pa.PA_KV_INT8) == 5  # int8, three: 1600-token partitions
     assert pa.pa_decode_workspace_size(1, 3, 2, 128, 16, 0, 100) == 0  # invalid -> 0
 
 
