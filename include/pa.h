@@ -276,10 +276,11 @@ pa_status pa_decode_shared_prefix(pa_bf16 *out, const pa_bf16 *query, const void
  * arguments as pa_decode.  With head_dim 128 and max_query_len * Hq / Hkv >= 64
  * (prefill-shaped calls), 8-bit entries of the attended blocks are first dequantised
  * into the workspace's pool as bf16 (code x scale, rounded once) and the products are bf16
- * with fp32 accumulation, as for a bf16 cache.  Otherwise the codes pass through
- * shared memory as exact fp16 values and the query rows as fp16 scaled by a power of
- * two per row; the products are fp16 with fp32 accumulation, the key scale multiplies
- * the score and the value scale the softmax weight in fp32 (no range limit).
+ * with fp32 accumulation, as for a bf16 cache.  Otherwise the codes are converted to
+ * exact fp16 values (in registers for chunks of at most 8 new tokens, through shared
+ * memory for longer ones) and the query rows to fp16 scaled by a power of two; the
+ * products are fp16 with fp32 accumulation, the key scale multiplies the score and the
+ * value scale the softmax weight in fp32 (no range limit).
  */
 size_t pa_multi_token_workspace_size(int S, int T, int Hq, int Hkv, int D, int bs, int kv_dtype,
                                      int max_context_len, int max_query_len);
