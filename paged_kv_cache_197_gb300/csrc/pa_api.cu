@@ -106,8 +106,7 @@ DecodePlan plan_decode(int S, int Hq, int Hkv, int D, int bs, int kv_dtype, int 
         // 768 (2.9) 108.8, 1344 111.9, 512 114.1, 640 115.4, 1024 (2.1 waves) 121.3 --
         // the order of the score.
         p.single = true;
-        // four CTAs per SM for bf16 caches, three for int8 (paged_decode_single_kernel)
-        const double slots3 = (double)device_sms() * (kv_dtype == PA_KV_BF16 ? 4 : 3);
+        const double slots3 = (double)device_sms() * decode_single_ctas_per_sm(kv_dtype);
         const int ctx = std::max(max_context_len, 1);
         double best = -1.0;
         int best_len = p.part_tokens;

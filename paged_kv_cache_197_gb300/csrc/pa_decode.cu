@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
 }
 
 // bf16 (16-token tiles) fits 128 registers: four CTAs per SM; int8 (32-token tiles)
-// three.
+// three (decode_single_ctas_per_sm, which the partition plan counts).
 template <typename KV, int D, int BS, int TILE>
 __global__ void __launch_bounds__(kThreads, sizeof(KV) == 2 ? 4 : 3) paged_decode_single_kernel(const DecodeArgs a) {
     decode_body<KV, D, BS, TILE, 0, true>(a);
@@ -987,6 +987,8 @@ cudaError_t launch_decode(const DecodeArgs &a, int D, int bs, int kv_dtype, cuda
 }
 
 int decode_rows_per_cta(int max_query_len) { return max_query_len >= 2 ? 2 : 1; }
+
+int decode_single_ctas_per_sm(int kv_dtype) { return kv_dtype == PA_KV_BF16 ? 4 : 3; }
 
 cudaError_t launch_decode_rows(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream) {
     if (!a.query_start || a.Lq <= 0 || a.start_tokens || a.partials_only || kv_dtype == PA_KV_BF16 ||

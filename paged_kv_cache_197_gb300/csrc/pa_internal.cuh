@@ -122,6 +122,8 @@ bool multi_per_token_eligible(int D, int kv_dtype, int G, int max_query_len);
 // launch); the caller launches the merge.  decode_rows_per_cta: the new tokens one
 // CTA takes for a call of max_query_len new tokens per sequence.
 int decode_rows_per_cta(int max_query_len);
+// CTAs per SM of the single-buffered decode kernel (its launch bounds) for a cache type.
+int decode_single_ctas_per_sm(int kv_dtype);
 cudaError_t launch_decode_rows(const DecodeArgs &a, int D, int bs, int kv_dtype, cudaStream_t stream);
 // Whether multi-token attention of this shape runs on the tcgen05 kernel (8-bit caches
 // after the dequantising pass below) rather than the mma.sync one; plan and launch both
@@ -130,6 +132,7 @@ bool multi_tc_eligible(int D, int kv_dtype, int G, int max_query_len);
 cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream);  // bf16 caches
 // The tcgen05 kernel in group mode (the caller merges the partials).
 cudaError_t launch_multi_tc_groups(const MultiArgs &a, int bs, cudaStream_t stream);
+int multi_tc_rows();  // (token or member, head) columns per CTA of the tcgen05 kernel
 // 8-bit caches, prefill-shaped calls: the attended blocks dequantised into a bf16 pool
 // of `cap` blocks, sequences packed back to back (offsets off[S + 1]), and the table
 // [S][Mq] of pool slots, all in the workspace.

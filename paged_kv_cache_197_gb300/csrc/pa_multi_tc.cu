@@ -838,6 +838,8 @@ cudaError_t launch_multi_tc(const MultiArgs &a, int bs, cudaStream_t stream) {
     return bs == 16 ? launch_tc_typed<16>(a, true, stream) : launch_tc_typed<32>(a, true, stream);
 }
 
+int multi_tc_rows() { return kTcRows; }
+
 cudaError_t launch_multi_tc_groups(const MultiArgs &a, int bs, cudaStream_t stream) {
     if (!a.group_prefix || !a.seq_group || !a.ws_acc || !a.ws_ml) return cudaErrorInvalidValue;
     return bs == 16 ? launch_tc_typed<16>(a, false, stream) : launch_tc_typed<32>(a, false, stream);

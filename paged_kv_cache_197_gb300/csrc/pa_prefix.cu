@@ -561,6 +561,8 @@ cudaError_t side_stream(int dev, cudaStream_t caller, SideStream *&out) {
 // leaving the same partials as the grouped kernel.
 template <int BS>
 cudaError_t launch_prefix_tc(const DecodeArgs &a, const PrefixArgs &p, cudaStream_t stream) {
+    // p.CB counts blocks of kColsPerCta columns; the tcgen05 kernel takes as many per CTA
+    if (multi_tc_rows() != kColsPerCta) return cudaErrorInvalidValue;
     MultiArgs m{};
     m.out = a.out;
     m.q = a.q;
