@@ -70,6 +70,16 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
+    # current sources: decode (single-buffered kernel for split bf16 / int8, rows mode
+    # for narrow 8-bit chunks) and the tcgen05 kernel (P V issued by a row thread)
+    ("gqa70b", "14b3764a27efcdbc"): 655759104 + 4136704,
+    ("mha13b", "14b3764a27efcdbc"): 1392701184 + 3305216,
+    ("int8", "14b3764a27efcdbc"): 3144262400 + 5417984,
+    ("fp8", "14b3764a27efcdbc"): 3144268800 + 5428992,
+    ("verify70b_fp8", "14b3764a27efcdbc"): 339384320 + 5014272,
+    ("prefill8b", "3048c7cf102e7a47"): 83948288 + 3426560,
+    ("verify70b", "3048c7cf102e7a47"): 656803584 + 13206272,
+    ("prefill8b_fp8", "3048c7cf102e7a47"): (5632 + 0) + (34648576 + 4945408) + (83977216 + 222464),
     # bf16 single-buffered kernel at four CTAs per SM (70B-shaped: 7 x 1152, retaken
     # after the plan change)
     ("gqa70b", "babc3b94b95e8207"): 655759104 + 4461056,
