@@ -70,81 +70,18 @@ L2_BYTES = 126 * 1024 * 1024
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant kernel, from
 # an ncu capture of the kernel source with this sha256 prefix (null once it changes).
 NCU_TRAFFIC = {
-    # current sources: decode (single-buffered kernel for split bf16 / int8, rows mode
-    # for narrow 8-bit chunks) and the tcgen05 kernel (P V issued by a row thread)
+    # decode: the single-buffered kernel for split bf16 / int8 contexts, the
+    # double-buffered one for the rest, rows mode for narrow 8-bit chunks
     ("gqa70b", "14b3764a27efcdbc"): 655759104 + 4136704,
     ("mha13b", "14b3764a27efcdbc"): 1392701184 + 3305216,
     ("int8", "14b3764a27efcdbc"): 3144262400 + 5417984,
     ("fp8", "14b3764a27efcdbc"): 3144268800 + 5428992,
     ("verify70b_fp8", "14b3764a27efcdbc"): 339384320 + 5014272,
+    # the tcgen05 kernel (P V issued by a row thread); prefill8b_fp8: every kernel of the
+    # call (pool offsets, dequantising pass, tcgen05 kernel), each captured cold
     ("prefill8b", "3048c7cf102e7a47"): 83948288 + 3426560,
     ("verify70b", "3048c7cf102e7a47"): 656803584 + 13206272,
     ("prefill8b_fp8", "3048c7cf102e7a47"): (5632 + 0) + (34648576 + 4945408) + (83977216 + 222464),
-    # bf16 single-buffered kernel at four CTAs per SM (70B-shaped: 7 x 1152, retaken
-    # after the plan change)
-    ("gqa70b", "babc3b94b95e8207"): 655759104 + 4461056,
-    ("mha13b", "babc3b94b95e8207"): 1392728064 + 3357952,
-    ("int8", "babc3b94b95e8207"): 3144418816 + 5426176,
-    ("fp8", "babc3b94b95e8207"): 3144262400 + 5445376,
-    ("verify70b_fp8", "babc3b94b95e8207"): 339334912 + 4692992,
-    # the single-buffered kernel with its own partition plan (70B-shaped: 8 x 1024)
-    ("gqa70b", "0df180f3524b8e7f"): 655757056 + 4864000,
-    ("mha13b", "0df180f3524b8e7f"): 1392701952 + 3723008,
-    ("int8", "0df180f3524b8e7f"): 3144269312 + 5220096,
-    ("fp8", "0df180f3524b8e7f"): 3144578304 + 5466368,
-    ("verify70b_fp8", "0df180f3524b8e7f"): 339324672 + 4783872,
-    # split bf16 / int8 contexts on the single-buffered kernel, three CTAs per SM
-    ("gqa70b", "095e29f621331af4"): 655772416 + 4880640,
-    ("mha13b", "095e29f621331af4"): 1392701440 + 3302144,
-    ("int8", "095e29f621331af4"): 3144270848 + 5010688,
-    ("fp8", "095e29f621331af4"): 3144264192 + 5480192,
-    ("verify70b_fp8", "095e29f621331af4"): 339326464 + 4800768,
-    # + rescale slack of 2^8 and fp8 key words converted in one block
-    ("gqa70b", "834753d87ef8f64f"): 655777280 + 5179392,
-    ("mha13b", "834753d87ef8f64f"): 1392741632 + 3417856,
-    ("int8", "834753d87ef8f64f"): 3144293632 + 5563136,
-    ("fp8", "834753d87ef8f64f"): 3144498176 + 5451520,
-    ("verify70b_fp8", "834753d87ef8f64f"): 339325952 + 4805376,
-    # fewer instructions per tile (fused score scale, unmasked full tiles, a vote for
-    # the value exponent)
-    ("gqa70b", "96b88d48f371f5fa"): 655776768 + 4920320,
-    ("mha13b", "96b88d48f371f5fa"): 1392700928 + 3355904,
-    ("int8", "96b88d48f371f5fa"): 3144285696 + 5479168,
-    ("fp8", "96b88d48f371f5fa"): 3144284416 + 5479168,
-    ("verify70b_fp8", "96b88d48f371f5fa"): 339326976 + 4881664,
-    # column sets (decode: one) and the one-round-trip merge
-    ("gqa70b", "80b6053b89d02567"): 655763968 + 4635904,
-    ("mha13b", "80b6053b89d02567"): 1392701440 + 3301632,
-    ("int8", "80b6053b89d02567"): 3144270848 + 5432320,
-    ("fp8", "80b6053b89d02567"): 3144286464 + 5454592,
-    # the decode kernel launched as a programmatic dependent (griddepcontrol.wait first)
-    ("gqa70b", "b150daeb73620bab"): 655764736 + 5164800,
-    ("mha13b", "b150daeb73620bab"): 1392701696 + 3443712,
-    ("int8", "b150daeb73620bab"): 3144388864 + 5860352,
-    ("fp8", "b150daeb73620bab"): 3144270848 + 5449984,
-    ("mha13b", "0a92d8beb0508d47"): 1392700672 + 3298304,
-    ("gqa70b", "0a92d8beb0508d47"): 655764224 + 5198848,
-    ("int8", "0a92d8beb0508d47"): 3144346368 + 5461760,
-    ("fp8", "0a92d8beb0508d47"): 3144265472 + 5437952,
-    ("prefix", "0a92d8beb0508d47"): 72100608 + 1082624,
-    # five 1600-token partitions (balanced partition plan); their partials are the writes
-    ("verify70b", "91323db2ddaade17"): 656797696 + 13285120,
-    ("prefill8b", "91323db2ddaade17"): 83940352 + 3092992,
-    ("verify70b_fp8", "5b771ca2846ad7f5"): 340236544 + 13805056,
-    # the decode kernel in rows mode (two new tokens per CTA), 2048-token partitions
-    ("verify70b_fp8", "80b6053b89d02567"): 339351296 + 5274368,
-    # the tcgen05 kernel reading the dequantised bf16 pool (the pass before it reads the
-    # 8-bit blocks once)
-    ("prefill8b_fp8", "91323db2ddaade17"): 83939328 + 3236096,
-    # P V issued by row thread 0; prefill8b_fp8: every kernel of the call
-    ("verify70b", "491c378341fcbbee"): 656803584 + 13247744,
-    ("prefill8b", "491c378341fcbbee"): 83943680 + 3076096,
-    ("prefill8b_fp8", "491c378341fcbbee"): (5376 + 0) + (34652672 + 5374720) + (83958016 + 54272),
-    # current tcgen05 source; prefill8b_fp8: every kernel of the call (pool offsets,
-    # dequantising pass, tcgen05 kernel), each captured cold
-    ("verify70b", "10421af6d5a0669e"): 656793088 + 13301504,
-    ("prefill8b", "10421af6d5a0669e"): 83941376 + 3069696,
-    ("prefill8b_fp8", "10421af6d5a0669e"): (5632 + 0) + (34645760 + 5123072) + (83940352 + 76544),
 }
 
 
