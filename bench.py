@@ -77,11 +77,12 @@ NCU_TRAFFIC = {
     ("int8", "14b3764a27efcdbc"): 3144262400 + 5417984,
     ("fp8", "14b3764a27efcdbc"): 3144268800 + 5428992,
     ("verify70b_fp8", "14b3764a27efcdbc"): 339384320 + 5014272,
-    # the tcgen05 kernel (P V issued by a row thread); prefill8b_fp8: every kernel of the
-    # call (pool offsets, dequantising pass, tcgen05 kernel), each captured cold
-    ("prefill8b", "3048c7cf102e7a47"): 83948288 + 3426560,
-    ("verify70b", "3048c7cf102e7a47"): 656803584 + 13206272,
-    ("prefill8b_fp8", "3048c7cf102e7a47"): (5632 + 0) + (34648576 + 4945408) + (83977216 + 222464),
+    # the tcgen05 kernel (P V issued by a row thread, padding row warps only keeping step);
+    # prefill8b_fp8: every kernel of the call (pool offsets, dequantising pass, tcgen05
+    # kernel), each captured cold
+    ("prefill8b", "2dc02eb0952f1757"): 83980288 + 3249408,
+    ("verify70b", "2dc02eb0952f1757"): 656806912 + 13232640,
+    ("prefill8b_fp8", "2dc02eb0952f1757"): (5376 + 0) + (34649856 + 5105920) + (83948544 + 214784),
 }
 
 

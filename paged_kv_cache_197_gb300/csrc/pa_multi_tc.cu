@@ -27,7 +27,8 @@
 //     tile's max exceeds it by more than 2^8 in the exp2 domain; O is then rescaled in
 //     tensor memory) and sum, write P in bf16 to shared memory in the swizzled K-major
 //     layout, and finally write the output row or its (max, sum, output) partial for
-//     the merge kernel shared with the mma.sync path.
+//     the merge kernel shared with the mma.sync path; a warp whose 32 rows are all
+//     padding (narrow chunks) only keeps step with the barriers.
 // Tensor memory: S in columns 0-63, Q (bf16 pairs) 64-127, O 128-255.
 // Every wait is bounded (PA_FLAG_TIMEOUT when one gives up; the outputs are then not
 // written).
@@ -496,8 +497,42 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         int pv_issued = 0;  // row thread 0: P V products issued
+        // A row warp none of whose 32 columns is real (a chunk of fewer than 97 columns
+        // per kv head, e.g. draft verification) keeps only its part of the barrier
+        // protocol -- it arrives on sfree and pfull in step, after the waits that keep
+        // each arrival in its phase, and zeroes its share of the last tile's stale V
+        // rows -- instead of reading S and writing P for rows no one reads.  Group mode
+        // keeps every warp busy: there the prefix runs beside the own-token decode, and
+        // a faster prefix only takes bandwidth from it.
+        const bool idle_warp = !grouped && col0 + warp * 32 >= ncols;
 #pragma unroll 1
-        for (int j = 0; j < ntile; ++j) {
+        for (int j = 0; idle_warp && j < ntile; ++j) {
+            const int st = j % kTcStages;
+            ok = mbar_wait(tc_smem(&sh.sfull), j & 1);
+            if (__any_sync(0xffffffffu, !ok || sh.abort != 0)) { ok = false; break; }
+            mbar_arrive(tc_smem(&sh.sfree));
+            if (j > 0) {
+                ok = mbar_wait(tc_smem(&sh.odone), (j - 1) & 1);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+            }
+            const int k0 = tok_begin + j * kTcTile;
+            const int r_lo = tok_end - k0;
+            if (j == ntile - 1 && r_lo < kTcTile && tok_end % BS != 0) {
+                ok = mbar_wait(tc_smem(&sh.vfull[st]), (j / kTcStages) & 1);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                const int r_hi = min(kTcTile, (tok_end + BS - 1) / BS * BS - k0);
+                unsigned char *vst = base + kOffV + st * kTcTileBytes;
+                for (int i = tid; i < (r_hi - r_lo) * 16; i += kTcRows) {
+                    const int r = r_lo + i / 16, ch = i % 16;
+                    *reinterpret_cast<uint4 *>(vst + (ch >> 3) * kTcAtom + (r >> 3) * 1024 + (r & 7) * 128 +
+                                               (((ch & 7) ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            mbar_arrive(tc_smem(&sh.pfull));
+        }
+#pragma unroll 1
+        for (int j = 0; !idle_warp && j < ntile; ++j) {
             const int st = j % kTcStages;
             ok = mbar_wait(tc_smem(&sh.sfull), j & 1);
             if (__any_sync(0xffffffffu, !ok || sh.abort != 0)) { ok = false; break; }
@@ -618,7 +653,7 @@ multi_tc_kernel(const __grid_constant__ MultiArgs a, const __grid_constant__ CUt
         }
         tc_fence_after();
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        if (__all_sync(0xffffffffu, ok)) {
+        if (__all_sync(0xffffffffu, ok) && !idle_warp) {
             // ---- epilogue: this thread's output row (the tensor-memory loads are
             // warp-wide; rows with nothing to write discard them)
             const bool write = has && tok_begin <= lim;
